@@ -1,0 +1,115 @@
+"""Seeded synthetic inputs for ring attention, shared by the tests, the bench
+and the oracle's callers.
+
+This module draws random numbers and nothing else: it holds none of the
+attention arithmetic, so the CUDA path and the fp64 oracle can both be fed
+from it without sharing any of the method.
+
+Recipe (the same for every workload):
+  * one ``torch.Generator('cpu')`` seeded with ``seed`` draws q, k, v and then
+    (when asked) dO, in that order, as fp32 standard normals;
+  * each tensor is then cast to the workload's dtype (bf16 rounds to nearest
+    even), so the oracle reads exactly the values the GPU reads;
+  * packed-document lengths come from a second generator seeded ``seed + 1``:
+    integers uniform in [lo, hi] inclusive, drawn one at a time until their sum
+    reaches the token total, the last one truncated so the sum is exact.
+
+The named workloads mirror the shapes the pages talk about: Llama-3-8B
+attention heads (32 query / 8 key-value heads of dimension 128, axolotl
+"Sequence Parallelism" page, "Example") at 8K to 64K tokens, with context
+parallel degrees 4 and 8 ("Configuration"), and packed samples whose shards
+split documents mid-sample ("Sample Packing with Sequence Parallelism").
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+CONTIGUOUS = 0
+ZIGZAG = 1
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    total_tokens: int
+    hq: int
+    hkv: int
+    head_dim: int
+    num_shards: int
+    layout: int          # CONTIGUOUS or ZIGZAG
+    causal: bool
+    dtype: str           # "fp32" or "bf16"
+    varlen: bool = False  # packed documents, lengths uniform in [doc_lo, doc_hi]
+    doc_lo: int = 512
+    doc_hi: int = 8192
+    backward: bool = False
+    heads_k_stride: int = 1
+
+
+WORKLOADS = {
+    w.name: w for w in [
+        Workload("tiny_fp32_noncausal_t256", 256, 2, 2, 64, 2, CONTIGUOUS,
+                 False, "fp32"),
+        Workload("causal_mha_t8192_p4_zigzag", 8192, 8, 8, 128, 4, ZIGZAG,
+                 True, "bf16"),
+        Workload("causal_gqa_t32768_p8_zigzag", 32768, 32, 8, 128, 8, ZIGZAG,
+                 True, "bf16"),
+        Workload("varlen_causal_gqa_t65536_p8_contiguous", 65536, 32, 8, 128, 8,
+                 CONTIGUOUS, True, "bf16", varlen=True),
+        Workload("causal_gqa_fwdbwd_t65536_p8_zigzag", 65536, 32, 8, 128, 8,
+                 ZIGZAG, True, "bf16", backward=True),
+    ]
+}
+
+
+def torch_dtype(name: str) -> torch.dtype:
+    return {"fp32": torch.float32, "bf16": torch.bfloat16}[name]
+
+
+def doc_lengths(total: int, lo: int, hi: int, seed: int) -> list[int]:
+    """Document lengths uniform in [lo, hi], drawn until they cover ``total``;
+    the last is truncated so they sum to ``total`` exactly."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    out: list[int] = []
+    acc = 0
+    while acc < total:
+        n = int(torch.randint(lo, hi + 1, (1,), generator=g).item())
+        n = min(n, total - acc)
+        out.append(n)
+        acc += n
+    return out
+
+
+def cu_seqlens_from_lengths(lengths) -> torch.Tensor:
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + int(n))
+    return torch.tensor(cu, dtype=torch.int32)
+
+
+def make_qkv(total_tokens: int, hq: int, hkv: int, head_dim: int, dtype: str,
+             seed: int, with_dout: bool = False):
+    """q [T,Hq,D], k [T,Hkv,D], v [T,Hkv,D] (and dO [T,Hq,D]) on the CPU."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    dt = torch_dtype(dtype)
+    q = torch.randn(total_tokens, hq, head_dim, generator=g).to(dt)
+    k = torch.randn(total_tokens, hkv, head_dim, generator=g).to(dt)
+    v = torch.randn(total_tokens, hkv, head_dim, generator=g).to(dt)
+    if not with_dout:
+        return q, k, v
+    do = torch.randn(total_tokens, hq, head_dim, generator=g).to(dt)
+    return q, k, v, do
+
+
+def make_inputs(w: Workload, seed: int = 0, with_dout: bool | None = None):
+    """All inputs of a workload: dict with q, k, v, (dout), cu_seqlens (or None)."""
+    wd = w.backward if with_dout is None else with_dout
+    t = make_qkv(w.total_tokens, w.hq, w.hkv, w.head_dim, w.dtype, seed, wd)
+    out = {"q": t[0], "k": t[1], "v": t[2], "dout": t[3] if wd else None,
+           "cu_seqlens": None}
+    if w.varlen:
+        out["cu_seqlens"] = cu_seqlens_from_lengths(
+            doc_lengths(w.total_tokens, w.doc_lo, w.doc_hi, seed + 1))
+    return out
