@@ -1,0 +1,270 @@
+"""B300-native ring attention: Python binding of ``libringattn.so``.
+
+Argument marshalling only.  Every step of the computation runs in the CUDA
+library (``csrc/``), reached through its C ABI (``include/ringattn.h``);
+torch tensors are only the owners of device memory and ``torch.cuda``
+streams the ordering.  If the library has not been built the import of a
+compute function raises: there is no CPU fallback.
+
+Entry points (same names as the C ABI):
+    ringattn_fwd, ringattn_fwd_stepwise, ringattn_bwd, attn_lse_merge,
+    ringattn_get_status, plan_fwd (host-only work-list introspection).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+CONTIGUOUS = 0
+ZIGZAG = 1
+RA_BF16 = 0
+RA_FP32 = 1
+
+STATUS = {
+    0: "RA_OK", -1: "RA_ERR_INVALID_ARG", -2: "RA_ERR_NOT_DIVISIBLE",
+    -3: "RA_ERR_UNSUPPORTED", -4: "RA_ERR_CUDA", -5: "RA_ERR_TIMEOUT",
+    -6: "RA_ERR_WORKSPACE",
+}
+PLAN_ITEM_FIELDS = 16
+PLAN_SEG_FIELDS = 4
+ITEM_COLUMNS = ("q0_a", "q0_b", "qlen_a", "qlen_b", "head_a", "head_b", "seg_begin",
+                "seg_count", "rank", "cost", "mask_lo_a", "mask_lo_b", "mask_hi_a",
+                "mask_hi_b", "pass", "pad")
+SEG_COLUMNS = ("k0", "k1", "step", "src")
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libringattn.so")
+_lib = None
+
+
+class RingAttnError(RuntimeError):
+    def __init__(self, func: str, code: int):
+        self.code = code
+        super().__init__(f"{func} failed: {STATUS.get(code, code)}")
+
+
+class ra_dims(ctypes.Structure):
+    _fields_ = [("total_tokens", ctypes.c_int), ("num_seqs", ctypes.c_int),
+                ("hq", ctypes.c_int), ("hkv", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("heads_k_stride", ctypes.c_int)]
+
+
+_vp = ctypes.c_void_p
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_ip = ctypes.POINTER(ctypes.c_int)
+
+
+def library():
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m context_long_sequence_fwd_b300.build` (nvcc, sm_103a)")
+        lib = ctypes.CDLL(LIB_PATH)
+        lib.ringattn_fwd.argtypes = [_vp, _vp, _vp, _i32p, ra_dims, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, _vp, _vp, _vp]
+        lib.ringattn_fwd_stepwise.argtypes = [_vp, _vp, _vp, _i32p, ra_dims, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, _vp, _vp, _vp,
+                                              ctypes.c_size_t, _vp]
+        lib.ringattn_fwd_stepwise_workspace_size.argtypes = [ra_dims]
+        lib.ringattn_fwd_stepwise_workspace_size.restype = ctypes.c_size_t
+        lib.ringattn_bwd_workspace_size.argtypes = [ra_dims]
+        lib.ringattn_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.ringattn_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32p, ra_dims, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp,
+                                     ctypes.c_size_t, _vp]
+        lib.attn_lse_merge.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, _vp]
+        lib.ringattn_get_status.argtypes = [_vp]
+        lib.ringattn_status_string.argtypes = [ctypes.c_int]
+        lib.ringattn_status_string.restype = ctypes.c_char_p
+        lib.ringattn_version.restype = ctypes.c_int
+        lib.ringattn_plan_fwd.argtypes = [_i32p, ra_dims, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, _i32p, ctypes.c_int, _i32p, ctypes.c_int,
+                                          _ip, _ip]
+        for fn in ("ringattn_fwd", "ringattn_fwd_stepwise", "ringattn_bwd", "attn_lse_merge",
+                   "ringattn_get_status", "ringattn_plan_fwd"):
+            getattr(lib, fn).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _check(func: str, code: int):
+    if code != 0:
+        raise RingAttnError(func, code)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return RA_BF16
+    if t.dtype == torch.float32:
+        return RA_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream))
+
+
+def _cu_host(cu_seqlens):
+    """cu_seqlens as a host int32 array (the library copies what it needs)."""
+    if cu_seqlens is None:
+        return None, 0, None
+    if hasattr(cu_seqlens, "detach"):
+        arr = cu_seqlens.detach().to("cpu").numpy()
+    else:
+        arr = np.asarray(cu_seqlens)
+    arr = np.ascontiguousarray(arr, dtype=np.int32)
+    return arr.ctypes.data_as(_i32p), arr.size - 1, arr
+
+
+def make_dims(q, k, num_seqs=0, heads_k_stride=1) -> ra_dims:
+    T, hq, d = q.shape
+    return ra_dims(T, num_seqs, hq, k.shape[1], d, _dtype_code(q), heads_k_stride)
+
+
+def _need(t, name, shape=None, dtype=None):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+
+
+def _check_qkv(q, k, v):
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n)
+    if k.shape != v.shape or q.shape[0] != k.shape[0] or q.shape[2] != k.shape[2]:
+        raise ValueError("q [T,Hq,D], k and v [T,Hkv,D] expected")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise ValueError("q, k, v must share a dtype")
+
+
+def ringattn_fwd(q, k, v, cu_seqlens=None, num_shards=1, shard_layout=CONTIGUOUS, causal=True,
+                 out=None, lse=None, stream=None, heads_k_stride=1):
+    """Fused ring-attention forward; returns (out [T,Hq,D], lse fp32 [Hq,T])."""
+    import torch
+    _check_qkv(q, k, v)
+    T, hq, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(hq, T, dtype=torch.float32, device=q.device)
+    _need(out, "out", q.shape, q.dtype)
+    _need(lse, "lse", (hq, T), torch.float32)
+    cu_p, nseq, _keep = _cu_host(cu_seqlens)
+    dims = make_dims(q, k, nseq, heads_k_stride)
+    _check("ringattn_fwd", library().ringattn_fwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), cu_p, dims, int(num_shards),
+        int(shard_layout), int(bool(causal)), out.data_ptr(), lse.data_ptr(), _stream(stream)))
+    return out, lse
+
+
+def fwd_stepwise_workspace_size(q, k, heads_k_stride=1) -> int:
+    return int(library().ringattn_fwd_stepwise_workspace_size(make_dims(q, k, 0, heads_k_stride)))
+
+
+def ringattn_fwd_stepwise(q, k, v, cu_seqlens=None, num_shards=1, shard_layout=CONTIGUOUS,
+                          causal=True, out=None, lse=None, workspace=None, stream=None,
+                          heads_k_stride=1):
+    """Ring forward as one launch per ring step plus a log-sum-exp merge."""
+    import torch
+    _check_qkv(q, k, v)
+    T, hq, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(hq, T, dtype=torch.float32, device=q.device)
+    _need(out, "out", q.shape, q.dtype)
+    _need(lse, "lse", (hq, T), torch.float32)
+    need = fwd_stepwise_workspace_size(q, k, heads_k_stride)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    cu_p, nseq, _keep = _cu_host(cu_seqlens)
+    dims = make_dims(q, k, nseq, heads_k_stride)
+    _check("ringattn_fwd_stepwise", library().ringattn_fwd_stepwise(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), cu_p, dims, int(num_shards), int(shard_layout),
+        int(bool(causal)), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out, lse
+
+
+def bwd_workspace_size(q, k, heads_k_stride=1) -> int:
+    return int(library().ringattn_bwd_workspace_size(make_dims(q, k, 0, heads_k_stride)))
+
+
+def ringattn_bwd(q, k, v, out, lse, dout, cu_seqlens=None, num_shards=1,
+                 shard_layout=CONTIGUOUS, causal=True, dq=None, dk=None, dv=None,
+                 workspace=None, stream=None, heads_k_stride=1):
+    """Ring-attention backward; returns (dq, dk, dv)."""
+    import torch
+    _check_qkv(q, k, v)
+    T, hq, d = q.shape
+    _need(out, "out", q.shape, q.dtype)
+    _need(dout, "dout", q.shape, q.dtype)
+    _need(lse, "lse", (hq, T), torch.float32)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _need(dq, "dq", q.shape, q.dtype)
+    _need(dk, "dk", k.shape, k.dtype)
+    _need(dv, "dv", v.shape, v.dtype)
+    need = bwd_workspace_size(q, k, heads_k_stride)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    cu_p, nseq, _keep = _cu_host(cu_seqlens)
+    dims = make_dims(q, k, nseq, heads_k_stride)
+    _check("ringattn_bwd", library().ringattn_bwd(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+        dout.data_ptr(), cu_p, dims, int(num_shards), int(shard_layout), int(bool(causal)),
+        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return dq, dk, dv
+
+
+def attn_lse_merge(o_a, lse_a, o_b, lse_b, stream=None):
+    """In-place log-sum-exp merge of (o_b, lse_b) into (o_a, lse_a)."""
+    import torch
+    _need(o_a, "o_a")
+    _need(o_b, "o_b", o_a.shape, o_a.dtype)
+    rows, heads, d = o_a.shape
+    _need(lse_a, "lse_a", (heads, rows), torch.float32)
+    _need(lse_b, "lse_b", (heads, rows), torch.float32)
+    _check("attn_lse_merge", library().attn_lse_merge(
+        o_a.data_ptr(), lse_a.data_ptr(), o_b.data_ptr(), lse_b.data_ptr(), rows, heads, d,
+        _dtype_code(o_a), _stream(stream)))
+    return o_a, lse_a
+
+
+def ringattn_get_status(stream=None) -> int:
+    """Synchronises the stream; returns and clears the kernel-side error word."""
+    return int(library().ringattn_get_status(_stream(stream)))
+
+
+def plan_fwd(total_tokens, hq, hkv, num_shards, shard_layout, causal, cu_seqlens=None,
+             heads_k_stride=1):
+    """Host-only: the forward work list as (items [n,16], segments [m,4]) int32 arrays."""
+    cu_p, nseq, _keep = _cu_host(cu_seqlens)
+    dims = ra_dims(total_tokens, nseq, hq, hkv, 64, RA_FP32, heads_k_stride)
+    ni, ns = ctypes.c_int(0), ctypes.c_int(0)
+    lib = library()
+    code = lib.ringattn_plan_fwd(cu_p, dims, num_shards, shard_layout, int(bool(causal)), None, 0,
+                                 None, 0, ctypes.byref(ni), ctypes.byref(ns))
+    if code not in (0, -6):
+        raise RingAttnError("ringattn_plan_fwd", code)
+    items = np.zeros((max(ni.value, 1), PLAN_ITEM_FIELDS), np.int32)
+    segs = np.zeros((max(ns.value, 1), PLAN_SEG_FIELDS), np.int32)
+    _check("ringattn_plan_fwd", lib.ringattn_plan_fwd(
+        cu_p, dims, num_shards, shard_layout, int(bool(causal)), items.ctypes.data_as(_i32p),
+        items.shape[0], segs.ctypes.data_as(_i32p), segs.shape[0], ctypes.byref(ni),
+        ctypes.byref(ns)))
+    return items[:ni.value], segs[:ns.value]

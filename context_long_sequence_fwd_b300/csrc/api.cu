@@ -1,0 +1,426 @@
+// C ABI of the ring-attention library: argument checks, the per-problem plan
+// cache, tensor-map encoding and kernel launches.  See include/ringattn.h for
+// the contract of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <list>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "launch.h"
+#include "planner.h"
+#include "ringattn.h"
+
+namespace ra {
+
+// First kernel-side error since the last ringattn_get_status (0 = none).
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kMaxCachedPlans = 32;
+
+struct DeviceState {
+  bool ready = false;
+  ra_status why = RA_OK;
+  int* status = nullptr;  // device address of g_status_word
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+struct CachedPlan {
+  int dev = -1;
+  PlanInput key;
+  Plan plan;
+  void* buf = nullptr;  // items | segments | cu on the device
+  PlanItem* items = nullptr;
+  PlanSegment* segs = nullptr;
+  int32_t* cu = nullptr;
+  cudaEvent_t last_use = nullptr;
+};
+std::list<CachedPlan> g_plans;  // most recently used first
+
+bool same_key(const PlanInput& a, const PlanInput& b) {
+  return a.T == b.T && a.hq == b.hq && a.hkv == b.hkv && a.num_shards == b.num_shards &&
+         a.layout == b.layout && a.causal == b.causal && a.heads_k_stride == b.heads_k_stride &&
+         a.cu == b.cu;
+}
+
+// Checks the current device once: it must be an sm_103 part.
+ra_status current_device(int* dev_out, DeviceState** st_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RA_ERR_CUDA;
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return RA_ERR_CUDA;
+    if (!(prop.major == 10 && prop.minor == 3)) {
+      st.why = RA_ERR_UNSUPPORTED;
+    } else {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return RA_ERR_CUDA;
+      if (cudaMemset(addr, 0, sizeof(int)) != cudaSuccess) return RA_ERR_CUDA;
+      st.status = static_cast<int*>(addr);
+      st.why = RA_OK;
+    }
+    st.ready = true;
+  }
+  if (st.why != RA_OK) return st.why;
+  *dev_out = dev;
+  *st_out = &st;
+  return RA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode;
+}
+
+// [T, H, D] bf16 tensor viewed as 3-D (D, H, T); box 64 x 1 x 128, 128 B swizzle.
+bool encode_thd(CUtensorMap* map, const void* ptr, int T, int H, int D) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PlanInput make_input(const int32_t* cu_seqlens, const ra_dims& d, int P, int layout, int causal) {
+  PlanInput in;
+  in.T = d.total_tokens;
+  in.hq = d.hq;
+  in.hkv = d.hkv;
+  in.num_shards = P;
+  in.layout = layout;
+  in.causal = causal ? 1 : 0;
+  in.heads_k_stride = d.heads_k_stride == 0 ? 1 : d.heads_k_stride;
+  if (cu_seqlens && d.num_seqs >= 1) {
+    in.cu.assign(cu_seqlens, cu_seqlens + d.num_seqs + 1);
+  } else {
+    in.cu = {0, d.total_tokens};
+  }
+  return in;
+}
+
+// Common argument checks; returns RA_OK and fills `in`.
+ra_status check_problem(const int32_t* cu_seqlens, const ra_dims& d, int P, int layout, int causal,
+                        PlanInput* in) {
+  if (d.total_tokens < 0 || d.hq < 1 || d.hkv < 1 || d.head_dim < 1) return RA_ERR_INVALID_ARG;
+  if (d.heads_k_stride < 0) return RA_ERR_INVALID_ARG;
+  if (cu_seqlens && d.num_seqs < 1) return RA_ERR_INVALID_ARG;
+  if (P < 1 || (layout != RA_CONTIGUOUS && layout != RA_ZIGZAG)) return RA_ERR_INVALID_ARG;
+  const long long parts = layout == RA_ZIGZAG ? 2LL * P : P;
+  if (d.total_tokens % parts) return RA_ERR_NOT_DIVISIBLE;
+  if (d.dtype != RA_BF16 && d.dtype != RA_FP32) return RA_ERR_UNSUPPORTED;
+  if (d.dtype == RA_BF16 && d.head_dim != 128) return RA_ERR_UNSUPPORTED;
+  if (d.dtype == RA_FP32 && d.head_dim != 64 && d.head_dim != 128) return RA_ERR_UNSUPPORTED;
+  if ((long long)d.total_tokens * d.hq * d.head_dim >= (1LL << 40)) return RA_ERR_UNSUPPORTED;
+  *in = make_input(cu_seqlens, d, P, layout, causal);
+  if (!plan_check(*in).empty()) return RA_ERR_INVALID_ARG;
+  return RA_OK;
+}
+
+// Finds or builds (and uploads) the plan; caller holds g_mu.
+ra_status get_plan(int dev, const PlanInput& in, cudaStream_t stream, CachedPlan** out) {
+  for (auto it = g_plans.begin(); it != g_plans.end(); ++it) {
+    if (it->dev == dev && same_key(it->key, in)) {
+      g_plans.splice(g_plans.begin(), g_plans, it);
+      *out = &g_plans.front();
+      return RA_OK;
+    }
+  }
+  while (g_plans.size() >= kMaxCachedPlans) {
+    CachedPlan& old = g_plans.back();
+    int cur = 0;
+    cudaGetDevice(&cur);
+    cudaSetDevice(old.dev);
+    if (old.last_use) {
+      cudaEventSynchronize(old.last_use);
+      cudaEventDestroy(old.last_use);
+    }
+    cudaFree(old.buf);
+    cudaSetDevice(cur);
+    g_plans.pop_back();
+  }
+  CachedPlan cp;
+  cp.dev = dev;
+  cp.key = in;
+  cp.plan = build_fwd_plan(in);
+  const size_t nb_items = cp.plan.items.size() * sizeof(PlanItem);
+  const size_t nb_segs = cp.plan.segs.size() * sizeof(PlanSegment);
+  const size_t nb_cu = cp.plan.cu.size() * sizeof(int32_t);
+  const size_t off_segs = (nb_items + 255) & ~size_t(255);
+  const size_t off_cu = off_segs + ((nb_segs + 255) & ~size_t(255));
+  const size_t total = off_cu + nb_cu;
+  if (cudaMalloc(&cp.buf, total) != cudaSuccess) return RA_ERR_CUDA;
+  char* b = static_cast<char*>(cp.buf);
+  cp.items = reinterpret_cast<PlanItem*>(b);
+  cp.segs = reinterpret_cast<PlanSegment*>(b + off_segs);
+  cp.cu = reinterpret_cast<int32_t*>(b + off_cu);
+  // synchronous uploads: the plan is built once per distinct problem
+  if ((nb_items && cudaMemcpy(cp.items, cp.plan.items.data(), nb_items, cudaMemcpyHostToDevice)) ||
+      (nb_segs && cudaMemcpy(cp.segs, cp.plan.segs.data(), nb_segs, cudaMemcpyHostToDevice)) ||
+      cudaMemcpy(cp.cu, cp.plan.cu.data(), nb_cu, cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(cp.buf);
+    return RA_ERR_CUDA;
+  }
+  if (cudaEventCreateWithFlags(&cp.last_use, cudaEventDisableTiming) != cudaSuccess) {
+    cudaFree(cp.buf);
+    return RA_ERR_CUDA;
+  }
+  (void)stream;
+  g_plans.push_front(std::move(cp));
+  *out = &g_plans.front();
+  return RA_OK;
+}
+
+FwdParams make_params(const void* q, const void* k, const void* v, void* out, float* lse,
+                      const ra_dims& d, int causal, const CachedPlan& cp, int* status) {
+  FwdParams p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.out = out;
+  p.lse = lse;
+  p.items = cp.items;
+  p.segs = cp.segs;
+  p.cu = cp.cu;
+  p.num_docs = static_cast<int>(cp.plan.cu.size()) - 1;
+  p.num_items = static_cast<int>(cp.plan.items.size());
+  p.T = d.total_tokens;
+  p.hq = d.hq;
+  p.hkv = d.hkv;
+  p.D = d.head_dim;
+  p.group = d.hq / d.hkv;
+  p.causal = causal ? 1 : 0;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(d.head_dim));
+  p.scale_log2 = p.scale * 1.4426950408889634f;
+  p.step_filter = -1;
+  p.out_fp32 = d.dtype == RA_FP32 ? 1 : 0;
+  p.status = status;
+  return p;
+}
+
+struct Maps {
+  CUtensorMap q, k, v;
+};
+
+ra_status launch_fwd(const FwdParams& p, const ra_dims& d, const Maps* maps, cudaStream_t stream) {
+  cudaError_t e;
+  if (d.dtype == RA_FP32)
+    e = launch_fwd_simt_fp32(p, stream);
+  else
+    e = launch_fwd_tc_bf16(p, maps->q, maps->k, maps->v, stream);
+  return e == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
+ra_status prepare_maps(const void* q, const void* k, const void* v, const ra_dims& d, Maps* maps) {
+  if (d.dtype != RA_BF16) return RA_OK;
+  if (!encode_thd(&maps->q, q, d.total_tokens, d.hq, d.head_dim) ||
+      !encode_thd(&maps->k, k, d.total_tokens, d.hkv, d.head_dim) ||
+      !encode_thd(&maps->v, v, d.total_tokens, d.hkv, d.head_dim))
+    return RA_ERR_CUDA;
+  return RA_OK;
+}
+
+size_t fp32_o_bytes(const ra_dims& d) {
+  return ((size_t)d.total_tokens * d.hq * d.head_dim * 4 + 255) & ~size_t(255);
+}
+size_t lse_bytes(const ra_dims& d) { return ((size_t)d.hq * d.total_tokens * 4 + 255) & ~size_t(255); }
+
+}  // namespace
+}  // namespace ra
+
+using namespace ra;
+
+extern "C" {
+
+ra_status ringattn_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                       ra_dims dims, int num_shards, int shard_layout, int causal, void* out,
+                       float* lse, void* stream) {
+  PlanInput in;
+  ra_status st = check_problem(cu_seqlens, dims, num_shards, shard_layout, causal, &in);
+  if (st != RA_OK) return st;
+  if (dims.total_tokens == 0) return RA_OK;
+  if (!q || !k || !v || !out || !lse) return RA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return RA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev;
+  DeviceState* ds;
+  if ((st = current_device(&dev, &ds)) != RA_OK) return st;
+  Maps maps;
+  if ((st = prepare_maps(q, k, v, dims, &maps)) != RA_OK) return st;
+  CachedPlan* cp;
+  if ((st = get_plan(dev, in, static_cast<cudaStream_t>(stream), &cp)) != RA_OK) return st;
+  const FwdParams p = make_params(q, k, v, out, lse, dims, causal, *cp, ds->status);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = launch_fwd(p, dims, &maps, s)) != RA_OK) return st;
+  if (cudaEventRecord(cp->last_use, s) != cudaSuccess) return RA_ERR_CUDA;
+  return RA_OK;
+}
+
+size_t ringattn_fwd_stepwise_workspace_size(ra_dims dims) {
+  if (dims.total_tokens < 0 || dims.hq < 1 || dims.head_dim < 1) return 0;
+  return 2 * (fp32_o_bytes(dims) + lse_bytes(dims));
+}
+
+ra_status ringattn_fwd_stepwise(const void* q, const void* k, const void* v,
+                                const int32_t* cu_seqlens, ra_dims dims, int num_shards,
+                                int shard_layout, int causal, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  PlanInput in;
+  ra_status st = check_problem(cu_seqlens, dims, num_shards, shard_layout, causal, &in);
+  if (st != RA_OK) return st;
+  if (dims.total_tokens == 0) return RA_OK;
+  if (!q || !k || !v || !out || !lse) return RA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return RA_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < ringattn_fwd_stepwise_workspace_size(dims) ||
+      !aligned16(workspace))
+    return RA_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev;
+  DeviceState* ds;
+  if ((st = current_device(&dev, &ds)) != RA_OK) return st;
+  Maps maps;
+  if ((st = prepare_maps(q, k, v, dims, &maps)) != RA_OK) return st;
+  CachedPlan* cp;
+  if ((st = get_plan(dev, in, static_cast<cudaStream_t>(stream), &cp)) != RA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(workspace);
+  float* acc_o = reinterpret_cast<float*>(w);
+  float* acc_l = reinterpret_cast<float*>(w + fp32_o_bytes(dims));
+  float* stp_o = reinterpret_cast<float*>(w + fp32_o_bytes(dims) + lse_bytes(dims));
+  float* stp_l = reinterpret_cast<float*>(w + 2 * fp32_o_bytes(dims) + lse_bytes(dims));
+  const bool out_fp32 = dims.dtype == RA_FP32;
+  for (int step = 0; step < num_shards; ++step) {
+    const bool last = step == num_shards - 1;
+    // step 0 starts the accumulator; one shard writes the result directly
+    void* o_dst = step == 0 ? (last ? out : static_cast<void*>(acc_o)) : stp_o;
+    float* l_dst = step == 0 ? (last ? lse : acc_l) : stp_l;
+    FwdParams p = make_params(q, k, v, o_dst, l_dst, dims, causal, *cp, ds->status);
+    p.step_filter = step;
+    p.out_fp32 = (step == 0 && last) ? (out_fp32 ? 1 : 0) : 1;
+    if ((st = launch_fwd(p, dims, &maps, s)) != RA_OK) return st;
+    if (step > 0) {
+      cudaError_t e = launch_lse_merge(acc_o, true, acc_l, stp_o, true, stp_l,
+                                       last ? out : static_cast<void*>(acc_o),
+                                       last ? out_fp32 : true, last ? lse : acc_l,
+                                       dims.total_tokens, dims.hq, dims.head_dim, s);
+      if (e != cudaSuccess) return RA_ERR_CUDA;
+    }
+  }
+  if (cudaEventRecord(cp->last_use, s) != cudaSuccess) return RA_ERR_CUDA;
+  return RA_OK;
+}
+
+size_t ringattn_bwd_workspace_size(ra_dims dims) {
+  if (dims.total_tokens < 0 || dims.hq < 1 || dims.head_dim < 1) return 0;
+  return fp32_o_bytes(dims) + lse_bytes(dims);
+}
+
+ra_status ringattn_bwd(const void* q, const void* k, const void* v, const void* out,
+                       const float* lse, const void* dout, const int32_t* cu_seqlens,
+                       ra_dims dims, int num_shards, int shard_layout, int causal, void* dq,
+                       void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  (void)q; (void)k; (void)v; (void)out; (void)lse; (void)dout; (void)cu_seqlens; (void)dims;
+  (void)num_shards; (void)shard_layout; (void)causal; (void)dq; (void)dk; (void)dv;
+  (void)workspace; (void)workspace_bytes; (void)stream;
+  return RA_ERR_UNSUPPORTED;
+}
+
+ra_status attn_lse_merge(void* o_a, float* lse_a, const void* o_b, const float* lse_b, int rows,
+                         int heads, int head_dim, int dtype, void* stream) {
+  if (rows < 0 || heads < 1 || head_dim < 8 || head_dim % 8 || 32 % (head_dim / 8))
+    return RA_ERR_INVALID_ARG;
+  if (dtype != RA_BF16 && dtype != RA_FP32) return RA_ERR_UNSUPPORTED;
+  if (rows == 0) return RA_OK;
+  if (!o_a || !lse_a || !o_b || !lse_b) return RA_ERR_INVALID_ARG;
+  if (!aligned16(o_a) || !aligned16(o_b)) return RA_ERR_INVALID_ARG;
+  int dev;
+  DeviceState* ds;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    ra_status st = current_device(&dev, &ds);
+    if (st != RA_OK) return st;
+  }
+  const bool f32 = dtype == RA_FP32;
+  cudaError_t e = launch_lse_merge(o_a, f32, lse_a, o_b, f32, lse_b, o_a, f32, lse_a, rows, heads,
+                                   head_dim, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RA_OK : RA_ERR_CUDA;
+}
+
+ra_status ringattn_get_status(void* stream) {
+  int dev;
+  DeviceState* ds;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    ra_status st = current_device(&dev, &ds);
+    if (st != RA_OK) return st;
+  }
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return RA_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, ds->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return RA_ERR_CUDA;
+  if (word != 0 && cudaMemset(ds->status, 0, sizeof(int)) != cudaSuccess) return RA_ERR_CUDA;
+  return static_cast<ra_status>(word);
+}
+
+const char* ringattn_status_string(int status) {
+  switch (status) {
+    case RA_OK: return "ok";
+    case RA_ERR_INVALID_ARG: return "invalid argument";
+    case RA_ERR_NOT_DIVISIBLE: return "total_tokens not divisible by the number of shard chunks";
+    case RA_ERR_UNSUPPORTED: return "unsupported dtype, head_dim or device";
+    case RA_ERR_CUDA: return "CUDA runtime error";
+    case RA_ERR_TIMEOUT: return "a kernel wait timed out";
+    case RA_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+int ringattn_version(void) { return 100; }
+
+ra_status ringattn_plan_fwd(const int32_t* cu_seqlens, ra_dims dims, int num_shards,
+                            int shard_layout, int causal, int32_t* items, int max_items,
+                            int32_t* segments, int max_segments, int* num_items,
+                            int* num_segments) {
+  PlanInput in;
+  // the plan does not depend on dtype or head_dim: check shapes only
+  ra_dims d = dims;
+  d.dtype = RA_FP32;
+  d.head_dim = 64;
+  ra_status st = check_problem(cu_seqlens, d, num_shards, shard_layout, causal, &in);
+  if (st != RA_OK) return st;
+  if (!num_items || !num_segments) return RA_ERR_INVALID_ARG;
+  const Plan plan = build_fwd_plan(in);
+  *num_items = static_cast<int>(plan.items.size());
+  *num_segments = static_cast<int>(plan.segs.size());
+  if (*num_items > max_items || *num_segments > max_segments) return RA_ERR_WORKSPACE;
+  if (*num_items && items) std::memcpy(items, plan.items.data(), plan.items.size() * sizeof(PlanItem));
+  if (*num_segments && segments)
+    std::memcpy(segments, plan.segs.data(), plan.segs.size() * sizeof(PlanSegment));
+  return RA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,58 @@
+// Device-side view of the planner's work list and the parameters shared by
+// the forward kernels.
+#pragma once
+#include <cstdint>
+
+#include "planner.h"
+
+namespace ra {
+
+struct FwdParams {
+  const void* q;          // [T, Hq, D]
+  const void* k;          // [T, Hkv, D]
+  const void* v;          // [T, Hkv, D]
+  void* out;              // [T, Hq, D], bf16 or fp32 (out_fp32)
+  float* lse;             // [Hq, T]
+  const PlanItem* items;  // device copy of the plan
+  const PlanSegment* segs;
+  const int32_t* cu;      // document offsets, num_docs + 1
+  int num_docs;
+  int num_items;
+  int T, hq, hkv, D;
+  int group;              // Hq / Hkv
+  int causal;
+  float scale;            // 1 / sqrt(D)
+  float scale_log2;       // scale * log2(e)
+  int step_filter;        // -1: every ring step; s >= 0: only segments of step s
+  int out_fp32;           // 1: out is fp32, 0: out is bf16
+  int* status;            // device status word (first error wins)
+};
+
+// Start and end of the document holding token t (binary search over cu).
+__device__ __forceinline__ void doc_bounds(const int32_t* cu, int num_docs, int t, int* start,
+                                           int* end) {
+  int lo = 0, hi = num_docs;  // cu[lo] <= t < cu[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(cu + mid) <= t)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  *start = __ldg(cu + lo);
+  *end = __ldg(cu + lo + 1);
+}
+
+// Keys query row `row` may see: [lo, hi) (same document, and <= row if causal).
+__device__ __forceinline__ void row_key_interval(const FwdParams& p, int row, int* lo, int* hi) {
+  int s, e;
+  doc_bounds(p.cu, p.num_docs, row, &s, &e);
+  *lo = s;
+  *hi = p.causal ? row + 1 : e;
+}
+
+__device__ __forceinline__ bool seg_selected(const PlanSegment& s, int step_filter) {
+  return step_filter < 0 || s.step == step_filter;
+}
+
+}  // namespace ra

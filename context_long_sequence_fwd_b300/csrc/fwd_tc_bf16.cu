@@ -1,0 +1,391 @@
+// bf16 ring-attention forward on the sm_103a tensor cores (tcgen05 + TMEM).
+//
+// One CTA takes one planner item: two 128-row query tiles (A and B) that read
+// the same key/value head, and the item's key ranges in ring order (ring
+// step s visits the K/V shard of rank (r - s) mod P; axolotl "Sequence
+// Parallelism" page, introduction; aicassindra "tm_sp_math", "Context
+// parallelism is the axis that is independent").  No T x T score matrix is
+// formed: each 128 x 128 block of scores lives in tensor memory only while
+// its softmax runs (FlashAttention-style tiling, archcrux interview page).
+//
+// Roles (384 threads):
+//   warp 0      TMA producer: Q_A, Q_B once, then K_j, V_j into a ring of
+//               five 32 KB shared-memory slots (128 B swizzle).
+//   warp 1      allocates TMEM; one thread issues every tcgen05.mma:
+//                 S_X = Q_X K_j^T      (SS, both operands K-major)
+//                 O_X += P_X V_j       (TS: P from TMEM, V MN-major)
+//               ordered PV_A(j), S_A(j+1), PV_B(j), S_B(j+1) so one tile's
+//               softmax overlaps the other tile's MMAs.
+//   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: one query
+//               row per thread, read from TMEM lane (warp % 4) * 32 + lane.
+// TMEM columns: S_A 0-127, S_B 128-255, O_A 256-383, O_B 384-511.  P (bf16,
+// two per column) overwrites the first 64 columns of its S block; tcgen05
+// MMAs of one thread execute in issue order, so S_X(j+1) cannot overwrite
+// P_X(j) before PV_X(j) has read it.
+//
+// Online softmax, in the log2 domain (scores pre-multiplied by
+// scale * log2 e): the running maximum is only raised when a tile's maximum
+// exceeds it by more than 8 (a factor 256), so O in TMEM is rescaled rarely;
+// the final O / l and lse = ln 2 * (m + log2 l) are exact whatever maximum
+// was used.  Carrying (m, l, O) from one ring step to the next is exactly
+// the log-sum-exp merge of the steps' partial results.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "device_common.cuh"
+#include "launch.h"
+#include "sm103_ptx.cuh"
+
+namespace ra {
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kBN = 128;                     // keys per K/V tile
+constexpr int kStages = 5;                   // K/V slots
+constexpr int kTileBytes = kBN * kD * 2;     // 32 KB: one 128 x 128 bf16 tile
+constexpr int kHalfBytes = kTileBytes / 2;   // 128 rows x 64 columns (one swizzle span)
+constexpr int kThreads = 384;
+constexpr int kOffQ = 0;                     // Q_A, Q_B
+constexpr int kOffKV = 2 * kTileBytes;       // K/V ring
+constexpr int kOffCtl = kOffKV + kStages * kTileBytes;
+constexpr int kSmemBytes = kOffCtl + 256 + 1024;  // control block + alignment slack
+constexpr float kRescaleThreshold = 8.0f;    // log2 units
+
+constexpr uint32_t kIdescQK = make_idesc_bf16(128, 128, false, false);
+constexpr uint32_t kIdescPV = make_idesc_bf16(128, 128, false, true);
+
+struct Ctl {
+  uint64_t q_full;
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(Ctl) <= 256, "control block");
+
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+    mma_bf16_ss(d_tmem, make_sdesc_sw128(q_smem + off, 16, 1024),
+                make_sdesc_sw128(k_smem + off, 16, 1024), kIdescQK, kk > 0);
+  }
+}
+
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kBN / 16; ++kk) {
+    mma_bf16_ts(d_tmem, p_tmem + kk * 8, make_sdesc_sw128(v_smem + kk * 2048, kHalfBytes, 1024),
+                kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_bf16_kernel(const __grid_constant__ CUtensorMap map_q,
+                       const __grid_constant__ CUtensorMap map_k,
+                       const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + kOffCtl);
+  const uint32_t sQ = smem_u32(smem + kOffQ);
+  const uint32_t sKV = smem_u32(smem + kOffKV);
+  volatile int* abort = &ctl->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const PlanItem it = p.items[blockIdx.x];
+  const bool has_b = it.qlen[1] > 0;
+  const int g = it.head[0] / p.group;
+
+  // K/V tiles this item visits (same count in every role)
+  int n = 0;
+  for (int si = 0; si < it.seg_count; ++si) {
+    const PlanSegment sg = p.segs[it.seg_begin + si];
+    if (seg_selected(sg, p.step_filter)) n += (sg.k1 - sg.k0 + kBN - 1) / kBN;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl->q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&ctl->kv_full[s], 1);
+      mbar_init(&ctl->kv_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&ctl->s_full[x], 1);
+      mbar_init(&ctl->p_full[x], 128);
+      mbar_init(&ctl->o_full[x], 1);
+    }
+    mbar_init(&ctl->mma_done, 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (elect_one_sync() && n > 0) {
+      tma_prefetch_map(&map_q);
+      tma_prefetch_map(&map_k);
+      tma_prefetch_map(&map_v);
+      mbar_arrive_expect_tx(&ctl->q_full, (has_b ? 2 : 1) * kTileBytes);
+      for (int x = 0; x < (has_b ? 2 : 1); ++x)
+        for (int hf = 0; hf < 2; ++hf)
+          tma_load_3d(smem + kOffQ + x * kTileBytes + hf * kHalfBytes, &map_q, &ctl->q_full,
+                      hf * 64, it.head[x], it.q0[x]);
+      int li = 0;
+      bool ok = true;
+      for (int si = 0; si < it.seg_count && ok; ++si) {
+        const PlanSegment sg = p.segs[it.seg_begin + si];
+        if (!seg_selected(sg, p.step_filter)) continue;
+        for (int kt = sg.k0; kt < sg.k1 && ok; kt += kBN) {
+          for (int kv = 0; kv < 2; ++kv, ++li) {
+            const int slot = li % kStages;
+            if (li >= kStages &&
+                !mbar_wait(&ctl->kv_empty[slot], ((li / kStages) - 1) & 1, p.status, abort)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&ctl->kv_full[slot], kTileBytes);
+            const CUtensorMap* map = kv == 0 ? &map_k : &map_v;
+            for (int hf = 0; hf < 2; ++hf)
+              tma_load_3d(smem + kOffKV + slot * kTileBytes + hf * kHalfBytes, map,
+                          &ctl->kv_full[slot], hf * 64, g, kt);
+          }
+        }
+      }
+      if (!ok) *abort = 1;
+      // let every copy this thread started land before the CTA can exit
+      for (int s = 0; s < kStages && s < li; ++s) {
+        const int last = s + ((li - 1 - s) / kStages) * kStages;
+        mbar_wait(&ctl->kv_full[s], (last / kStages) & 1, p.status, nullptr);
+      }
+      mbar_wait(&ctl->q_full, 0, p.status, nullptr);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA
+    if (elect_one_sync() && n > 0) {
+      const uint32_t tS[2] = {tmem + 0, tmem + 128};
+      const uint32_t tO[2] = {tmem + 256, tmem + 384};
+      const uint32_t sQx[2] = {sQ, sQ + kTileBytes};
+      bool ok = mbar_wait(&ctl->q_full, 0, p.status, abort);
+      tc_fence_after_sync();
+      auto kv_ready = [&](int li) {
+        return mbar_wait(&ctl->kv_full[li % kStages], (li / kStages) & 1, p.status, abort);
+      };
+      auto slot_addr = [&](int li) { return sKV + (li % kStages) * kTileBytes; };
+      if (ok && (ok = kv_ready(0))) {
+        tc_fence_after_sync();
+        issue_qk(tS[0], sQx[0], slot_addr(0));
+        mma_commit(&ctl->s_full[0]);
+        if (has_b) {
+          issue_qk(tS[1], sQx[1], slot_addr(0));
+          mma_commit(&ctl->s_full[1]);
+        }
+        mma_commit(&ctl->kv_empty[0]);
+      }
+      for (int j = 0; j < n && ok; ++j) {
+        const int liV = 2 * j + 1, liK = 2 * j + 2;
+        if (!(ok = kv_ready(liV))) break;
+        if (!(ok = mbar_wait(&ctl->p_full[0], j & 1, p.status, abort))) break;
+        tc_fence_after_sync();
+        issue_pv(tO[0], tS[0], slot_addr(liV), j > 0);
+        if (j == n - 1) mma_commit(&ctl->o_full[0]);
+        const bool more = j + 1 < n;
+        if (more) {
+          if (!(ok = kv_ready(liK))) break;
+          tc_fence_after_sync();
+          issue_qk(tS[0], sQx[0], slot_addr(liK));
+          mma_commit(&ctl->s_full[0]);
+        }
+        if (has_b) {
+          if (!(ok = mbar_wait(&ctl->p_full[1], j & 1, p.status, abort))) break;
+          tc_fence_after_sync();
+          issue_pv(tO[1], tS[1], slot_addr(liV), j > 0);
+          if (j == n - 1) mma_commit(&ctl->o_full[1]);
+        }
+        mma_commit(&ctl->kv_empty[liV % kStages]);
+        if (more) {
+          if (has_b) {
+            issue_qk(tS[1], sQx[1], slot_addr(liK));
+            mma_commit(&ctl->s_full[1]);
+          }
+          mma_commit(&ctl->kv_empty[liK % kStages]);
+        }
+      }
+      if (!ok) *abort = 1;
+      // every MMA this thread issued has completed before TMEM is released
+      mma_commit(&ctl->mma_done);
+      mbar_wait(&ctl->mma_done, 0, p.status, nullptr);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int x = (warp - 4) >> 2;  // query tile
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    if (x == 0 || has_b) {
+      const int row = it.q0[x] + r;
+      const bool valid = r < it.qlen[x];
+      const int head = it.head[x];
+      int lo = 0, hi = 0;
+      if (valid) row_key_interval(p, row, &lo, &hi);
+      const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+      const uint32_t tS = tmem + lane_off + x * 128;
+      const uint32_t tO = tmem + lane_off + 256 + x * 128;
+      const int mlo = it.mask_lo[x], mhi = it.mask_hi[x];
+      const float sl2 = p.scale_log2;
+      float m2 = -INFINITY;  // running max, log2 units
+      float l = 0.f;
+      bool ok = true;
+      int j = 0;
+      for (int si = 0; si < it.seg_count && ok; ++si) {
+        const PlanSegment sg = p.segs[it.seg_begin + si];
+        if (!seg_selected(sg, p.step_filter)) continue;
+        const int a = max(lo, sg.k0), b = min(hi, sg.k1);
+        const int full_lo = max(sg.k0, mlo), full_hi = min(sg.k1, mhi);
+        for (int kt = sg.k0; kt < sg.k1; kt += kBN, ++j) {
+          // .sync.aligned TMEM accesses follow: keep the warp's decision uniform
+          ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_full[x], j & 1, p.status, abort));
+          if (!ok) break;
+          tc_fence_after_sync();
+          float s[kBN];
+#pragma unroll
+          for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t u[32];
+            tmem_load_32(tS + c * 32, u);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(u[i]);
+          }
+          // keys outside [a, b) are hidden unless the whole tile is visible
+          // to every row of this query tile
+          if (!(kt >= full_lo && kt + kBN <= full_hi)) {
+#pragma unroll
+            for (int c = 0; c < kBN; ++c) {
+              const int key = kt + c;
+              if (key < a || key >= b) s[c] = -INFINITY;
+            }
+          }
+          float mx = s[0];
+#pragma unroll
+          for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+          const float m_new = fmaxf(m2, mx * sl2);
+          const bool resc = m_new > m2 + kRescaleThreshold;
+          float alpha = 1.f;
+          if (resc) {
+            alpha = fast_exp2(m2 - m_new);
+            m2 = m_new;
+          }
+          const float m_use = (m2 == -INFINITY) ? 0.f : m2;
+          float sum = 0.f;
+          uint32_t pk[kBN / 2];
+#pragma unroll
+          for (int c = 0; c < kBN / 2; ++c) {
+            const float p0 = fast_exp2(fmaf(s[2 * c], sl2, -m_use));
+            const float p1 = fast_exp2(fmaf(s[2 * c + 1], sl2, -m_use));
+            sum += p0 + p1;
+            pk[c] = pack_bf16x2(p0, p1);
+          }
+          l = l * alpha + sum;
+          tmem_store_64(tS, pk);
+          if (j > 0 && __any_sync(0xffffffffu, resc)) {
+#pragma unroll
+            for (int c = 0; c < kD / 32; ++c) {
+              uint32_t u[32];
+              tmem_load_32(tO + c * 32, u);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+              tmem_store_32(tO + c * 32, u);
+            }
+          }
+          tmem_store_wait();
+          tc_fence_before_sync();
+          mbar_arrive(&ctl->p_full[x]);
+        }
+      }
+      if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->o_full[x], 0, p.status, abort));
+      if (!ok) *abort = 1;
+      tc_fence_after_sync();
+      // ------------------------------------------------------- epilogue
+      const bool empty = !(l > 0.f);
+      const float inv_l = empty ? 0.f : 1.f / l;
+      const size_t ob = ((size_t)row * p.hq + head) * kD;
+#pragma unroll
+      for (int c = 0; c < kD / 32; ++c) {
+        uint32_t u[32];
+        if (ok && n > 0) {
+          tmem_load_32(tO + c * 32, u);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = 0u;
+        }
+        if (valid && ok) {
+          if (p.out_fp32) {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + ob + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(u[4 * i]) * inv_l,
+                                   __uint_as_float(u[4 * i + 1]) * inv_l,
+                                   __uint_as_float(u[4 * i + 2]) * inv_l,
+                                   __uint_as_float(u[4 * i + 3]) * inv_l);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + ob + c * 32);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(pack_bf16x2(__uint_as_float(u[8 * i]) * inv_l,
+                                              __uint_as_float(u[8 * i + 1]) * inv_l),
+                                  pack_bf16x2(__uint_as_float(u[8 * i + 2]) * inv_l,
+                                              __uint_as_float(u[8 * i + 3]) * inv_l),
+                                  pack_bf16x2(__uint_as_float(u[8 * i + 4]) * inv_l,
+                                              __uint_as_float(u[8 * i + 5]) * inv_l),
+                                  pack_bf16x2(__uint_as_float(u[8 * i + 6]) * inv_l,
+                                              __uint_as_float(u[8 * i + 7]) * inv_l));
+          }
+        }
+      }
+      if (valid && ok)
+        p.lse[(size_t)head * p.T + row] =
+            empty ? -INFINITY : (m2 + log2f(l)) * 0.69314718055994530942f;
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc_bf16(const FwdParams& p, const CUtensorMap& map_q,
+                               const CUtensorMap& map_k, const CUtensorMap& map_v,
+                               cudaStream_t stream) {
+  if (p.num_items == 0) return cudaSuccess;
+  static bool configured = false;  // per process; the attribute is per function
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(fwd_tc_bf16_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  fwd_tc_bf16_kernel<<<p.num_items, kThreads, kSmemBytes, stream>>>(map_q, map_k, map_v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace ra

@@ -1,0 +1,26 @@
+// Internal launchers (host side).  Each returns the CUDA error of the launch.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+
+namespace ra {
+
+// fp32 forward on CUDA cores (D = 64 or 128).
+cudaError_t launch_fwd_simt_fp32(const FwdParams& p, cudaStream_t stream);
+
+// bf16 forward on tcgen05 tensor cores (D = 128).  The tensor maps describe
+// q [T, Hq, D] and k, v [T, Hkv, D] with 64 x 1 x 128 boxes, 128 B swizzle.
+cudaError_t launch_fwd_tc_bf16(const FwdParams& p, const CUtensorMap& map_q,
+                               const CUtensorMap& map_k, const CUtensorMap& map_v,
+                               cudaStream_t stream);
+
+// Log-sum-exp merge of (o_b, lse_b) into (o_a, lse_a), written to
+// (o_out, lse_out) (which may alias a).  o_* are [rows, heads, D]; each of
+// them is fp32 when its *_fp32 flag is set, else bf16.  lse_* are [heads, rows].
+cudaError_t launch_lse_merge(const void* o_a, bool a_fp32, const float* lse_a, const void* o_b,
+                             bool b_fp32, const float* lse_b, void* o_out, bool out_fp32,
+                             float* lse_out, int rows, int heads, int D, cudaStream_t stream);
+
+}  // namespace ra

@@ -1,0 +1,137 @@
+// Host-side shard / ring-step planner (see planner.h).
+//
+// Ring schedule: virtual rank r holds the query rows of its chunk(s); at ring
+// step s = 0 .. P-1 it uses the keys/values of rank (r - s) mod P, so step 0
+// is its own shard (axolotl "Sequence Parallelism" page: results aggregated
+// through a ring pattern; aicassindra "tm_sp_math", "Context parallelism is
+// the axis that is independent": K/V blocks rotate around the ring).
+// ZIGZAG gives rank r chunks r and 2P-1-r of 2P, which evens out the causal
+// work per rank (the "causal-mask load-balance problem" on the same page).
+#include "planner.h"
+
+#include <algorithm>
+#include <climits>
+
+namespace ra {
+
+void rank_chunks(int T, int P, int layout, int r, int out[2][2], int* n) {
+  if (layout == 0) {
+    const int C = T / P;
+    out[0][0] = r * C;
+    out[0][1] = (r + 1) * C;
+    *n = 1;
+  } else {
+    const int C = T / (2 * P);
+    out[0][0] = r * C;
+    out[0][1] = (r + 1) * C;
+    out[1][0] = (2 * P - 1 - r) * C;
+    out[1][1] = (2 * P - r) * C;
+    *n = 2;
+  }
+}
+
+std::string plan_check(const PlanInput& in) {
+  if (in.T < 0) return "total_tokens < 0";
+  if (in.hq < 1 || in.hkv < 1) return "head counts must be >= 1";
+  if (in.hq % in.hkv) return "hq must be a multiple of hkv";
+  if (in.num_shards < 1 || in.num_shards > 65536) return "num_shards out of range";
+  if (in.layout != 0 && in.layout != 1) return "unknown shard layout";
+  if (in.heads_k_stride < 1 || in.hkv % in.heads_k_stride) return "heads_k_stride must divide hkv";
+  if (in.cu.size() < 2) return "cu_seqlens needs at least two entries";
+  if (in.cu.front() != 0 || in.cu.back() != in.T) return "cu_seqlens must run from 0 to T";
+  for (size_t i = 1; i < in.cu.size(); ++i)
+    if (in.cu[i] < in.cu[i - 1]) return "cu_seqlens must not decrease";
+  return "";
+}
+
+namespace {
+
+struct Docs {
+  const std::vector<int32_t>& cu;
+  int doc_of(int t) const {  // last document d with cu[d] <= t
+    auto it = std::upper_bound(cu.begin(), cu.end(), t);
+    return static_cast<int>(it - cu.begin()) - 1;
+  }
+  int start(int t) const { return cu[doc_of(t)]; }
+  int end(int t) const { return cu[doc_of(t) + 1]; }
+};
+
+}  // namespace
+
+Plan build_fwd_plan(const PlanInput& in) {
+  Plan plan;
+  plan.cu = in.cu;
+  if (in.T == 0) return plan;
+  const Docs docs{plan.cu};
+  const int P = in.num_shards;
+  const int G = in.hq / in.hkv;
+  const bool head_pairs = (G % 2) == 0;
+  const int npass = in.hkv / in.heads_k_stride;
+
+  for (int pass = 0; pass < npass; ++pass) {
+    const size_t first_item = plan.items.size();
+    for (int g = pass * in.heads_k_stride; g < (pass + 1) * in.heads_k_stride; ++g) {
+      for (int r = 0; r < P; ++r) {
+        int qch[2][2], nq;
+        rank_chunks(in.T, P, in.layout, r, qch, &nq);
+        for (int c = 0; c < nq; ++c) {
+          const int a = qch[c][0], b = qch[c][1];
+          const int row_step = head_pairs ? kTileRows : 2 * kTileRows;
+          for (int t0 = a; t0 < b; t0 += row_step) {
+            const int hstep = head_pairs ? 2 : 1;
+            for (int h = g * G; h < (g + 1) * G; h += hstep) {
+              PlanItem it{};
+              for (int x = 0; x < 2; ++x) {
+                int q0 = head_pairs ? t0 : t0 + x * kTileRows;
+                int len = std::max(0, std::min(kTileRows, b - q0));
+                it.q0[x] = q0;
+                it.qlen[x] = len;
+                it.head[x] = head_pairs ? h + x : h;
+                if (len > 0) {
+                  const int last = q0 + len - 1;
+                  it.mask_lo[x] = docs.start(last);
+                  it.mask_hi[x] = in.causal ? q0 + 1 : docs.end(q0);
+                } else {
+                  it.mask_lo[x] = 0;
+                  it.mask_hi[x] = 0;
+                }
+              }
+              // keys any row of the item may see: from the first row's
+              // document start to the last row (causal) or its document end
+              const int first_row = it.q0[0];
+              const int last_row =
+                  it.qlen[1] > 0 ? it.q0[1] + it.qlen[1] - 1 : it.q0[0] + it.qlen[0] - 1;
+              const int lo = docs.start(first_row);
+              const int hi = in.causal ? last_row + 1 : docs.end(last_row);
+              it.seg_begin = static_cast<int32_t>(plan.segs.size());
+              it.rank = r;
+              it.pass = pass;
+              int cost = 0;
+              for (int s = 0; s < P; ++s) {
+                const int src = ((r - s) % P + P) % P;
+                int kch[2][2], nk;
+                rank_chunks(in.T, P, in.layout, src, kch, &nk);
+                for (int kc = 0; kc < nk; ++kc) {
+                  const int k0 = std::max(kch[kc][0], lo);
+                  const int k1 = std::min(kch[kc][1], hi);
+                  if (k0 >= k1) continue;  // fully masked at this step: skipped
+                  plan.segs.push_back(PlanSegment{k0, k1, s, src});
+                  cost += (k1 - k0 + kTileRows - 1) / kTileRows;
+                }
+              }
+              it.seg_count = static_cast<int32_t>(plan.segs.size()) - it.seg_begin;
+              it.cost = cost;
+              plan.items.push_back(it);
+            }
+          }
+        }
+      }
+    }
+    // longest first inside the pass, so the CTAs that start last are short
+    std::stable_sort(plan.items.begin() + first_item, plan.items.end(),
+                     [](const PlanItem& x, const PlanItem& y) { return x.cost > y.cost; });
+  }
+  return plan;
+}
+
+}  // namespace ra

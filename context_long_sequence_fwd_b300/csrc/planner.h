@@ -1,0 +1,61 @@
+// Host-side shard / ring-step planner.
+//
+// Turns (T, heads, P, layout, causal, documents) into a flat work list the
+// kernels walk: each item is one CTA's worth of queries (two 128-row query
+// tiles that share a key/value head) together with the list of key ranges
+// it must visit, in ring order.  Work that the causal or document mask hides
+// completely is never emitted (causal skip), and items are ordered longest
+// first inside each pass over the key/value heads.
+#pragma once
+#include <cstdint>
+#include <string>
+#include <vector>
+
+namespace ra {
+
+constexpr int kTileRows = 128;  // query rows per tile; also keys per K/V tile
+
+// One CTA of work: query tiles A (index 0) and B (index 1).
+struct PlanItem {
+  int32_t q0[2];       // first query token of each tile
+  int32_t qlen[2];     // valid rows of each tile (0 = tile absent)
+  int32_t head[2];     // query head of each tile
+  int32_t seg_begin;   // first segment of this item
+  int32_t seg_count;   // segments, in ring order
+  int32_t rank;        // virtual rank that owns the queries
+  int32_t cost;        // K/V tiles visited (scheduling weight)
+  int32_t mask_lo[2];  // per tile: largest first-visible key over its rows
+  int32_t mask_hi[2];  // per tile: smallest end-of-visible-keys over its rows
+  int32_t pass;        // pass over key/value heads (heads_k_stride groups)
+  int32_t pad;
+};
+static_assert(sizeof(PlanItem) == 16 * 4, "PlanItem is 16 int32");
+
+// Keys [k0, k1) of rank `src`, visited at ring step `step`.
+struct PlanSegment {
+  int32_t k0, k1, step, src;
+};
+
+struct PlanInput {
+  int T = 0, hq = 0, hkv = 0;
+  int num_shards = 1, layout = 0, causal = 0, heads_k_stride = 1;
+  std::vector<int32_t> cu;  // num_docs + 1 offsets (always filled: one doc if none given)
+};
+
+struct Plan {
+  std::vector<PlanItem> items;
+  std::vector<PlanSegment> segs;
+  std::vector<int32_t> cu;  // document offsets (copied to the device with the plan)
+};
+
+// Key ranges [a, b) of the chunks rank r holds (one for CONTIGUOUS, two for
+// ZIGZAG, ascending).
+void rank_chunks(int T, int P, int layout, int r, int out[2][2], int* n);
+
+// Validates the input; returns "" if fine, else a reason.
+std::string plan_check(const PlanInput& in);
+
+// Builds the forward schedule.  `in` must have passed plan_check.
+Plan build_fwd_plan(const PlanInput& in);
+
+}  // namespace ra

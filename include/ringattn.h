@@ -1,0 +1,178 @@
+/*
+ * ringattn.h -- C ABI of the B300 (sm_103a) ring-attention library.
+ *
+ * Ring attention (context parallelism) splits the token sequence into P
+ * shards ("virtual ranks"); each shard's queries visit every key/value shard
+ * in ring order and the partial results are aggregated (axolotl "Sequence
+ * Parallelism" page, introduction and "Implementation Details"; aicassindra
+ * "tm_sp_math", section "Context parallelism is the axis that is
+ * independent": K/V blocks rotate around a ring so no device holds the whole
+ * sequence, at the price of a causal-mask load-balance problem).  Here all P
+ * virtual ranks run on ONE GPU: a ring step indexes a K/V chunk that is
+ * already resident in device memory, and the partial results of the steps are
+ * folded with a log-sum-exp merge, so no T x T score matrix is ever formed
+ * (FlashAttention-style tiling: archcrux interview page; aicassindra page,
+ * "Why FlashAttention makes SP more valuable").
+ *
+ * Conventions shared by every call:
+ *   - Tensors are dense, row-major, 16-byte aligned DEVICE memory owned by the
+ *     caller.  q / out / dout / dq: [T, Hq, D]; k / v / dk / dv: [T, Hkv, D];
+ *     lse: fp32 [Hq, T], natural logarithm.  T = dims.total_tokens.
+ *   - Token order is the natural global order for every shard layout: the
+ *     layout changes the schedule (which shard's queries visit which K/V
+ *     chunk at which ring step), never the meaning of the result.
+ *   - cu_seqlens, when not NULL, is a HOST array of num_seqs + 1 int32
+ *     offsets (0 = cu[0] <= cu[1] <= ... <= cu[num_seqs] = T) describing
+ *     packed documents; positions restart at each document (axolotl page,
+ *     "Sample Packing with Sequence Parallelism"), so a query sees only keys
+ *     of its own document.  NULL means one document of T tokens.  The library
+ *     copies what it needs; the array may be freed after the call returns.
+ *   - Shards: CONTIGUOUS gives rank r tokens [r T/P, (r+1) T/P); ZIGZAG cuts
+ *     the sequence into 2P chunks and gives rank r chunks r and 2P-1-r, which
+ *     balances causal work.  T must be divisible by P (CONTIGUOUS) or 2P
+ *     (ZIGZAG), else RA_ERR_NOT_DIVISIBLE: the pages require the sequence to
+ *     split into equal chunks (axolotl page, "Implementation Details";
+ *     aicassindra page, "The knob you cannot turn on its own": s must be
+ *     divisible by the degree).
+ *   - GQA: query head h reads key/value head h / (Hq / Hkv).
+ *   - heads_k_stride (0 means 1) is the number of key/value heads processed
+ *     per pass over the ring (axolotl page, "Configuration").  It changes the
+ *     order of work only; results do not depend on it.  It must divide Hkv.
+ *   - Softmax scale is 1 / sqrt(D).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  Argument errors are returned synchronously and launch
+ *     nothing.  There is no fallback path: an unsupported shape or dtype
+ *     returns RA_ERR_UNSUPPORTED (the archcrux page warns that a silent
+ *     fallback of the attention kernel defeats the memory plan).
+ *   - Errors raised inside kernels (a bounded wait that timed out) are
+ *     recorded in a device status word that ringattn_get_status() reads.
+ *   - The library allocates no device memory per call.  It caches work lists
+ *     (one small device buffer per distinct problem) and one status word per
+ *     device, and releases them at unload.
+ */
+#ifndef RINGATTN_H
+#define RINGATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RA_OK = 0,
+  RA_ERR_INVALID_ARG = -1,   /* null pointer, bad size, bad cu_seqlens */
+  RA_ERR_NOT_DIVISIBLE = -2, /* T not divisible by P (or 2P for ZIGZAG) */
+  RA_ERR_UNSUPPORTED = -3,   /* dtype / head_dim / device not supported */
+  RA_ERR_CUDA = -4,          /* a CUDA runtime call failed */
+  RA_ERR_TIMEOUT = -5,       /* a kernel's bounded wait gave up */
+  RA_ERR_WORKSPACE = -6      /* workspace missing or too small */
+} ra_status;
+
+typedef enum { RA_BF16 = 0, RA_FP32 = 1 } ra_dtype;
+typedef enum { RA_CONTIGUOUS = 0, RA_ZIGZAG = 1 } ra_layout;
+
+typedef struct {
+  int total_tokens;   /* T >= 0 */
+  int num_seqs;       /* packed documents; ignored when cu_seqlens is NULL */
+  int hq;             /* query heads */
+  int hkv;            /* key/value heads, divides hq */
+  int head_dim;       /* D: 64 or 128 (bf16 path: 128) */
+  int dtype;          /* ra_dtype of q, k, v, out (and dout, dq, dk, dv) */
+  int heads_k_stride; /* key/value heads per ring pass; 0 = 1 */
+} ra_dims;
+
+/*
+ * Ring-attention forward (fused): every virtual rank's queries visit the K/V
+ * chunks of ranks (r - s) mod P for ring steps s = 0 .. P-1 in order; K/V
+ * tiles that the causal or document mask hides completely are skipped; the
+ * running (max, sum, O) of the online softmax is carried across tiles and
+ * steps, which is the log-sum-exp merge of the per-step partial results.
+ *   out: [T, Hq, D] in dims.dtype;  lse: fp32 [Hq, T].
+ * fp32 inputs run a CUDA-core path (fp32 arithmetic throughout); bf16 inputs
+ * run the tensor-core path (bf16 operands, fp32 accumulation).
+ */
+ra_status ringattn_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                       ra_dims dims, int num_shards, int shard_layout, int causal, void* out,
+                       float* lse, void* stream);
+
+/*
+ * Ring-attention forward, one launch per ring step: step s computes every
+ * rank's partial result over the single K/V shard it holds at that step
+ * (rows that see no key there get O = 0, lse = -inf), and attn_lse_merge
+ * folds it into the running result.  Same result as ringattn_fwd up to
+ * rounding; it is the literal ring algorithm, and the shape one step of a
+ * multi-GPU ring would take.  Needs a caller-owned device workspace of
+ * ringattn_fwd_stepwise_workspace_size(dims) bytes (fp32 partials).
+ */
+size_t ringattn_fwd_stepwise_workspace_size(ra_dims dims);
+ra_status ringattn_fwd_stepwise(const void* q, const void* k, const void* v,
+                                const int32_t* cu_seqlens, ra_dims dims, int num_shards,
+                                int shard_layout, int causal, void* out, float* lse,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Ring-attention backward.  Inputs q, k, v, out, lse from the forward and
+ * dout = dL/dout; outputs dq [T, Hq, D], dk and dv [T, Hkv, D] (summed over
+ * the query heads of each GQA group), all in dims.dtype.  With
+ * P_ij = exp(scale q_i.k_j - lse_i), D_i = dout_i . out_i:
+ *   dv_j = sum_i P_ij dout_i,  dS_ij = P_ij (dout_i . v_j - D_i),
+ *   dq_i = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i.
+ * Needs a caller-owned device workspace of ringattn_bwd_workspace_size(dims)
+ * bytes (fp32 dq accumulator and the D_i vector).
+ */
+size_t ringattn_bwd_workspace_size(ra_dims dims);
+ra_status ringattn_bwd(const void* q, const void* k, const void* v, const void* out,
+                       const float* lse, const void* dout, const int32_t* cu_seqlens,
+                       ra_dims dims, int num_shards, int shard_layout, int causal, void* dq,
+                       void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Log-sum-exp merge of two partial attention results over disjoint key sets,
+ * in place into (o_a, lse_a) -- how the pages' ring steps are aggregated
+ * (axolotl page, introduction).  Per row:
+ *   lse = max(a, b) + log1p(exp(-|a - b|)),
+ *   o   = exp(a - lse) o_a + exp(b - lse) o_b;
+ * a side with lse = -inf contributes nothing; two empty sides give o = 0,
+ * lse = -inf.  o_*: [rows, heads, head_dim] in dtype; lse_*: fp32
+ * [heads, rows].  rows = 0 is a no-op.
+ */
+ra_status attn_lse_merge(void* o_a, float* lse_a, const void* o_b, const float* lse_b, int rows,
+                         int heads, int head_dim, int dtype, void* stream);
+
+/* Synchronises `stream`, returns the first kernel-side error recorded since
+ * the last call (RA_OK if none) and clears it. */
+ra_status ringattn_get_status(void* stream);
+
+/* Static text for a status code. */
+const char* ringattn_status_string(int status);
+
+/* Library version as MAJOR * 10000 + MINOR * 100 + PATCH. */
+int ringattn_version(void);
+
+/*
+ * Host-only work-list introspection (no GPU needed), for tests and tools.
+ * Fills the forward schedule: items of RA_PLAN_ITEM_FIELDS int32 each and
+ * segments of RA_PLAN_SEG_FIELDS int32 each (layouts below).  Returns
+ * RA_OK and the counts; if a capacity is too small nothing is written
+ * beyond it and RA_ERR_WORKSPACE is returned with the counts still set.
+ *   item:    q0_a, q0_b, qlen_a, qlen_b, head_a, head_b, seg_begin,
+ *            seg_count, rank, cost (kv tiles), mask_lo_a, mask_lo_b,
+ *            mask_hi_a, mask_hi_b, pass, pad
+ *            (tile a/b: first query row, valid rows, query head; the key
+ *            range a tile may skip masking in is [mask_lo, mask_hi))
+ *   segment: k0, k1, step, src  (keys [k0, k1) of rank src at ring step)
+ */
+#define RA_PLAN_ITEM_FIELDS 16
+#define RA_PLAN_SEG_FIELDS 4
+ra_status ringattn_plan_fwd(const int32_t* cu_seqlens, ra_dims dims, int num_shards,
+                            int shard_layout, int causal, int32_t* items, int max_items,
+                            int32_t* segments, int max_segments, int* num_items,
+                            int* num_segments);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RINGATTN_H */

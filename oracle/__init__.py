@@ -101,8 +101,8 @@ def _cu(cu_seqlens, T):
     if cu_seqlens is None:
         return None, 0
     cu = _i32(cu_seqlens)
-    if cu.ndim != 1 or cu.size < 2 or cu[0] != 0 or cu[-1] != T or np.any(np.diff(cu) <= 0):
-        raise ValueError("cu_seqlens must rise strictly from 0 to T")
+    if cu.ndim != 1 or cu.size < 2 or cu[0] != 0 or cu[-1] != T or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens must run from 0 to T without decreasing")
     return cu, cu.size - 1
 
 

@@ -1,0 +1,85 @@
+"""The C-ABI library loads without a GPU and exports every function that
+include/ringattn.h declares; argument errors come back synchronously."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import context_long_sequence_fwd_b300 as ra
+from context_long_sequence_fwd_b300 import build as ra_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(ra.LIB_PATH):
+        ra_build.build()
+    return ra.library()
+
+
+def declared_functions():
+    names = set()
+    for hdr in os.listdir(os.path.join(ROOT, "include")):
+        if not hdr.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", hdr)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                             text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("ringattn_fwd", "ringattn_bwd", "attn_lse_merge", "ringattn_fwd_stepwise",
+              "ringattn_get_status", "ringattn_status_string"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(lib):
+    assert lib.ringattn_status_string(0) == b"ok"
+    assert b"divisible" in lib.ringattn_status_string(-2)
+    assert lib.ringattn_version() >= 100
+
+
+def dims(T=256, hq=2, hkv=2, d=128, dtype=ra.RA_BF16, hks=1, nseq=0):
+    return ra.ra_dims(T, nseq, hq, hkv, d, dtype, hks)
+
+
+def test_argument_errors_without_gpu(lib):
+    f = lib.ringattn_fwd
+    # sizes that do not split into equal chunks
+    assert f(None, None, None, None, dims(T=250), 4, ra.CONTIGUOUS, 1, None, None, None) == -2
+    assert f(None, None, None, None, dims(T=256), 3, ra.ZIGZAG, 1, None, None, None) == -2
+    # heads, dtype, head_dim
+    assert f(None, None, None, None, dims(hq=3, hkv=2), 1, 0, 1, None, None, None) == -1
+    assert f(None, None, None, None, dims(d=64), 1, 0, 1, None, None, None) == -3
+    assert f(None, None, None, None, dims(dtype=7), 1, 0, 1, None, None, None) == -3
+    assert f(None, None, None, None, dims(hks=3, hkv=2), 1, 0, 1, None, None, None) == -1
+    # null tensors with a non-empty problem
+    assert f(None, None, None, None, dims(), 1, 0, 1, None, None, None) == -1
+    # empty problem: nothing to do
+    assert f(None, None, None, None, dims(T=0), 2, ra.ZIGZAG, 1, None, None, None) == 0
+    # bad cu_seqlens (must run 0 .. T without decreasing)
+    cu = np.array([0, 100, 50, 256], np.int32)
+    p = cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    assert f(None, None, None, p, dims(nseq=3), 1, 0, 1, None, None, None) == -1
+    # workspace checks come before any device work
+    assert lib.ringattn_fwd_stepwise(16, 16, 16, None, dims(), 1, 0, 1, 16, 16, None, 0, None) == -6
+    assert lib.attn_lse_merge(None, None, None, None, 4, 2, 12, 0, None) == -1
+    assert lib.attn_lse_merge(None, None, None, None, 0, 2, 64, 0, None) == 0
+
+
+def test_workspace_sizes(lib):
+    d = dims(T=1024, hq=4, hkv=2)
+    assert lib.ringattn_fwd_stepwise_workspace_size(d) >= 2 * (1024 * 4 * 128 * 4 + 4 * 1024 * 4)
+    assert lib.ringattn_bwd_workspace_size(d) >= 1024 * 4 * 128 * 4

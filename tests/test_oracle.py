@@ -75,6 +75,7 @@ CASES = [
     (64, 6, 2, 8, [0, 10, 11, 30, 64], True),
     (64, 3, 1, 4, [0, 7, 40, 64], False),
     (33, 4, 4, 5, [0, 1, 2, 20, 33], True),
+    (30, 2, 1, 4, [0, 0, 10, 10, 30], True),          # empty documents
 ]
 
 

@@ -1,0 +1,182 @@
+"""Host-side checks of the shard / ring-step planner (no GPU).
+
+The planner's work list must cover, for every query row and head, exactly the
+keys the causal / document mask lets it see -- no key missing, none visited
+twice -- visit them in ring order (step s reads the K/V shard of rank
+(r - s) mod P, axolotl "Sequence Parallelism" page, introduction), skip key
+ranges nobody can see (causal skip), and keep ZIGZAG's per-rank causal work
+equal (aicassindra "tm_sp_math", "Context parallelism is the axis that is
+independent": the causal-mask load-balance problem).
+"""
+import numpy as np
+import pytest
+
+import context_long_sequence_fwd_b300 as ra
+from context_long_sequence_fwd_b300.workloads import cu_seqlens_from_lengths, doc_lengths
+
+TILE = 128
+
+
+def doc_index(T, cu):
+    bounds = [0, T] if cu is None else [int(x) for x in cu]
+    doc = np.empty(T, np.int64)
+    for d, (a, b) in enumerate(zip(bounds[:-1], bounds[1:])):
+        doc[a:b] = d
+    return doc
+
+
+def visible_keys(i, doc, causal):
+    ks = np.nonzero(doc == doc[i])[0]
+    return ks[ks <= i] if causal else ks
+
+
+def rank_chunks(T, P, layout, r):
+    if layout == ra.CONTIGUOUS:
+        C = T // P
+        return [(r * C, (r + 1) * C)]
+    C = T // (2 * P)
+    return [(r * C, (r + 1) * C), ((2 * P - 1 - r) * C, (2 * P - r) * C)]
+
+
+CASES = [
+    # T, hq, hkv, P, layout, causal, cu
+    (512, 2, 2, 2, ra.CONTIGUOUS, True, None),
+    (512, 4, 2, 4, ra.ZIGZAG, True, None),
+    (768, 2, 1, 3, ra.CONTIGUOUS, False, None),
+    (1000, 2, 2, 2, ra.CONTIGUOUS, True, None),        # chunks of 500: ragged tiles
+    (1040, 4, 2, 4, ra.ZIGZAG, True, None),            # zigzag chunks of 130
+    (1024, 4, 1, 4, ra.CONTIGUOUS, True, [0, 100, 101, 400, 777, 1024]),
+    (960, 6, 2, 2, ra.CONTIGUOUS, False, [0, 300, 310, 960]),
+    (1024, 2, 2, 2, ra.ZIGZAG, True, [0, 200, 200, 900, 1024]),   # empty document
+    (256, 3, 3, 1, ra.CONTIGUOUS, True, None),         # P = 1
+    (384, 2, 2, 1, ra.ZIGZAG, True, None),             # zigzag with one rank
+]
+
+
+def check_plan(T, hq, hkv, P, layout, causal, cu, hks=1):
+    items, segs = ra.plan_fwd(T, hq, hkv, P, layout, causal, cu, heads_k_stride=hks)
+    doc = doc_index(T, cu)
+    G = hq // hkv
+    seen = np.zeros((hq, T), np.int64)
+    for it in items:
+        (q0a, q0b, qla, qlb, ha, hb, sb, sc, rank, cost, mla, mlb, mha, mhb, pas, _) = it
+        my = segs[sb:sb + sc]
+        # ring order and shard ownership of every segment
+        assert np.all(np.diff(my[:, 2]) >= 0), "segments out of ring order"
+        for k0, k1, step, src in my:
+            assert src == (rank - step) % P
+            assert k0 < k1
+            assert any(a <= k0 and k1 <= b for a, b in rank_chunks(T, P, layout, src))
+        keys = np.concatenate([np.arange(k0, k1) for k0, k1, _, _ in my]) if len(my) else \
+            np.zeros(0, np.int64)
+        assert len(np.unique(keys)) == len(keys), "a key is visited twice"
+        assert cost == sum((k1 - k0 + TILE - 1) // TILE for k0, k1, _, _ in my)
+        rows_all = []
+        for q0, ql, h, mlo, mhi in ((q0a, qla, ha, mla, mha), (q0b, qlb, hb, mlb, mhb)):
+            if ql == 0:
+                continue
+            assert h // G == ha // G, "tiles of an item share a kv head"
+            assert pas == (h // G) // hks
+            assert any(a <= q0 and q0 + ql <= b for a, b in rank_chunks(T, P, layout, rank))
+            rows = np.arange(q0, q0 + ql)
+            rows_all.append(rows)
+            seen[h, rows] += 1
+            for i in rows:
+                vis = visible_keys(i, doc, causal)
+                got = np.intersect1d(keys, vis)
+                assert len(got) == len(vis), f"row {i} misses keys"
+            # a tile inside [mask_lo, mask_hi) needs no mask: every key of it
+            # must be visible to every row of the query tile
+            lo_i = np.array([visible_keys(i, doc, causal).min() for i in rows])
+            hi_i = np.array([visible_keys(i, doc, causal).max() + 1 for i in rows])
+            assert mlo == lo_i.max() and mhi == hi_i.min()
+        # causal skip is tight: every visited key is visible to some row
+        rows_all = np.concatenate(rows_all)
+        vis_any = np.zeros(T, bool)
+        for i in rows_all:
+            vis_any[visible_keys(i, doc, causal)] = True
+        assert np.all(vis_any[keys]), "a segment holds keys no row can see"
+    assert np.all(seen == 1), "every (head, row) belongs to exactly one tile"
+    # longest first inside each pass
+    for p in np.unique(items[:, 14]):
+        c = items[items[:, 14] == p, 9]
+        assert np.all(np.diff(c) <= 0)
+    passes = items[:, 14]
+    assert np.all(np.diff(passes) >= 0), "passes run in order"
+    return items, segs
+
+
+@pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
+def test_plan_covers_exactly_the_mask(case):
+    check_plan(*case)
+
+
+@pytest.mark.parametrize("hks", [1, 2, 4])
+def test_heads_k_stride_groups_passes(hks):
+    items, _ = check_plan(512, 8, 4, 2, ra.ZIGZAG, True, None, hks=hks)
+    assert items[:, 14].max() == 4 // hks - 1
+
+
+def test_zigzag_balances_causal_work():
+    T, P = 4096, 4
+    items, segs = ra.plan_fwd(T, 1, 1, P, ra.ZIGZAG, True)
+    pairs = np.zeros(P)
+    step_pairs = np.zeros((P, P))
+    for it in items:
+        for q0, ql in ((it[0], it[2]), (it[1], it[3])):
+            if ql == 0:
+                continue
+            for k0, k1, step, src in segs[it[6]:it[6] + it[7]]:
+                # visible (q, k) pairs of this tile and segment
+                qi = np.arange(q0, q0 + ql)[:, None]
+                kj = np.arange(k0, k1)[None, :]
+                n = int(np.sum(kj <= qi))
+                pairs[it[8]] += n
+                step_pairs[it[8], step] += n
+    assert np.all(pairs == pairs[0]), pairs
+    C = T // (2 * P)
+    for r in range(P):
+        for s in range(1, P):
+            # every non-diagonal step is exactly half of a 2C x 2C block
+            assert step_pairs[r, s] == 2 * C * C
+
+
+def test_contiguous_causal_skips_future_shards():
+    T, P = 2048, 4
+    items, segs = ra.plan_fwd(T, 1, 1, P, ra.CONTIGUOUS, True)
+    for it in items:
+        r = it[8]
+        srcs = set(segs[it[6]:it[6] + it[7], 3])
+        assert all(s <= r for s in srcs)          # shards after r are never visited
+
+
+def test_varlen_workload_plan():
+    lens = doc_lengths(65536, 512, 8192, 1)
+    cu = cu_seqlens_from_lengths(lens).numpy()
+    assert cu[-1] == 65536 and all(512 <= x <= 8192 for x in lens[:-1])
+    items, segs = ra.plan_fwd(65536, 32, 8, 8, ra.CONTIGUOUS, True, cu)
+    # every segment stays inside one document of the item's first row
+    doc = doc_index(65536, cu)
+    for it in items[:200]:
+        for k0, k1, _, _ in segs[it[6]:it[6] + it[7]]:
+            assert doc[k0] >= doc[it[0]]
+
+
+@pytest.mark.parametrize("T,P,layout", [(1000, 3, ra.CONTIGUOUS), (1000, 3, ra.ZIGZAG),
+                                        (512, 3, ra.ZIGZAG)])
+def test_not_divisible_is_rejected(T, P, layout):
+    with pytest.raises(ra.RingAttnError) as e:
+        ra.plan_fwd(T, 2, 2, P, layout, True)
+    assert e.value.code == -2
+
+
+@pytest.mark.parametrize("cu", [[0, 10, 9, 100], [1, 100], [0, 50], [0]])
+def test_bad_cu_seqlens_rejected(cu):
+    with pytest.raises(ra.RingAttnError) as e:
+        ra.plan_fwd(100, 2, 2, 1, ra.CONTIGUOUS, True, np.array(cu, np.int32))
+    assert e.value.code == -1
+
+
+def test_empty_sequence_plan():
+    items, segs = ra.plan_fwd(0, 2, 2, 2, ra.CONTIGUOUS, True)
+    assert len(items) == 0 and len(segs) == 0
