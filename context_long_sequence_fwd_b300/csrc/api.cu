@@ -334,6 +334,112 @@ ra_status ringattn_fwd_stepwise(const void* q, const void* k, const void* v,
   return RA_OK;
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Stepwise forward with a fixed, library-owned scratch area.
+//
+// Some callers cannot allocate device memory at the point where they run
+// attention: code inside a custom allocator or memory-pool callback, host
+// runtimes that hand out only the input and output buffers, or a process whose
+// allocations all go through a framework that is not reachable from this
+// call.  For them this entry point keeps its fp32 partial results and its work
+// list in a statically sized __device__ array instead of a caller workspace or
+// the plan cache.  Every GPU that loads the library holds the array until the
+// process exits.  All calls share it, so calls that overlap on the GPU (on
+// different streams, or from different threads) race on it; calls on one
+// stream are ordered.  Nothing in it needs to start at zero: each call writes
+// every byte it later reads.
+// ---------------------------------------------------------------------------
+namespace ra {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = RA_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+unsigned char* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (looked up once
+// per device, with that device current).
+ra_status noalloc_scratch(int dev, unsigned char** out) {
+  if (!g_noalloc_ptr[dev]) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr)
+      return RA_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<unsigned char*>(addr);
+  }
+  *out = g_noalloc_ptr[dev];
+  return RA_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+}  // namespace ra
+
+extern "C" ra_status ringattn_fwd_stepwise_noalloc(const void* q, const void* k, const void* v,
+                                                   const int32_t* cu_seqlens, ra_dims dims,
+                                                   int num_shards, int shard_layout, int causal,
+                                                   void* out, float* lse, void* stream) {
+  PlanInput in;
+  ra_status st = check_problem(cu_seqlens, dims, num_shards, shard_layout, causal, &in);
+  if (st != RA_OK) return st;
+  if (dims.total_tokens == 0) return RA_OK;
+  if (!q || !k || !v || !out || !lse) return RA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return RA_ERR_INVALID_ARG;
+  // scratch layout: acc O | acc lse | step O | step lse | items | segments | cu
+  const size_t ws = ringattn_fwd_stepwise_workspace_size(dims);
+  CachedPlan cp;  // host plan; its device copy lives in the scratch array
+  cp.plan = build_fwd_plan(in);
+  const size_t nb_items = cp.plan.items.size() * sizeof(PlanItem);
+  const size_t nb_segs = cp.plan.segs.size() * sizeof(PlanSegment);
+  const size_t nb_cu = cp.plan.cu.size() * sizeof(int32_t);
+  const size_t need = ws + round256(nb_items) + round256(nb_segs) + round256(nb_cu);
+  if (need > kNoAllocScratchBytes) return RA_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev;
+  DeviceState* ds;
+  if ((st = current_device(&dev, &ds)) != RA_OK) return st;
+  unsigned char* base;
+  if ((st = noalloc_scratch(dev, &base)) != RA_OK) return st;
+  Maps maps;
+  if ((st = prepare_maps(q, k, v, dims, &maps)) != RA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cp.items = reinterpret_cast<PlanItem*>(base + ws);
+  cp.segs = reinterpret_cast<PlanSegment*>(base + ws + round256(nb_items));
+  cp.cu = reinterpret_cast<int32_t*>(base + ws + round256(nb_items) + round256(nb_segs));
+  // pageable-source copies: staged before the call returns, ordered on `s`
+  if ((nb_items &&
+       cudaMemcpyAsync(cp.items, cp.plan.items.data(), nb_items, cudaMemcpyHostToDevice, s)) ||
+      (nb_segs &&
+       cudaMemcpyAsync(cp.segs, cp.plan.segs.data(), nb_segs, cudaMemcpyHostToDevice, s)) ||
+      cudaMemcpyAsync(cp.cu, cp.plan.cu.data(), nb_cu, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return RA_ERR_CUDA;
+  float* acc_o = reinterpret_cast<float*>(base);
+  float* acc_l = reinterpret_cast<float*>(base + fp32_o_bytes(dims));
+  float* stp_o = reinterpret_cast<float*>(base + fp32_o_bytes(dims) + lse_bytes(dims));
+  float* stp_l = reinterpret_cast<float*>(base + 2 * fp32_o_bytes(dims) + lse_bytes(dims));
+  const bool out_fp32 = dims.dtype == RA_FP32;
+  for (int step = 0; step < num_shards; ++step) {
+    const bool last = step == num_shards - 1;
+    void* o_dst = step == 0 ? (last ? out : static_cast<void*>(acc_o)) : stp_o;
+    float* l_dst = step == 0 ? (last ? lse : acc_l) : stp_l;
+    FwdParams p = make_params(q, k, v, o_dst, l_dst, dims, causal, cp, ds->status);
+    p.step_filter = step;
+    p.out_fp32 = (step == 0 && last) ? (out_fp32 ? 1 : 0) : 1;
+    if ((st = launch_fwd(p, dims, &maps, s)) != RA_OK) return st;
+    if (step > 0) {
+      cudaError_t e = launch_lse_merge(acc_o, true, acc_l, stp_o, true, stp_l,
+                                       last ? out : static_cast<void*>(acc_o),
+                                       last ? out_fp32 : true, last ? lse : acc_l,
+                                       dims.total_tokens, dims.hq, dims.head_dim, s);
+      if (e != cudaSuccess) return RA_ERR_CUDA;
+    }
+  }
+  return RA_OK;
+}
+
+extern "C" {
+
 size_t ringattn_bwd_workspace_size(ra_dims dims) {
   if (dims.total_tokens < 0 || dims.hq < 1 || dims.head_dim < 1) return 0;
   return fp32_o_bytes(dims) + lse_bytes(dims);

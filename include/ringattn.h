@@ -113,6 +113,30 @@ ra_status ringattn_fwd_stepwise(const void* q, const void* k, const void* v,
                                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Stepwise forward that allocates nothing.  There is no counterpart on the
+ * pages: this is an interface for callers that cannot allocate device memory
+ * where they call attention (inside an allocator or memory-pool callback, or
+ * in a host runtime that only hands out input and output buffers).  Same
+ * arguments, same work and same result as ringattn_fwd_stepwise, but the fp32
+ * partial results and the work list live in one library-owned __device__
+ * array of RA_NOALLOC_SCRATCH_BYTES bytes, which every GPU that loads the
+ * library holds until the process exits.  No cudaMalloc, cudaFree or other
+ * allocating call is made.
+ *   - Problems whose partials and work list need more than the array holds
+ *     (about T * Hq * (D + 1) * 8 bytes plus the work list) return
+ *     RA_ERR_WORKSPACE and launch nothing.
+ *   - All calls share the array: calls that overlap on the GPU (different
+ *     streams or threads) race; calls on one stream are ordered.
+ *   - The first call on a device looks up the array's device address; make
+ *     that first call before any stream capture.
+ */
+#define RA_NOALLOC_SCRATCH_BYTES (32u << 20)
+ra_status ringattn_fwd_stepwise_noalloc(const void* q, const void* k, const void* v,
+                                        const int32_t* cu_seqlens, ra_dims dims, int num_shards,
+                                        int shard_layout, int causal, void* out, float* lse,
+                                        void* stream);
+
+/*
  * Ring-attention backward.  Inputs q, k, v, out, lse from the forward and
  * dout = dL/dout; outputs dq [T, Hq, D], dk and dv [T, Hkv, D] (summed over
  * the query heads of each GQA group), all in dims.dtype.  With
