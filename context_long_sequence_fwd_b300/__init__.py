@@ -33,6 +33,9 @@ ITEM_COLUMNS = ("q0_a", "q0_b", "qlen_a", "qlen_b", "head_a", "head_b", "seg_beg
                 "seg_count", "rank", "cost", "mask_lo_a", "mask_lo_b", "mask_hi_a",
                 "mask_hi_b", "pass", "pad")
 SEG_COLUMNS = ("k0", "k1", "step", "src")
+PLAN_BWD_ITEM_FIELDS = 8
+BWD_ITEM_COLUMNS = ("k0", "klen", "kv_head", "src", "seg_begin", "seg_count", "cost", "pad")
+BWD_SEG_COLUMNS = ("q0", "q1", "step", "rank")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libringattn.so")
@@ -48,7 +51,8 @@ class RingAttnError(RuntimeError):
 class ra_dims(ctypes.Structure):
     _fields_ = [("total_tokens", ctypes.c_int), ("num_seqs", ctypes.c_int),
                 ("hq", ctypes.c_int), ("hkv", ctypes.c_int), ("head_dim", ctypes.c_int),
-                ("dtype", ctypes.c_int), ("heads_k_stride", ctypes.c_int)]
+                ("dtype", ctypes.c_int), ("heads_k_stride", ctypes.c_int),
+                ("grad_fp32", ctypes.c_int)]
 
 
 _vp = ctypes.c_void_p
@@ -86,8 +90,9 @@ def library():
         lib.ringattn_plan_fwd.argtypes = [_i32p, ra_dims, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, _i32p, ctypes.c_int, _i32p, ctypes.c_int,
                                           _ip, _ip]
+        lib.ringattn_plan_bwd.argtypes = lib.ringattn_plan_fwd.argtypes
         for fn in ("ringattn_fwd", "ringattn_fwd_stepwise", "ringattn_bwd", "attn_lse_merge",
-                   "ringattn_get_status", "ringattn_plan_fwd"):
+                   "ringattn_get_status", "ringattn_plan_fwd", "ringattn_plan_bwd"):
             getattr(lib, fn).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -126,9 +131,10 @@ def _cu_host(cu_seqlens):
     return arr.ctypes.data_as(_i32p), arr.size - 1, arr
 
 
-def make_dims(q, k, num_seqs=0, heads_k_stride=1) -> ra_dims:
+def make_dims(q, k, num_seqs=0, heads_k_stride=1, grad_fp32=False) -> ra_dims:
     T, hq, d = q.shape
-    return ra_dims(T, num_seqs, hq, k.shape[1], d, _dtype_code(q), heads_k_stride)
+    return ra_dims(T, num_seqs, hq, k.shape[1], d, _dtype_code(q), heads_k_stride,
+                   int(bool(grad_fp32)))
 
 
 def _need(t, name, shape=None, dtype=None):
@@ -204,25 +210,26 @@ def bwd_workspace_size(q, k, heads_k_stride=1) -> int:
 
 def ringattn_bwd(q, k, v, out, lse, dout, cu_seqlens=None, num_shards=1,
                  shard_layout=CONTIGUOUS, causal=True, dq=None, dk=None, dv=None,
-                 workspace=None, stream=None, heads_k_stride=1):
-    """Ring-attention backward; returns (dq, dk, dv)."""
+                 workspace=None, stream=None, heads_k_stride=1, grad_fp32=False):
+    """Ring-attention backward; returns (dq, dk, dv) (fp32 if grad_fp32)."""
     import torch
     _check_qkv(q, k, v)
     T, hq, d = q.shape
     _need(out, "out", q.shape, q.dtype)
     _need(dout, "dout", q.shape, q.dtype)
     _need(lse, "lse", (hq, T), torch.float32)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    _need(dq, "dq", q.shape, q.dtype)
-    _need(dk, "dk", k.shape, k.dtype)
-    _need(dv, "dv", v.shape, v.dtype)
+    gdt = torch.float32 if grad_fp32 else q.dtype
+    dq = torch.empty(q.shape, dtype=gdt, device=q.device) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=gdt, device=k.device) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=gdt, device=v.device) if dv is None else dv
+    _need(dq, "dq", q.shape, gdt)
+    _need(dk, "dk", k.shape, gdt)
+    _need(dv, "dv", v.shape, gdt)
     need = bwd_workspace_size(q, k, heads_k_stride)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     cu_p, nseq, _keep = _cu_host(cu_seqlens)
-    dims = make_dims(q, k, nseq, heads_k_stride)
+    dims = make_dims(q, k, nseq, heads_k_stride, grad_fp32)
     _check("ringattn_bwd", library().ringattn_bwd(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
         dout.data_ptr(), cu_p, dims, int(num_shards), int(shard_layout), int(bool(causal)),
@@ -250,21 +257,33 @@ def ringattn_get_status(stream=None) -> int:
     return int(library().ringattn_get_status(_stream(stream)))
 
 
+def _plan(fn_name, item_fields, total_tokens, hq, hkv, num_shards, shard_layout, causal,
+          cu_seqlens, heads_k_stride):
+    cu_p, nseq, _keep = _cu_host(cu_seqlens)
+    dims = ra_dims(total_tokens, nseq, hq, hkv, 64, RA_FP32, heads_k_stride, 0)
+    ni, ns = ctypes.c_int(0), ctypes.c_int(0)
+    fn = getattr(library(), fn_name)
+    code = fn(cu_p, dims, num_shards, shard_layout, int(bool(causal)), None, 0, None, 0,
+              ctypes.byref(ni), ctypes.byref(ns))
+    if code not in (0, -6):
+        raise RingAttnError(fn_name, code)
+    items = np.zeros((max(ni.value, 1), item_fields), np.int32)
+    segs = np.zeros((max(ns.value, 1), PLAN_SEG_FIELDS), np.int32)
+    _check(fn_name, fn(cu_p, dims, num_shards, shard_layout, int(bool(causal)),
+                       items.ctypes.data_as(_i32p), items.shape[0], segs.ctypes.data_as(_i32p),
+                       segs.shape[0], ctypes.byref(ni), ctypes.byref(ns)))
+    return items[:ni.value], segs[:ns.value]
+
+
 def plan_fwd(total_tokens, hq, hkv, num_shards, shard_layout, causal, cu_seqlens=None,
              heads_k_stride=1):
     """Host-only: the forward work list as (items [n,16], segments [m,4]) int32 arrays."""
-    cu_p, nseq, _keep = _cu_host(cu_seqlens)
-    dims = ra_dims(total_tokens, nseq, hq, hkv, 64, RA_FP32, heads_k_stride)
-    ni, ns = ctypes.c_int(0), ctypes.c_int(0)
-    lib = library()
-    code = lib.ringattn_plan_fwd(cu_p, dims, num_shards, shard_layout, int(bool(causal)), None, 0,
-                                 None, 0, ctypes.byref(ni), ctypes.byref(ns))
-    if code not in (0, -6):
-        raise RingAttnError("ringattn_plan_fwd", code)
-    items = np.zeros((max(ni.value, 1), PLAN_ITEM_FIELDS), np.int32)
-    segs = np.zeros((max(ns.value, 1), PLAN_SEG_FIELDS), np.int32)
-    _check("ringattn_plan_fwd", lib.ringattn_plan_fwd(
-        cu_p, dims, num_shards, shard_layout, int(bool(causal)), items.ctypes.data_as(_i32p),
-        items.shape[0], segs.ctypes.data_as(_i32p), segs.shape[0], ctypes.byref(ni),
-        ctypes.byref(ns)))
-    return items[:ni.value], segs[:ns.value]
+    return _plan("ringattn_plan_fwd", PLAN_ITEM_FIELDS, total_tokens, hq, hkv, num_shards,
+                 shard_layout, causal, cu_seqlens, heads_k_stride)
+
+
+def plan_bwd(total_tokens, hq, hkv, num_shards, shard_layout, causal, cu_seqlens=None,
+             heads_k_stride=1):
+    """Host-only: the key-side backward work list (items [n,8], segments [m,4])."""
+    return _plan("ringattn_plan_bwd", PLAN_BWD_ITEM_FIELDS, total_tokens, hq, hkv, num_shards,
+                 shard_layout, causal, cu_seqlens, heads_k_stride)

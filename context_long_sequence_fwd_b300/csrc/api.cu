@@ -45,6 +45,12 @@ struct CachedPlan {
   PlanSegment* segs = nullptr;
   int32_t* cu = nullptr;
   cudaEvent_t last_use = nullptr;
+  // key-side backward schedule, built on the first backward call
+  BwdPlan bwd;
+  void* bwd_buf = nullptr;
+  BwdItem* bitems = nullptr;
+  BwdSegment* bsegs = nullptr;
+  bool has_bwd = false;
 };
 std::list<CachedPlan> g_plans;  // most recently used first
 
@@ -160,6 +166,7 @@ ra_status get_plan(int dev, const PlanInput& in, cudaStream_t stream, CachedPlan
       cudaEventDestroy(old.last_use);
     }
     cudaFree(old.buf);
+    if (old.bwd_buf) cudaFree(old.bwd_buf);
     cudaSetDevice(cur);
     g_plans.pop_back();
   }
@@ -192,6 +199,27 @@ ra_status get_plan(int dev, const PlanInput& in, cudaStream_t stream, CachedPlan
   (void)stream;
   g_plans.push_front(std::move(cp));
   *out = &g_plans.front();
+  return RA_OK;
+}
+
+// Adds the key-side backward schedule to a cached plan; caller holds g_mu.
+ra_status get_bwd_plan(CachedPlan* cp) {
+  if (cp->has_bwd) return RA_OK;
+  cp->bwd = build_bwd_plan(cp->key);
+  const size_t nb_items = cp->bwd.items.size() * sizeof(BwdItem);
+  const size_t nb_segs = cp->bwd.segs.size() * sizeof(BwdSegment);
+  const size_t off_segs = (nb_items + 255) & ~size_t(255);
+  if (cudaMalloc(&cp->bwd_buf, off_segs + nb_segs + 16) != cudaSuccess) return RA_ERR_CUDA;
+  char* b = static_cast<char*>(cp->bwd_buf);
+  cp->bitems = reinterpret_cast<BwdItem*>(b);
+  cp->bsegs = reinterpret_cast<BwdSegment*>(b + off_segs);
+  if ((nb_items && cudaMemcpy(cp->bitems, cp->bwd.items.data(), nb_items, cudaMemcpyHostToDevice)) ||
+      (nb_segs && cudaMemcpy(cp->bsegs, cp->bwd.segs.data(), nb_segs, cudaMemcpyHostToDevice))) {
+    cudaFree(cp->bwd_buf);
+    cp->bwd_buf = nullptr;
+    return RA_ERR_CUDA;
+  }
+  cp->has_bwd = true;
   return RA_OK;
 }
 
@@ -442,17 +470,74 @@ extern "C" {
 
 size_t ringattn_bwd_workspace_size(ra_dims dims) {
   if (dims.total_tokens < 0 || dims.hq < 1 || dims.head_dim < 1) return 0;
-  return fp32_o_bytes(dims) + lse_bytes(dims);
+  return lse_bytes(dims);  // D_i = dO_i . O_i, fp32 [Hq, T]
 }
 
 ra_status ringattn_bwd(const void* q, const void* k, const void* v, const void* out,
                        const float* lse, const void* dout, const int32_t* cu_seqlens,
                        ra_dims dims, int num_shards, int shard_layout, int causal, void* dq,
                        void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
-  (void)q; (void)k; (void)v; (void)out; (void)lse; (void)dout; (void)cu_seqlens; (void)dims;
-  (void)num_shards; (void)shard_layout; (void)causal; (void)dq; (void)dk; (void)dv;
-  (void)workspace; (void)workspace_bytes; (void)stream;
-  return RA_ERR_UNSUPPORTED;
+  PlanInput in;
+  ra_status st = check_problem(cu_seqlens, dims, num_shards, shard_layout, causal, &in);
+  if (st != RA_OK) return st;
+  if (dims.total_tokens == 0) return RA_OK;
+  if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv) return RA_ERR_INVALID_ARG;
+  for (const void* t : {q, k, v, out, dout, static_cast<const void*>(dq), static_cast<const void*>(dk),
+                        static_cast<const void*>(dv)})
+    if (!aligned16(t)) return RA_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < ringattn_bwd_workspace_size(dims) || !aligned16(workspace))
+    return RA_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev;
+  DeviceState* ds;
+  if ((st = current_device(&dev, &ds)) != RA_OK) return st;
+  Maps maps;
+  CUtensorMap map_do;
+  if ((st = prepare_maps(q, k, v, dims, &maps)) != RA_OK) return st;
+  if (dims.dtype == RA_BF16 && !encode_thd(&map_do, dout, dims.total_tokens, dims.hq, dims.head_dim))
+    return RA_ERR_CUDA;
+  CachedPlan* cp;
+  if ((st = get_plan(dev, in, static_cast<cudaStream_t>(stream), &cp)) != RA_OK) return st;
+  if ((st = get_bwd_plan(cp)) != RA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* Dvec = static_cast<float*>(workspace);
+  const bool f32 = dims.dtype == RA_FP32;
+  if (launch_bwd_preprocess(out, dout, f32, Dvec, dims.total_tokens, dims.hq, dims.head_dim, s) !=
+      cudaSuccess)
+    return RA_ERR_CUDA;
+  BwdParams p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.dout = dout;
+  p.lse = lse;
+  p.Dvec = Dvec;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.items = cp->items;
+  p.segs = cp->segs;
+  p.bitems = cp->bitems;
+  p.bsegs = cp->bsegs;
+  p.cu = cp->cu;
+  p.num_docs = static_cast<int>(cp->plan.cu.size()) - 1;
+  p.num_items = static_cast<int>(cp->plan.items.size());
+  p.num_bitems = static_cast<int>(cp->bwd.items.size());
+  p.T = dims.total_tokens;
+  p.hq = dims.hq;
+  p.hkv = dims.hkv;
+  p.D = dims.head_dim;
+  p.group = dims.hq / dims.hkv;
+  p.causal = causal ? 1 : 0;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(dims.head_dim));
+  p.scale_log2 = p.scale * 1.4426950408889634f;
+  p.grad_fp32 = (f32 || dims.grad_fp32) ? 1 : 0;
+  p.status = ds->status;
+  cudaError_t e = f32 ? launch_bwd_simt_fp32(p, s)
+                      : launch_bwd_tc_bf16(p, maps.q, maps.k, maps.v, map_do, s);
+  if (e != cudaSuccess) return RA_ERR_CUDA;
+  if (cudaEventRecord(cp->last_use, s) != cudaSuccess) return RA_ERR_CUDA;
+  return RA_OK;
 }
 
 ra_status attn_lse_merge(void* o_a, float* lse_a, const void* o_b, const float* lse_b, int rows,
@@ -526,6 +611,27 @@ ra_status ringattn_plan_fwd(const int32_t* cu_seqlens, ra_dims dims, int num_sha
   if (*num_items && items) std::memcpy(items, plan.items.data(), plan.items.size() * sizeof(PlanItem));
   if (*num_segments && segments)
     std::memcpy(segments, plan.segs.data(), plan.segs.size() * sizeof(PlanSegment));
+  return RA_OK;
+}
+
+ra_status ringattn_plan_bwd(const int32_t* cu_seqlens, ra_dims dims, int num_shards,
+                            int shard_layout, int causal, int32_t* items, int max_items,
+                            int32_t* segments, int max_segments, int* num_items,
+                            int* num_segments) {
+  PlanInput in;
+  ra_dims d = dims;
+  d.dtype = RA_FP32;
+  d.head_dim = 64;
+  ra_status st = check_problem(cu_seqlens, d, num_shards, shard_layout, causal, &in);
+  if (st != RA_OK) return st;
+  if (!num_items || !num_segments) return RA_ERR_INVALID_ARG;
+  const BwdPlan plan = build_bwd_plan(in);
+  *num_items = static_cast<int>(plan.items.size());
+  *num_segments = static_cast<int>(plan.segs.size());
+  if (*num_items > max_items || *num_segments > max_segments) return RA_ERR_WORKSPACE;
+  if (*num_items && items) std::memcpy(items, plan.items.data(), plan.items.size() * sizeof(BwdItem));
+  if (*num_segments && segments)
+    std::memcpy(segments, plan.segs.data(), plan.segs.size() * sizeof(BwdSegment));
   return RA_OK;
 }
 

@@ -1,0 +1,646 @@
+// bf16 ring-attention backward on the sm_103a tensor cores (tcgen05 + TMEM).
+//
+// With P_ij = exp(scale q_i.k_j - lse_i), dP_ij = dO_i . v_j and
+// D_i = dO_i . O_i (preprocess kernel):
+//   dS_ij = P_ij (dP_ij - D_i),
+//   dV_j = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j.
+// The sums over the ring are split by output, so no output is accumulated
+// with atomics and the result does not depend on scheduling:
+//
+//   bwd_dkdv_kernel  one CTA per 128-key tile of one key/value head.  It walks
+//     the query tiles that see the keys in ring order (at step s the keys of
+//     rank src sit on rank (src + s) mod P) and, for GQA, every query head of
+//     the group, accumulating dK and dV in TMEM (so they come out summed over
+//     the group).  Each query tile is split into two 64-row halves handled
+//     by two softmax warpgroups, so one half's elementwise work overlaps the
+//     other half's MMAs:
+//       S^T  = K Q_h^T        (M = 128 keys, N = 64 queries, K = D)
+//       dP^T = V dO_h^T
+//       dV  += P^T dO_h       (TS: P^T from TMEM, dO MN-major)
+//       dK  += dS^T Q_h       (TS: dS^T from TMEM, Q MN-major)
+//     TMEM: S^T_a 0-63, dP^T_a 64-127, S^T_b 128-191, dP^T_b 192-255,
+//     dV 256-383, dK 384-511; P^T and dS^T (bf16, two per column) overwrite
+//     the first 32 columns of their S^T / dP^T block.
+//
+//   bwd_dq_kernel  one CTA per 128-row query tile (the forward plan's tiles),
+//     walking its key ranges in ring order; each key tile is split into two
+//     64-key halves, one per softmax warpgroup:
+//       S  = Q K_h^T,  dP = dO V_h^T   (M = 128 queries, N = 64 keys)
+//       dQ += dS K_h                   (TS: dS from TMEM, K MN-major)
+//     TMEM: S_a 0-63, dP_a 64-127, S_b 128-191, dP_b 192-255, dQ 256-383.
+//
+// Roles in both kernels (384 threads): warp 0 TMA producer, warp 1 TMEM
+// allocation and the single MMA-issuing thread, warp 2 (dK/dV only) loads the
+// per-query-row values (lse, D, visible key range) of each stage, warps 4-7
+// and 8-11 the two softmax warpgroups.  Every barrier wait is bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "device_common.cuh"
+#include "launch.h"
+#include "sm103_ptx.cuh"
+
+namespace ra {
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kTile = 128;
+constexpr int kTileBytes = kTile * kD * 2;   // 32 KB
+constexpr int kHalfBytes = kTileBytes / 2;   // 128 rows x 64 columns
+constexpr int kRowsHalf = 64 * 128;          // byte offset of row 64 in a 64-column half
+constexpr int kThreads = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+
+constexpr uint32_t kIdescN64 = make_idesc_bf16(128, 64, false, false);    // S-type, K-major B
+constexpr uint32_t kIdescMN = make_idesc_bf16(128, 128, false, true);     // X += A_tmem * B(MN)
+
+// X[128 x 64] = A[128 x D] * B[64 x D]^T, both K-major; b_smem points at the
+// first of B's 64 rows inside a 128-row, 128-byte-swizzled tile.
+__device__ __forceinline__ void mma_rows_x_half(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+    mma_bf16_ss(d_tmem, make_sdesc_sw128(a_smem + off, 16, 1024),
+                make_sdesc_sw128(b_smem + off, 16, 1024), kIdescN64, kk > 0);
+  }
+}
+
+// X[128 x D] (+)= A_tmem[128 x 64] * B[64 x D]; B is 64 rows (the K
+// dimension) of a 128-row tile whose D values are contiguous (MN-major).
+__device__ __forceinline__ void mma_tmem_x_rows(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
+                                                bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < 64 / 16; ++kk) {
+    mma_bf16_ts(d_tmem, a_tmem + kk * 8, make_sdesc_sw128(b_smem + kk * 2048, kHalfBytes, 1024),
+                kIdescMN, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+__device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
+                                          int head, int row) {
+  tma_load_3d(dst, map, bar, 0, head, row);
+  tma_load_3d(dst + kHalfBytes, map, bar, 64, head, row);
+}
+
+// Stores 32 fp32 values (times `mul`) as fp32 at dst (16-byte aligned).
+__device__ __forceinline__ void store_f32x32(float* dst, const uint32_t (&u)[32], float mul) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    d[i] = make_float4(__uint_as_float(u[4 * i]) * mul, __uint_as_float(u[4 * i + 1]) * mul,
+                       __uint_as_float(u[4 * i + 2]) * mul, __uint_as_float(u[4 * i + 3]) * mul);
+}
+
+// Stores 32 fp32 values (times `mul`) as bf16 at dst (16-byte aligned).
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t (&u)[32], float mul) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    d[i] = make_uint4(pack_bf16x2(__uint_as_float(u[8 * i]) * mul, __uint_as_float(u[8 * i + 1]) * mul),
+                      pack_bf16x2(__uint_as_float(u[8 * i + 2]) * mul, __uint_as_float(u[8 * i + 3]) * mul),
+                      pack_bf16x2(__uint_as_float(u[8 * i + 4]) * mul, __uint_as_float(u[8 * i + 5]) * mul),
+                      pack_bf16x2(__uint_as_float(u[8 * i + 6]) * mul, __uint_as_float(u[8 * i + 7]) * mul));
+}
+
+// ============================================================== dK / dV
+
+constexpr int kKvStages = 2;
+struct RowInfo {
+  float lse2;  // lse_i * log2(e)
+  float Dv;    // D_i
+  int lo, hi;  // keys row i may see: [lo, hi); empty for rows outside the segment
+};
+constexpr int kOffK = 0;
+constexpr int kOffV = kTileBytes;
+constexpr int kOffStage = 2 * kTileBytes;                      // per stage: Q, dO
+constexpr int kStageBytes = 2 * kTileBytes;
+constexpr int kOffInfo = kOffStage + kKvStages * kStageBytes;  // per stage: 128 RowInfo + flag
+constexpr int kInfoBytes = 128 * sizeof(RowInfo) + 16;
+constexpr int kOffCtlKV = kOffInfo + kKvStages * ((kInfoBytes + 127) / 128 * 128);
+constexpr int kSmemKV = kOffCtlKV + 256 + 1024;
+
+struct CtlKV {
+  uint64_t kv_full;
+  uint64_t q_full[kKvStages];
+  uint64_t info_full[kKvStages];
+  uint64_t stage_empty[kKvStages];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t acc_full;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(CtlKV) <= 256, "control block");
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                    const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                    const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  CtlKV* ctl = reinterpret_cast<CtlKV*>(smem + kOffCtlKV);
+  volatile int* abort = &ctl->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const BwdItem it = p.bitems[blockIdx.x];
+  const int g = it.kv_head;
+  const int G = p.group;
+  const int kend = it.k0 + it.klen;
+
+  int n = 0;  // (query tile, head) pairs
+  for (int si = 0; si < it.seg_count; ++si) {
+    const BwdSegment sg = p.bsegs[it.seg_begin + si];
+    n += (sg.q1 - sg.q0 + kTile - 1) / kTile * G;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl->kv_full, 1);
+    for (int s = 0; s < kKvStages; ++s) {
+      mbar_init(&ctl->q_full[s], 1);
+      mbar_init(&ctl->info_full[s], 32);
+      mbar_init(&ctl->stage_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&ctl->s_full[x], 1);
+      mbar_init(&ctl->p_full[x], 128);
+    }
+    mbar_init(&ctl->acc_full, 1);
+    mbar_init(&ctl->mma_done, 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ---------------------------------------------------- TMA producer
+    if (elect_one_sync() && n > 0) {
+      tma_prefetch_map(&map_q);
+      tma_prefetch_map(&map_do);
+      mbar_arrive_expect_tx(&ctl->kv_full, 2 * kTileBytes);
+      load_tile(smem + kOffK, &map_k, &ctl->kv_full, g, it.k0);
+      load_tile(smem + kOffV, &map_v, &ctl->kv_full, g, it.k0);
+      int li = 0;
+      bool ok = true;
+      for (int si = 0; si < it.seg_count && ok; ++si) {
+        const BwdSegment sg = p.bsegs[it.seg_begin + si];
+        for (int i0 = sg.q0; i0 < sg.q1 && ok; i0 += kTile) {
+          for (int h = g * G; h < (g + 1) * G; ++h, ++li) {
+            const int slot = li % kKvStages;
+            if (li >= kKvStages &&
+                !mbar_wait(&ctl->stage_empty[slot], ((li / kKvStages) - 1) & 1, p.status, abort)) {
+              ok = false;
+              break;
+            }
+            uint8_t* st = smem + kOffStage + slot * kStageBytes;
+            mbar_arrive_expect_tx(&ctl->q_full[slot], 2 * kTileBytes);
+            load_tile(st, &map_q, &ctl->q_full[slot], h, i0);
+            load_tile(st + kTileBytes, &map_do, &ctl->q_full[slot], h, i0);
+          }
+        }
+      }
+      if (!ok) *abort = 1;
+      for (int s = 0; s < kKvStages && s < li; ++s) {
+        const int last = s + ((li - 1 - s) / kKvStages) * kKvStages;
+        mbar_wait(&ctl->q_full[s], (last / kKvStages) & 1, p.status, nullptr);
+      }
+      mbar_wait(&ctl->kv_full, 0, p.status, nullptr);
+    }
+  } else if (warp == 2) {
+    // -------------------------------------- per-row values of each stage
+    int li = 0;
+    bool ok = true;
+    for (int si = 0; si < it.seg_count && ok; ++si) {
+      const BwdSegment sg = p.bsegs[it.seg_begin + si];
+      for (int i0 = sg.q0; i0 < sg.q1 && ok; i0 += kTile) {
+        for (int h = g * G; h < (g + 1) * G; ++h, ++li) {
+          const int slot = li % kKvStages;
+          if (li >= kKvStages) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&ctl->stage_empty[slot], ((li / kKvStages) - 1) & 1,
+                                                   p.status, abort));
+            if (!ok) break;
+          }
+          RowInfo* info = reinterpret_cast<RowInfo*>(smem + kOffInfo + slot * ((kInfoBytes + 127) / 128 * 128));
+          bool full = true;
+          for (int r = lane; r < kTile; r += 32) {
+            const int i = i0 + r;
+            RowInfo ri{0.f, 0.f, 0, 0};
+            if (i < sg.q1) {
+              int ds, de;
+              doc_bounds(p.cu, p.num_docs, i, &ds, &de);
+              ri.lse2 = p.lse[(size_t)h * p.T + i] * kLog2e;
+              ri.Dv = p.Dvec[(size_t)h * p.T + i];
+              ri.lo = ds;
+              ri.hi = p.causal ? i + 1 : de;
+            }
+            // the tile needs no mask if every row is in the segment and sees
+            // every key of the tile
+            full = full && (i < sg.q1) && ri.lo <= it.k0 && ri.hi >= kend;
+            info[r] = ri;
+          }
+          full = __all_sync(0xffffffffu, full);
+          if (lane == 0) reinterpret_cast<int*>(info + kTile)[0] = full ? 1 : 0;
+          __syncwarp();
+          mbar_arrive(&ctl->info_full[slot]);
+        }
+      }
+    }
+    if (!ok) *abort = 1;
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA
+    if (elect_one_sync() && n > 0) {
+      const uint32_t sK = smem_u32(smem + kOffK), sV = smem_u32(smem + kOffV);
+      auto sQ = [&](int li) { return smem_u32(smem + kOffStage + (li % kKvStages) * kStageBytes); };
+      const uint32_t tS[2] = {tmem + 0, tmem + 128};
+      const uint32_t tdP[2] = {tmem + 64, tmem + 192};
+      const uint32_t tdV = tmem + 256, tdK = tmem + 384;
+      auto q_ready = [&](int li) {
+        return mbar_wait(&ctl->q_full[li % kKvStages], (li / kKvStages) & 1, p.status, abort);
+      };
+      // S^T and dP^T of half x of pair li
+      auto issue_s = [&](int li, int x) {
+        const uint32_t q = sQ(li) + x * kRowsHalf, dO = sQ(li) + kTileBytes + x * kRowsHalf;
+        mma_rows_x_half(tS[x], sK, q);
+        mma_rows_x_half(tdP[x], sV, dO);
+        mma_commit(&ctl->s_full[x]);
+      };
+      auto issue_acc = [&](int li, int x, bool accumulate) {
+        const uint32_t q = sQ(li) + x * kRowsHalf, dO = sQ(li) + kTileBytes + x * kRowsHalf;
+        mma_tmem_x_rows(tdV, tS[x], dO, accumulate);
+        mma_tmem_x_rows(tdK, tdP[x], q, accumulate);
+      };
+      bool ok = mbar_wait(&ctl->kv_full, 0, p.status, abort) && q_ready(0);
+      if (ok) {
+        tc_fence_after_sync();
+        issue_s(0, 0);
+        issue_s(0, 1);
+      }
+      for (int j = 0; j < n && ok; ++j) {
+        const bool more = j + 1 < n;
+        if (!(ok = mbar_wait(&ctl->p_full[0], j & 1, p.status, abort))) break;
+        tc_fence_after_sync();
+        issue_acc(j, 0, j > 0);
+        if (more) {
+          if (!(ok = q_ready(j + 1))) break;
+          tc_fence_after_sync();
+          issue_s(j + 1, 0);
+        }
+        if (!(ok = mbar_wait(&ctl->p_full[1], j & 1, p.status, abort))) break;
+        tc_fence_after_sync();
+        issue_acc(j, 1, true);
+        mma_commit(&ctl->stage_empty[j % kKvStages]);
+        if (more) issue_s(j + 1, 1);
+      }
+      if (ok) mma_commit(&ctl->acc_full);
+      if (!ok) *abort = 1;
+      mma_commit(&ctl->mma_done);
+      mbar_wait(&ctl->mma_done, 0, p.status, nullptr);
+    }
+  } else if (warp >= 4) {
+    // --------------------------------------------------- softmax halves
+    const int x = (warp - 4) >> 2;  // query-row half of each stage
+    const int quarter = warp & 3;
+    const int kr = quarter * 32 + lane;  // key row of the tile (TMEM lane)
+    const int j = it.k0 + kr;            // global key index
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_off + x * 128;
+    const uint32_t tdP = tS + 64;
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    for (int jj = 0; jj < n; ++jj) {
+      const int slot = jj % kKvStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->info_full[slot], (jj / kKvStages) & 1, p.status, abort));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_full[x], jj & 1, p.status, abort));
+      if (!ok) break;
+      tc_fence_after_sync();
+      const RowInfo* info = reinterpret_cast<const RowInfo*>(smem + kOffInfo + slot * ((kInfoBytes + 127) / 128 * 128));
+      const bool full = reinterpret_cast<const int*>(info + kTile)[0] != 0;
+      const RowInfo* hinfo = info + x * 64;
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t us[32], ud[32];
+        tmem_load_32(tS + c2 * 32, us);
+        tmem_load_32(tdP + c2 * 32, ud);
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const RowInfo ri = hinfo[c2 * 32 + c + e];
+            const bool vis = full || (j >= ri.lo && j < ri.hi);
+            const float pe = vis ? fast_exp2(fmaf(__uint_as_float(us[c + e]), sl2, -ri.lse2)) : 0.f;
+            pv[e] = pe;
+            dv[e] = pe * (__uint_as_float(ud[c + e]) - ri.Dv);
+          }
+          pp[c / 2] = pack_bf16x2(pv[0], pv[1]);
+          pd[c / 2] = pack_bf16x2(dv[0], dv[1]);
+        }
+        tmem_store_16(tS + c2 * 16, pp);
+        tmem_store_16(tdP + c2 * 16, pd);
+      }
+      tmem_store_wait();
+      tc_fence_before_sync();
+      mbar_arrive(&ctl->p_full[x]);
+    }
+    if (!ok) *abort = 1;
+    if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->acc_full, 0, p.status, abort));
+    tc_fence_after_sync();
+    // epilogue: half 0 writes dV, half 1 writes dK (times the softmax scale)
+    const uint32_t tAcc = tmem + lane_off + (x == 0 ? 256 : 384);
+    const size_t off = ((size_t)j * p.hkv + g) * kD;
+    void* dst = x == 0 ? p.dv : p.dk;
+    const float mul = x == 0 ? 1.f : p.scale;
+#pragma unroll
+    for (int c = 0; c < kD / 32; ++c) {
+      uint32_t u[32];
+      if (ok && n > 0) {
+        tmem_load_32(tAcc + c * 32, u);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) u[i] = 0u;
+      }
+      if (ok && kr < it.klen) {
+        if (p.grad_fp32)
+          store_f32x32(static_cast<float*>(dst) + off + c * 32, u, mul);
+        else
+          store_bf16x32(static_cast<__nv_bfloat16*>(dst) + off + c * 32, u, mul);
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================== dQ
+
+constexpr int kQStages = 2;
+constexpr int kOffQ = 0;
+constexpr int kOffDO = kTileBytes;
+constexpr int kOffKVq = 2 * kTileBytes;  // per stage: K, V
+constexpr int kOffCtlQ = kOffKVq + kQStages * 2 * kTileBytes;
+constexpr int kSmemQ = kOffCtlQ + 256 + 1024;
+
+struct CtlQ {
+  uint64_t qd_full;
+  uint64_t kv_full[kQStages];
+  uint64_t kv_empty[kQStages];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t acc_full;
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(CtlQ) <= 256, "control block");
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                  const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
+                  const BwdParams p) {
+  const PlanItem it = p.items[blockIdx.x >> 1];
+  const int tile = blockIdx.x & 1;
+  if (it.qlen[tile] == 0) return;  // whole CTA: this item has one query tile
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  CtlQ* ctl = reinterpret_cast<CtlQ*>(smem + kOffCtlQ);
+  volatile int* abort = &ctl->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int head = it.head[tile];
+  const int g = head / p.group;
+  const int q0 = it.q0[tile];
+
+  int n = 0;
+  for (int si = 0; si < it.seg_count; ++si) {
+    const PlanSegment sg = p.segs[it.seg_begin + si];
+    n += (sg.k1 - sg.k0 + kTile - 1) / kTile;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl->qd_full, 1);
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(&ctl->kv_full[s], 1);
+      mbar_init(&ctl->kv_empty[s], 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&ctl->s_full[x], 1);
+      mbar_init(&ctl->p_full[x], 128);
+    }
+    mbar_init(&ctl->acc_full, 1);
+    mbar_init(&ctl->mma_done, 1);
+    ctl->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (elect_one_sync() && n > 0) {
+      tma_prefetch_map(&map_k);
+      tma_prefetch_map(&map_v);
+      mbar_arrive_expect_tx(&ctl->qd_full, 2 * kTileBytes);
+      load_tile(smem + kOffQ, &map_q, &ctl->qd_full, head, q0);
+      load_tile(smem + kOffDO, &map_do, &ctl->qd_full, head, q0);
+      int li = 0;
+      bool ok = true;
+      for (int si = 0; si < it.seg_count && ok; ++si) {
+        const PlanSegment sg = p.segs[it.seg_begin + si];
+        for (int kt = sg.k0; kt < sg.k1; kt += kTile, ++li) {
+          const int slot = li % kQStages;
+          if (li >= kQStages &&
+              !mbar_wait(&ctl->kv_empty[slot], ((li / kQStages) - 1) & 1, p.status, abort)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + kOffKVq + slot * 2 * kTileBytes;
+          mbar_arrive_expect_tx(&ctl->kv_full[slot], 2 * kTileBytes);
+          load_tile(st, &map_k, &ctl->kv_full[slot], g, kt);
+          load_tile(st + kTileBytes, &map_v, &ctl->kv_full[slot], g, kt);
+        }
+      }
+      if (!ok) *abort = 1;
+      for (int s = 0; s < kQStages && s < li; ++s) {
+        const int last = s + ((li - 1 - s) / kQStages) * kQStages;
+        mbar_wait(&ctl->kv_full[s], (last / kQStages) & 1, p.status, nullptr);
+      }
+      mbar_wait(&ctl->qd_full, 0, p.status, nullptr);
+    }
+  } else if (warp == 1) {
+    if (elect_one_sync() && n > 0) {
+      const uint32_t sQ = smem_u32(smem + kOffQ), sdO = smem_u32(smem + kOffDO);
+      auto sK = [&](int li) { return smem_u32(smem + kOffKVq + (li % kQStages) * 2 * kTileBytes); };
+      const uint32_t tS[2] = {tmem + 0, tmem + 128};
+      const uint32_t tdP[2] = {tmem + 64, tmem + 192};
+      const uint32_t tdQ = tmem + 256;
+      auto kv_ready = [&](int li) {
+        return mbar_wait(&ctl->kv_full[li % kQStages], (li / kQStages) & 1, p.status, abort);
+      };
+      auto issue_s = [&](int li, int x) {
+        mma_rows_x_half(tS[x], sQ, sK(li) + x * kRowsHalf);
+        mma_rows_x_half(tdP[x], sdO, sK(li) + kTileBytes + x * kRowsHalf);
+        mma_commit(&ctl->s_full[x]);
+      };
+      bool ok = mbar_wait(&ctl->qd_full, 0, p.status, abort) && kv_ready(0);
+      if (ok) {
+        tc_fence_after_sync();
+        issue_s(0, 0);
+        issue_s(0, 1);
+      }
+      for (int j = 0; j < n && ok; ++j) {
+        const bool more = j + 1 < n;
+        if (!(ok = mbar_wait(&ctl->p_full[0], j & 1, p.status, abort))) break;
+        tc_fence_after_sync();
+        mma_tmem_x_rows(tdQ, tS[0], sK(j), j > 0);
+        if (more) {
+          if (!(ok = kv_ready(j + 1))) break;
+          tc_fence_after_sync();
+          issue_s(j + 1, 0);
+        }
+        if (!(ok = mbar_wait(&ctl->p_full[1], j & 1, p.status, abort))) break;
+        tc_fence_after_sync();
+        mma_tmem_x_rows(tdQ, tS[1], sK(j) + kRowsHalf, true);
+        mma_commit(&ctl->kv_empty[j % kQStages]);
+        if (more) issue_s(j + 1, 1);
+      }
+      if (ok) mma_commit(&ctl->acc_full);
+      if (!ok) *abort = 1;
+      mma_commit(&ctl->mma_done);
+      mbar_wait(&ctl->mma_done, 0, p.status, nullptr);
+    }
+  } else if (warp >= 4) {
+    const int x = (warp - 4) >> 2;  // key half of each tile
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int row = q0 + r;
+    const bool valid = r < it.qlen[tile];
+    int lo = 0, hi = 0;
+    float lse2 = 0.f, Dv = 0.f;
+    if (valid) {
+      int ds, de;
+      doc_bounds(p.cu, p.num_docs, row, &ds, &de);
+      lo = ds;
+      hi = p.causal ? row + 1 : de;
+      lse2 = p.lse[(size_t)head * p.T + row] * kLog2e;
+      Dv = p.Dvec[(size_t)head * p.T + row];
+    }
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_off + x * 128;
+    const uint32_t tdP = tS + 64;
+    const int mlo = it.mask_lo[tile], mhi = it.mask_hi[tile];
+    const float sl2 = p.scale_log2;
+    bool ok = true;
+    int jj = 0;
+    for (int si = 0; si < it.seg_count && ok; ++si) {
+      const PlanSegment sg = p.segs[it.seg_begin + si];
+      const int a = max(lo, sg.k0), b = min(hi, sg.k1);
+      const int full_lo = max(sg.k0, mlo), full_hi = min(sg.k1, mhi);
+      for (int kt = sg.k0; kt < sg.k1; kt += kTile, ++jj) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_full[x], jj & 1, p.status, abort));
+        if (!ok) break;
+        tc_fence_after_sync();
+        const int kb = kt + x * 64;  // first key of this half
+        const bool full = kb >= full_lo && kb + 64 <= full_hi;
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t us[32], ud[32];
+          tmem_load_32(tS + c2 * 32, us);
+          tmem_load_32(tdP + c2 * 32, ud);
+          uint32_t pd[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            float dv[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int key = kb + c2 * 32 + c + e;
+              const bool vis = full || (key >= a && key < b);
+              const float pe = vis ? fast_exp2(fmaf(__uint_as_float(us[c + e]), sl2, -lse2)) : 0.f;
+              dv[e] = pe * (__uint_as_float(ud[c + e]) - Dv);
+            }
+            pd[c / 2] = pack_bf16x2(dv[0], dv[1]);
+          }
+          tmem_store_16(tS + c2 * 16, pd);
+        }
+        tmem_store_wait();
+        tc_fence_before_sync();
+        mbar_arrive(&ctl->p_full[x]);
+      }
+    }
+    if (!ok) *abort = 1;
+    if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->acc_full, 0, p.status, abort));
+    tc_fence_after_sync();
+    // epilogue: half x writes columns [64 x, 64 x + 64) of its row of dQ
+    const size_t off = ((size_t)row * p.hq + head) * kD + x * 64;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      uint32_t u[32];
+      if (ok && n > 0) {
+        tmem_load_32(tmem + lane_off + 256 + x * 64 + c * 32, u);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) u[i] = 0u;
+      }
+      if (ok && valid) {
+        if (p.grad_fp32)
+          store_f32x32(static_cast<float*>(p.dq) + off + c * 32, u, p.scale);
+        else
+          store_bf16x32(static_cast<__nv_bfloat16*>(p.dq) + off + c * 32, u, p.scale);
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+bool g_configured = false;
+
+}  // namespace
+
+cudaError_t launch_bwd_tc_bf16(const BwdParams& p, const CUtensorMap& map_q,
+                               const CUtensorMap& map_k, const CUtensorMap& map_v,
+                               const CUtensorMap& map_do, cudaStream_t stream) {
+  if (!g_configured) {
+    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemKV);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemQ);
+    if (e != cudaSuccess) return e;
+    g_configured = true;
+  }
+  if (p.num_items > 0)
+    bwd_dq_kernel<<<2 * p.num_items, kThreads, kSmemQ, stream>>>(map_q, map_k, map_v, map_do, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (p.num_bitems > 0)
+    bwd_dkdv_kernel<<<p.num_bitems, kThreads, kSmemKV, stream>>>(map_q, map_k, map_v, map_do, p);
+  return cudaGetLastError();
+}
+
+}  // namespace ra

@@ -28,6 +28,32 @@ struct FwdParams {
   int* status;            // device status word (first error wins)
 };
 
+struct BwdParams {
+  const void* q;            // [T, Hq, D]
+  const void* k;            // [T, Hkv, D]
+  const void* v;            // [T, Hkv, D]
+  const void* dout;         // [T, Hq, D]
+  const float* lse;         // [Hq, T], natural log
+  const float* Dvec;        // [Hq, T]: D_i = dO_i . O_i
+  void* dq;                 // [T, Hq, D]
+  void* dk;                 // [T, Hkv, D]
+  void* dv;                 // [T, Hkv, D]
+  const PlanItem* items;    // forward plan: query tiles and their key ranges
+  const PlanSegment* segs;
+  const BwdItem* bitems;    // key tiles and their query ranges
+  const BwdSegment* bsegs;
+  const int32_t* cu;
+  int num_docs;
+  int num_items, num_bitems;
+  int T, hq, hkv, D;
+  int group;                // Hq / Hkv
+  int causal;
+  float scale;              // 1 / sqrt(D)
+  float scale_log2;         // scale * log2(e)
+  int grad_fp32;            // 1: dq, dk, dv are fp32, else bf16
+  int* status;
+};
+
 // Start and end of the document holding token t (binary search over cu).
 __device__ __forceinline__ void doc_bounds(const int32_t* cu, int num_docs, int t, int* start,
                                            int* end) {

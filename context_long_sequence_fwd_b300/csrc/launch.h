@@ -23,4 +23,18 @@ cudaError_t launch_lse_merge(const void* o_a, bool a_fp32, const float* lse_a, c
                              bool b_fp32, const float* lse_b, void* o_out, bool out_fp32,
                              float* lse_out, int rows, int heads, int D, cudaStream_t stream);
 
+// D_i = dO_i . O_i into Dvec [Hq, T] (O, dO fp32 when `fp32`, else bf16).
+cudaError_t launch_bwd_preprocess(const void* out, const void* dout, bool fp32, float* Dvec, int T,
+                                  int hq, int D, cudaStream_t stream);
+
+// bf16 backward on tcgen05 (D = 128): dQ (query-tile-major, over the forward
+// plan) and dK, dV (key-tile-major, over the backward plan).  Tensor maps as
+// for the forward, plus dout [T, Hq, D].
+cudaError_t launch_bwd_tc_bf16(const BwdParams& p, const CUtensorMap& map_q,
+                               const CUtensorMap& map_k, const CUtensorMap& map_v,
+                               const CUtensorMap& map_do, cudaStream_t stream);
+
+// fp32 backward on CUDA cores (D = 64 or 128).
+cudaError_t launch_bwd_simt_fp32(const BwdParams& p, cudaStream_t stream);
+
 }  // namespace ra

@@ -134,4 +134,57 @@ Plan build_fwd_plan(const PlanInput& in) {
   return plan;
 }
 
+BwdPlan build_bwd_plan(const PlanInput& in) {
+  BwdPlan plan;
+  if (in.T == 0) return plan;
+  const Docs docs{in.cu};
+  const int P = in.num_shards;
+  const int G = in.hq / in.hkv;
+  const int npass = in.hkv / in.heads_k_stride;
+  for (int pass = 0; pass < npass; ++pass) {
+    const size_t first_item = plan.items.size();
+    for (int g = pass * in.heads_k_stride; g < (pass + 1) * in.heads_k_stride; ++g) {
+      for (int src = 0; src < P; ++src) {
+        int kch[2][2], nk;
+        rank_chunks(in.T, P, in.layout, src, kch, &nk);
+        for (int c = 0; c < nk; ++c) {
+          for (int k0 = kch[c][0]; k0 < kch[c][1]; k0 += kTileRows) {
+            BwdItem it{};
+            it.k0 = k0;
+            it.klen = std::min(kTileRows, kch[c][1] - k0);
+            it.kv_head = g;
+            it.src = src;
+            it.seg_begin = static_cast<int32_t>(plan.segs.size());
+            const int k_last = k0 + it.klen - 1;
+            // queries that see some key of the tile: from the tile start
+            // (causal) or its first document's start, to the end of the last
+            // key's document
+            const int lo = in.causal ? k0 : docs.start(k0);
+            const int hi = docs.end(k_last);
+            int cost = 0;
+            for (int s = 0; s < P; ++s) {
+              const int r = (src + s) % P;
+              int qch[2][2], nq;
+              rank_chunks(in.T, P, in.layout, r, qch, &nq);
+              for (int qc = 0; qc < nq; ++qc) {
+                const int q0 = std::max(qch[qc][0], lo);
+                const int q1 = std::min(qch[qc][1], hi);
+                if (q0 >= q1) continue;  // fully masked at this step: skipped
+                plan.segs.push_back(BwdSegment{q0, q1, s, r});
+                cost += (q1 - q0 + kTileRows - 1) / kTileRows * G;
+              }
+            }
+            it.seg_count = static_cast<int32_t>(plan.segs.size()) - it.seg_begin;
+            it.cost = cost;
+            plan.items.push_back(it);
+          }
+        }
+      }
+    }
+    std::stable_sort(plan.items.begin() + first_item, plan.items.end(),
+                     [](const BwdItem& x, const BwdItem& y) { return x.cost > y.cost; });
+  }
+  return plan;
+}
+
 }  // namespace ra

@@ -48,6 +48,34 @@ struct Plan {
   std::vector<int32_t> cu;  // document offsets (copied to the device with the plan)
 };
 
+// Backward, key/value side: one CTA per 128-key tile of one key/value head.
+// Its query ranges come in ring order: at step s the K/V shard of rank `src`
+// sits on rank (src + s) mod P, whose queries contribute to its dK, dV.
+struct BwdItem {
+  int32_t k0;         // first key of the tile
+  int32_t klen;       // keys of the tile (<= 128; the tile stays in one chunk)
+  int32_t kv_head;
+  int32_t src;        // rank that holds the keys
+  int32_t seg_begin;  // query segments, in ring order
+  int32_t seg_count;
+  int32_t cost;       // (query tile, head) pairs visited
+  int32_t pad;
+};
+static_assert(sizeof(BwdItem) == 8 * 4, "BwdItem is 8 int32");
+
+// Queries [q0, q1) of rank `rank`, visited at ring step `step`.
+struct BwdSegment {
+  int32_t q0, q1, step, rank;
+};
+
+struct BwdPlan {
+  std::vector<BwdItem> items;
+  std::vector<BwdSegment> segs;
+};
+
+// Builds the key/value-side backward schedule.  `in` must have passed plan_check.
+BwdPlan build_bwd_plan(const PlanInput& in);
+
 // Key ranges [a, b) of the chunks rank r holds (one for CONTIGUOUS, two for
 // ZIGZAG, ascending).
 void rank_chunks(int T, int P, int layout, int r, int out[2][2], int* n);

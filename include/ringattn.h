@@ -81,6 +81,9 @@ typedef struct {
   int head_dim;       /* D: 64 or 128 (bf16 path: 128) */
   int dtype;          /* ra_dtype of q, k, v, out (and dout, dq, dk, dv) */
   int heads_k_stride; /* key/value heads per ring pass; 0 = 1 */
+  int grad_fp32;      /* backward only: 1 = dq, dk, dv are fp32 whatever dtype
+                         is (bf16 cannot hold gradients of magnitude >= 4 to
+                         within 1/64); 0 = they are in dtype */
 } ra_dims;
 
 /*
@@ -139,12 +142,16 @@ ra_status ringattn_fwd_stepwise_noalloc(const void* q, const void* k, const void
 /*
  * Ring-attention backward.  Inputs q, k, v, out, lse from the forward and
  * dout = dL/dout; outputs dq [T, Hq, D], dk and dv [T, Hkv, D] (summed over
- * the query heads of each GQA group), all in dims.dtype.  With
+ * the query heads of each GQA group), in dims.dtype, or fp32 when
+ * dims.grad_fp32 is set.  With
  * P_ij = exp(scale q_i.k_j - lse_i), D_i = dout_i . out_i:
  *   dv_j = sum_i P_ij dout_i,  dS_ij = P_ij (dout_i . v_j - D_i),
  *   dq_i = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i.
  * Needs a caller-owned device workspace of ringattn_bwd_workspace_size(dims)
- * bytes (fp32 dq accumulator and the D_i vector).
+ * bytes (the fp32 D_i vector, [Hq, T]).  dq accumulates in tensor memory
+ * over each query tile's whole ring, and dk, dv over each key tile's, so no
+ * output is accumulated with atomics and the result does not depend on the
+ * schedule.  bf16 runs on the tensor cores, fp32 on CUDA cores.
  */
 size_t ringattn_bwd_workspace_size(ra_dims dims);
 ra_status ringattn_bwd(const void* q, const void* k, const void* v, const void* out,
@@ -188,9 +195,22 @@ int ringattn_version(void);
  *            range a tile may skip masking in is [mask_lo, mask_hi))
  *   segment: k0, k1, step, src  (keys [k0, k1) of rank src at ring step)
  */
+#define RA_PLAN_BWD_ITEM_FIELDS 8
 #define RA_PLAN_ITEM_FIELDS 16
 #define RA_PLAN_SEG_FIELDS 4
 ra_status ringattn_plan_fwd(const int32_t* cu_seqlens, ra_dims dims, int num_shards,
+                            int shard_layout, int causal, int32_t* items, int max_items,
+                            int32_t* segments, int max_segments, int* num_items,
+                            int* num_segments);
+
+/*
+ * Host-only backward work list (key side): items of RA_PLAN_BWD_ITEM_FIELDS
+ * int32 (k0, klen, kv_head, src, seg_begin, seg_count, cost, pad) and
+ * segments of RA_PLAN_SEG_FIELDS int32 (q0, q1, step, rank: queries
+ * [q0, q1) of rank `rank` meet the tile's keys at ring step `step`).  Same
+ * return conventions as ringattn_plan_fwd.
+ */
+ra_status ringattn_plan_bwd(const int32_t* cu_seqlens, ra_dims dims, int num_shards,
                             int shard_layout, int causal, int32_t* items, int max_items,
                             int32_t* segments, int max_segments, int* num_items,
                             int* num_segments);

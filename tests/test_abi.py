@@ -52,7 +52,7 @@ def test_status_strings_and_version(lib):
 
 
 def dims(T=256, hq=2, hkv=2, d=128, dtype=ra.RA_BF16, hks=1, nseq=0):
-    return ra.ra_dims(T, nseq, hq, hkv, d, dtype, hks)
+    return ra.ra_dims(T, nseq, hq, hkv, d, dtype, hks, 0)
 
 
 def test_argument_errors_without_gpu(lib):
@@ -82,4 +82,4 @@ def test_argument_errors_without_gpu(lib):
 def test_workspace_sizes(lib):
     d = dims(T=1024, hq=4, hkv=2)
     assert lib.ringattn_fwd_stepwise_workspace_size(d) >= 2 * (1024 * 4 * 128 * 4 + 4 * 1024 * 4)
-    assert lib.ringattn_bwd_workspace_size(d) >= 1024 * 4 * 128 * 4
+    assert lib.ringattn_bwd_workspace_size(d) >= 4 * 1024 * 4   # the D_i vector

@@ -1,0 +1,133 @@
+"""GPU parity of the ring-attention backward against the fp64 oracle.
+
+The GPU backward takes the GPU forward's O and lse (as a training step does);
+the oracle computes dQ, dK, dV from the definition of attention, with D_i as
+sum_j P_ij dP_ij (not via O).  Small cases are compared element by element;
+the full 64K-token workload on sampled query rows (dQ) and on the last keys
+of two key/value heads (dK, dV), which the oracle can afford one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import context_long_sequence_fwd_b300 as ra
+import oracle
+from context_long_sequence_fwd_b300.workloads import WORKLOADS, make_inputs, make_qkv
+from tests._util import TOL_BF16_O, max_err, nan_like, sample_rows, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+# fp32 gradients sum up to a few thousand fp32 products of magnitude ~10:
+# the accumulated rounding stays well below 1e-4
+TOL_FP32_GRAD = 1e-4
+TOL_BF16_GRAD = TOL_BF16_O
+
+
+def run_fwd_bwd(q, k, v, do, cu, P, layout, causal, hks=1, grad_fp32=False):
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    out, lse = ra.ringattn_fwd(qd, kd, vd, cu, P, layout, causal, heads_k_stride=hks)
+    gdt = torch.float32 if grad_fp32 else qd.dtype
+    dq, dk, dv = (torch.full(t.shape, float("nan"), dtype=gdt, device=DEV) for t in (qd, kd, vd))
+    ra.ringattn_bwd(qd, kd, vd, out, lse, dod, cu, P, layout, causal, dq, dk, dv,
+                    heads_k_stride=hks, grad_fp32=grad_fp32)
+    assert ra.ringattn_get_status() == 0
+    return to_np(dq), to_np(dk), to_np(dv)
+
+
+def bf16_output_bound(ref, tol):
+    """tol plus half a bf16 ulp of the exact value: the rounding a bf16 output
+    cannot avoid (gradients of magnitude >= 4 have ulps of 1/32 and more)."""
+    a = np.abs(ref)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return tol + np.where(a > 0, 2.0 ** (e - 8), 0.0)
+
+
+def check_full(q, k, v, do, cu, P, layout, causal, tol, hks=1, grad_fp32=False):
+    dq, dk, dv = run_fwd_bwd(q, k, v, do, cu, P, layout, causal, hks, grad_fp32)
+    rq, rk, rv, _, _ = oracle.attention_bwd(q, k, v, do, causal=causal, cu_seqlens=cu)
+    errs = (max_err(dq, rq), max_err(dk, rk), max_err(dv, rv))
+    if grad_fp32 or q.dtype == torch.float32:
+        assert max(errs) <= tol, errs
+    else:
+        for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+            assert np.all(np.abs(got - ref) <= bf16_output_bound(ref, tol)), errs
+    return errs
+
+
+FP32_CASES = [
+    (256, 2, 2, 64, 2, ra.CONTIGUOUS, False, None),       # the tiny fp32 workload's shape
+    (300, 4, 2, 64, 3, ra.CONTIGUOUS, True, None),
+    (512, 4, 2, 64, 4, ra.ZIGZAG, True, [0, 100, 100, 333, 512]),
+    (260, 2, 1, 128, 2, ra.ZIGZAG, True, None),
+]
+
+
+@pytest.mark.parametrize("case", FP32_CASES, ids=[str(i) for i in range(len(FP32_CASES))])
+def test_fp32_backward(case):
+    T, hq, hkv, d, P, layout, causal, cu = case
+    q, k, v, do = make_qkv(T, hq, hkv, d, "fp32", seed=4, with_dout=True)
+    check_full(q, k, v, do, cu, P, layout, causal, TOL_FP32_GRAD)
+
+
+BF16_CASES = [
+    # T, hq, hkv, P, layout, causal, cu
+    (256, 2, 2, 1, ra.CONTIGUOUS, False, None),
+    (1024, 2, 2, 2, ra.CONTIGUOUS, True, None),
+    (1024, 4, 2, 4, ra.ZIGZAG, True, None),
+    (1000, 2, 2, 2, ra.CONTIGUOUS, True, None),         # ragged tiles
+    (1040, 4, 1, 4, ra.ZIGZAG, True, None),             # zigzag chunks of 130, G = 4
+    (777 * 2, 3, 1, 2, ra.CONTIGUOUS, True, None),      # odd group, ragged tail
+    (1536, 8, 2, 3, ra.CONTIGUOUS, False, None),
+    (2048, 4, 2, 8, ra.CONTIGUOUS, True, [0, 300, 301, 900, 1500, 2048]),
+    (2048, 4, 4, 2, ra.ZIGZAG, False, [0, 128, 640, 641, 2048]),
+    (1024, 2, 2, 2, ra.CONTIGUOUS, True, [0, 200, 200, 700, 1024]),
+]
+
+
+@pytest.mark.parametrize("grad_fp32", [True, False], ids=["fp32grad", "bf16grad"])
+@pytest.mark.parametrize("case", BF16_CASES, ids=[str(i) for i in range(len(BF16_CASES))])
+def test_bf16_backward(case, grad_fp32):
+    """bf16 inputs, fp32 accumulation.  With fp32 gradient outputs the strict
+    max-abs bound holds; bf16 outputs add their own rounding."""
+    T, hq, hkv, P, layout, causal, cu = case
+    q, k, v, do = make_qkv(T, hq, hkv, 128, "bf16", seed=12, with_dout=True)
+    check_full(q, k, v, do, cu, P, layout, causal, TOL_BF16_GRAD, grad_fp32=grad_fp32)
+
+
+def test_bwd_layout_and_stride_invariance():
+    T, hq, hkv = 2048, 8, 4
+    q, k, v, do = make_qkv(T, hq, hkv, 128, "bf16", seed=6, with_dout=True)
+    ref = run_fwd_bwd(q, k, v, do, None, 1, ra.CONTIGUOUS, True)
+    for P, layout, hks in [(4, ra.ZIGZAG, 2), (8, ra.CONTIGUOUS, 4)]:
+        got = run_fwd_bwd(q, k, v, do, None, P, layout, True, hks)
+        for a, b in zip(got, ref):
+            assert max_err(a, b) <= 3e-2
+
+
+def test_causal_gqa_fwdbwd_t65536_p8_zigzag():
+    """Full 64K workload: sampled dQ rows, the last 64 keys of kv heads 0 and 7."""
+    w = WORKLOADS["causal_gqa_fwdbwd_t65536_p8_zigzag"]
+    x = make_inputs(w, seed=0)
+    dq, dk, dv = run_fwd_bwd(x["q"], x["k"], x["v"], x["dout"], None, w.num_shards, w.layout,
+                             w.causal, grad_fp32=True)
+    T = w.total_tokens
+    C = T // (2 * w.num_shards)
+    hs, is_ = sample_rows(T, w.hq, 96, 7, [0, C - 1, C, T - 1])
+    rq, _, _ = oracle.bwd_rows(x["q"], x["k"], x["v"], x["dout"], hs, is_, causal=True)
+    assert max_err(dq[is_, hs], rq) <= TOL_BF16_GRAD
+    keys = np.arange(T - 64, T)
+    gs = np.repeat(np.array([0, w.hkv - 1], np.int32), keys.size)
+    js = np.tile(keys.astype(np.int32), 2)
+    rk, rv = oracle.bwd_keys(x["q"], x["k"], x["v"], x["dout"], gs, js, causal=True)
+    assert max_err(dk[js, gs], rk) <= TOL_BF16_GRAD
+    assert max_err(dv[js, gs], rv) <= TOL_BF16_GRAD
+    for t in (dq, dk, dv):
+        assert np.all(np.isfinite(t))
+
+
+def test_bwd_unsupported_is_loud():
+    q = torch.zeros(256, 2, 64, dtype=torch.bfloat16, device=DEV)
+    lse = torch.zeros(2, 256, device=DEV)
+    with pytest.raises(ra.RingAttnError) as e:
+        ra.ringattn_bwd(q, q, q, q, lse, q, None, 2, ra.CONTIGUOUS, True)
+    assert e.value.code == -3

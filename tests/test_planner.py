@@ -180,3 +180,36 @@ def test_bad_cu_seqlens_rejected(cu):
 def test_empty_sequence_plan():
     items, segs = ra.plan_fwd(0, 2, 2, 2, ra.CONTIGUOUS, True)
     assert len(items) == 0 and len(segs) == 0
+
+
+def check_bwd_plan(T, hq, hkv, P, layout, causal, cu, hks=1):
+    items, segs = ra.plan_bwd(T, hq, hkv, P, layout, causal, cu, heads_k_stride=hks)
+    doc = doc_index(T, cu)
+    seen = np.zeros((hkv, T), np.int64)
+    for k0, klen, g, src, sb, sc, cost, _ in items:
+        assert 1 <= klen <= TILE
+        assert any(a <= k0 and k0 + klen <= b for a, b in rank_chunks(T, P, layout, src))
+        seen[g, k0:k0 + klen] += 1
+        my = segs[sb:sb + sc]
+        assert np.all(np.diff(my[:, 2]) >= 0), "segments out of ring order"
+        for q0, q1, step, rank in my:
+            assert rank == (src + step) % P
+            assert any(a <= q0 and q1 <= b for a, b in rank_chunks(T, P, layout, rank))
+        rows = np.concatenate([np.arange(q0, q1) for q0, q1, _, _ in my])
+        assert len(np.unique(rows)) == len(rows), "a query row is visited twice"
+        assert cost == sum((q1 - q0 + TILE - 1) // TILE for q0, q1, _, _ in my) * (hq // hkv)
+        # every query that sees a key of the tile is visited, and no other
+        need = np.zeros(T, bool)
+        for j in range(k0, k0 + klen):
+            for i in range(T):
+                if doc[i] == doc[j] and (not causal or j <= i):
+                    need[i] = True
+        got = np.zeros(T, bool)
+        got[rows] = True
+        assert np.array_equal(need, got)
+    assert np.all(seen == 1), "every key of every kv head in exactly one tile"
+
+
+@pytest.mark.parametrize("case", CASES[:8], ids=[str(i) for i in range(8)])
+def test_bwd_plan_covers_exactly_the_mask(case):
+    check_bwd_plan(*case)
