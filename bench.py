@@ -2,18 +2,19 @@
 """Ring-attention throughput on B300: causal-effective TFLOP/s and % of the
 dense BF16 tensor peak.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--pass P]
     python bench.py --impl reference ...      # the fp64 CPU oracle, timed
 
-A step is one pass of the ring-attention hot path over one batch of seeded
-synthetic input of the named workload (default: causal GQA, 32 query / 8
-key-value heads of dimension 128, 32768 tokens, 8 zigzag shards -- the shape
-the 60 % target is quoted on).  Forward workloads run the fused forward;
-the fwd+bwd workload runs forward then backward.  Inputs (q, k, v: 400 MB at
-the default) are larger than the 126 MB L2, so no flush is needed between
-steps.  N > 1 GPUs run independent replicas (one process per GPU, launched by
-torchrun); the value is the sum over ranks of the work divided by the
-slowest rank's time.
+A step is one pass of the whole ring-attention hot path over one batch of
+seeded synthetic input: the fused forward (planner work list, tile kernel,
+in-kernel log-sum-exp merge, epilogue) and then the backward (preprocess,
+dQ and dK/dV tile kernels).  The default workload is the causal GQA shape
+the 60 % forward target is quoted on: 32 query / 8 key-value heads of
+dimension 128, 32768 tokens, 8 zigzag shards.  ``--pass fwd`` times the
+forward alone.  Inputs (q, k, v, dO: 670 MB at the default) are larger than
+the 126 MB L2, so no flush is needed between steps.  N > 1 GPUs run
+independent replicas (one process per GPU, launched by torchrun); the value
+is the sum over ranks of the work divided by the slowest rank's time.
 
 Prints one JSON line (rank 0).
 """
@@ -71,12 +72,18 @@ def load_peaks():
     return d
 
 
-def kernel_traffic(kernel_file: str, workload: str):
+KERNEL_SOURCES = {"fwd_tc_bf16_kernel": "fwd_tc_bf16.cu", "bwd_dkdv_kernel": "bwd_tc_bf16.cu",
+                  "bwd_dq_kernel": "bwd_tc_bf16.cu"}
+
+
+def kernel_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary of this kernel and
-    workload, if the kernel source is unchanged since the capture."""
-    src = os.path.join(ROOT, "context_long_sequence_fwd_b300", "csrc", kernel_file)
-    summ = os.path.join(ROOT, "profiles", f"{kernel_file.split('.')[0]}_{workload}.md")
-    if not (os.path.exists(src) and os.path.exists(summ)):
+    workload (profiles/<kernel>_<workload>.md), or None if there is none or
+    the kernel's source file has changed since the capture."""
+    src = os.path.join(ROOT, "context_long_sequence_fwd_b300", "csrc",
+                       KERNEL_SOURCES.get(kernel, ""))
+    summ = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not (os.path.isfile(src) and os.path.exists(summ)):
         return None
     digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     vals = {}
@@ -186,14 +193,23 @@ def max_over_ranks(x: float, world: int) -> float:
 
 # ------------------------------------------------------------- CPU oracle
 
-def oracle_sample(w, inputs, budget_s: float, seed: int):
-    """Times the fp64 oracle on a bounded sample of the workload's rows and
-    returns (flops_done, seconds, rows, threads)."""
+def oracle_sample(w, inputs, budget_s: float, seed: int, backward: bool):
+    """Times the fp64 oracle on a bounded sample of the workload and returns
+    (flops, seconds, description, threads).
+
+    The sample is random (head, row) outputs: forward rows (O, lse), and for a
+    fwd+bwd pass as many backward rows (dQ, with the row's lse and D).  Each
+    output is credited with the algorithmic FLOPs it stands for, per visible
+    key: 4 D for a forward row (Q K^T and P V), 6 D for a dQ row (Q K^T, dO V^T
+    and dS K).  The key side of the backward (dK, dV) is not sampled: the
+    oracle computes it per key only after the row statistics of every query
+    that sees the key, which makes one sampled key cost O(T^2)."""
     import oracle
     cu = inputs["cu_seqlens"]
     T = w.total_tokens
-    if "q64" not in inputs:          # widen once, outside the timed calls
-        for n in ("q", "k", "v"):
+    names = ("q", "k", "v", "dout") if backward else ("q", "k", "v")
+    for n in names:                   # widen once, outside the timed calls
+        if n + "64" not in inputs:
             inputs[n + "64"] = np.ascontiguousarray(inputs[n].float().numpy(), np.float64)
     r = np.random.default_rng(seed)
     bounds = [0, T] if cu is None else [int(x) for x in cu]
@@ -203,25 +219,47 @@ def oracle_sample(w, inputs, budget_s: float, seed: int):
         starts[a:b] = a
         ends[a:b] = b
 
-    def run(n):
+    def pick(n):
         hs = r.integers(0, w.hq, n).astype(np.int32)
         is_ = r.integers(0, T, n).astype(np.int32)
         nvis = (is_ + 1 - starts[is_]) if w.causal else (ends[is_] - starts[is_])
+        return hs, is_, float(nvis.sum())
+
+    def run_fwd(n):
+        hs, is_, vis = pick(n)
         t0 = time.perf_counter()
         oracle.fwd_rows(inputs["q64"], inputs["k64"], inputs["v64"], hs, is_,
                         causal=w.causal, cu_seqlens=cu)
-        dt = time.perf_counter() - t0
-        # QK^T and PV per visible key: 4 D flops (the same convention as the GPU count)
-        return 4.0 * w.head_dim * float(nvis.sum()), dt, n
+        return 4.0 * w.head_dim * vis, time.perf_counter() - t0
 
-    f0, t0, n0 = run(64)                      # calibrate
-    per_row = max(t0 / 64, 1e-6)
-    n = int(min(max(budget_s / per_row, 64), 200000))
-    f1, t1, n1 = run(n)
-    return f1, t1, n1, oracle.num_threads()
+    def run_bwd(n):
+        hs, is_, vis = pick(n)
+        t0 = time.perf_counter()
+        oracle.bwd_rows(inputs["q64"], inputs["k64"], inputs["v64"], inputs["dout64"], hs, is_,
+                        causal=w.causal, cu_seqlens=cu)
+        return 6.0 * w.head_dim * vis, time.perf_counter() - t0
+
+    parts = [("forward rows", run_fwd)] + ([("dQ rows", run_bwd)] if backward else [])
+    flops, secs, desc = 0.0, 0.0, []
+    for name, fn in parts:
+        f0, t0 = fn(32)                               # calibrate
+        n = int(min(max(budget_s / len(parts) / max(t0 / 32, 1e-6), 32), 200000))
+        f1, t1 = fn(n)
+        flops += f1
+        secs += t1
+        desc.append(f"{n} {name}")
+    return flops, secs, ", ".join(desc), oracle.num_threads()
 
 
 # ----------------------------------------------------------------- ours
+
+# Algorithmic FLOPs of one launch of each kernel, in units of the forward's
+# causal-effective FLOPs (2 matmuls per visible pair).  The backward's five
+# matmuls (2.5 forward) are split between its two tile kernels by output: the
+# dK/dV kernel owns S, dP, dV and dK; the dQ kernel owns dQ (it recomputes S
+# and dP, which is overhead, not algorithmic work).
+KERNEL_FWD_UNITS = {"fwd_tc_bf16_kernel": 1.0, "bwd_dkdv_kernel": 2.0, "bwd_dq_kernel": 0.5}
+
 
 def run_ours(args):
     import torch
@@ -237,13 +275,13 @@ def run_ours(args):
     w = WORKLOADS[args.workload]
     if w.dtype != "bf16":
         raise SystemExit("the throughput bench runs the bf16 workloads")
-    x = make_inputs(w, seed=args.seed)
+    backward = args.pass_ == "fwdbwd"
+    x = make_inputs(w, seed=args.seed, with_dout=backward)
     cu = x["cu_seqlens"]
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
     out = torch.empty_like(q)
     lse = torch.empty(w.hq, w.total_tokens, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    backward = w.backward
     if backward:
         do = x["dout"].to(dev)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -266,6 +304,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     if ra.ringattn_get_status() != 0:
         raise SystemExit("kernel reported an error during warm-up")
+    ra.trace_collect()  # drop anything recorded before the timed region
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
@@ -274,6 +313,7 @@ def run_ours(args):
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize()
+    ra.trace_enable(True)
     with ClockSampler(local) as clocks:
         t_start.record(stream)
         for i in range(args.steps):
@@ -286,13 +326,16 @@ def run_ours(args):
                 evb[i][1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
+    ra.trace_enable(False)
     barrier(world)
+    kernels = ra.trace_collect()
     status = ra.ringattn_get_status()
     ms_total = t_start.elapsed_time(t_end)
     ms_total = max_over_ranks(ms_total, world)
     fwd_ms = [a.elapsed_time(b) for a, b in ev]
     bwd_ms = [a.elapsed_time(b) for a, b in evb]
     clk = clocks.summary()
+    peak_mem = torch.cuda.max_memory_allocated(dev)
 
     # end to end through the public API from pinned host memory
     hq_, hk_, hv_ = (x[n].pin_memory() for n in ("q", "k", "v"))
@@ -338,94 +381,110 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        f, t, n, thr = oracle_sample(w, x, args.cpu_budget, args.seed)
-        cpu = {"value": f / t / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-               "sample": f"{n} random (head, row) outputs of the workload, fp64, {t:.1f} s"}
+        f, t, desc, thr = oracle_sample(w, x, args.cpu_budget, args.seed, backward)
+        cpu = {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": thr,
+               "kind": "oracle",
+               "sample": f"{desc} of the workload (random head and row), fp64, {t:.1f} s"}
 
     if rank != 0:
         return
     peaks = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    peak_s = float(peaks["bf16_tflops_sustained"])
     ms_step = ms_total / args.steps
     value = world * f_step / (ms_step * 1e-3) / 1e12
-    fwd_mean = statistics.mean(fwd_ms)
-    achieved = f_fwd / (fwd_mean * 1e-3) / 1e12
-    peak = float(peaks["bf16_tflops"])
-    roof = {"bound": "tensor", "kernel": "fwd_tc_bf16_kernel", "achieved": round(achieved, 2),
-            "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+
+    # per-kernel device time over the timed region (CUDA events on the launch stream)
+    ktab = {}
+    k_total = sum(ms for _, ms in kernels.values()) or 1.0
+    for name, (n, ms) in sorted(kernels.items(), key=lambda kv: -kv[1][1]):
+        ent = {"launches": n, "avg_ms": round(ms / n, 4), "share": round(ms / k_total, 4)}
+        if name in KERNEL_FWD_UNITS:
+            ent["tflops"] = round(KERNEL_FWD_UNITS[name] * f_fwd / (ms / n * 1e-3) / 1e12, 2)
+        ktab[name] = ent
+    top = max((n for n in ktab if n in KERNEL_FWD_UNITS), key=lambda n: ktab[n]["share"])
+    achieved = ktab[top]["tflops"]
+    roof = {"bound": "tensor", "kernel": top, "achieved": achieved, "peak": peak,
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
             "peak_source": f"{peaks['source']} bf16_tflops (burst)",
-            "frac_of_sustained": round(achieved / float(peaks["bf16_tflops_sustained"]), 4),
-            "traffic": kernel_traffic("fwd_tc_bf16.cu", args.workload),
-            "flops_per_launch": f_fwd}
-    launches_per_step = 1 + (0 if not backward else BWD_LAUNCHES)
+            "frac_of_sustained": round(achieved / peak_s, 4),
+            "traffic": kernel_traffic(top, args.workload),
+            "flops_per_launch": KERNEL_FWD_UNITS[top] * f_fwd}
+    fwd_mean = statistics.mean(fwd_ms)
+    fwd_tf = f_fwd / (fwd_mean * 1e-3) / 1e12
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
+        "data": "synthetic (seeded N(0,1) q, k, v, dO rounded to bf16)",
         "config": {"workload": args.workload, "total_tokens": w.total_tokens, "hq": w.hq,
                    "hkv": w.hkv, "head_dim": w.head_dim, "num_shards": w.num_shards,
                    "layout": "zigzag" if w.layout == 1 else "contiguous",
                    "causal": w.causal, "varlen_docs": None if cu is None else len(cu) - 1,
-                   "pass": "fwd+bwd" if backward else "fwd",
-                   "flops_per_step": f_step, "visible_pairs_per_head": visible_pairs(w, cu),
+                   "pass": args.pass_, "flops_per_step": f_step,
+                   "visible_pairs_per_head": visible_pairs(w, cu),
                    "parallelism": f"replicas{world}" if world > 1 else "1gpu",
-                   "l2": "inputs larger than L2 (q,k,v %.0f MB), no flush" %
-                         (sum(t.numel() * t.element_size() for t in (q, k, v)) / 1e6),
+                   "l2": "inputs larger than L2 (%.0f MB read per step), no flush" %
+                         (sum(t.numel() * t.element_size() for t in (q, k, v)) / 1e6 +
+                          (2 * do.numel() * do.element_size() / 1e6 if backward else 0)),
                    "seed": args.seed},
-        "pct_of_peak": round(100 * achieved / peak, 2),
-        "fwd_ms": round(fwd_mean, 4),
+        "fwd": {"ms": round(fwd_mean, 4), "tflops": round(fwd_tf, 2),
+                "frac": round(fwd_tf / peak, 4), "frac_of_sustained": round(fwd_tf / peak_s, 4)},
         "roofline": roof,
+        "kernels": ktab,
         "cpu_baseline": cpu,
         "e2e": {"value": round(world * f_step / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": sum(n for n, _ in kernels.values()),
         "clocks": clk,
+        "peak_mem_gb": round(peak_mem / 1e9, 3),
         "status": ra.STATUS.get(status, status),
     }
     if backward:
         bm = statistics.mean(bwd_ms)
-        line["bwd_ms"] = round(bm, 4)
-        line["bwd_tflops"] = round(2.5 * f_fwd / (bm * 1e-3) / 1e12, 2)
+        bt = 2.5 * f_fwd / (bm * 1e-3) / 1e12
+        line["bwd"] = {"ms": round(bm, 4), "tflops": round(bt, 2), "frac": round(bt / peak, 4),
+                       "frac_of_sustained": round(bt / peak_s, 4)}
     print(json.dumps(line), flush=True)
-
-
-BWD_LAUNCHES = 3  # preprocess, dK/dV(/dQ) tile kernel, dQ convert
 
 
 # ------------------------------------------------------------- reference
 
 def run_reference(args):
+    """The oracle as it stands, on the host cores, on bounded samples of the
+    same workload and pass (the reference arm of the comparison)."""
     from context_long_sequence_fwd_b300.workloads import WORKLOADS, make_inputs
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     w = WORKLOADS[args.workload]
-    x = make_inputs(w, seed=args.seed)
+    backward = args.pass_ == "fwdbwd"
+    x = make_inputs(w, seed=args.seed, with_dout=backward)
     budget = max(0.5, min(args.cpu_budget, 150.0 / max(1, args.steps + args.warmup)))
     for i in range(args.warmup):
-        oracle_sample(w, x, min(budget, 1.0), args.seed + 1000 + i)
-    fl, ts, rows, thr = 0.0, 0.0, 0, 1
+        oracle_sample(w, x, min(budget, 1.0), args.seed + 1000 + i, backward)
+    fl, ts, descs, thr = 0.0, 0.0, [], 1
     for i in range(args.steps):
-        f, t, n, thr = oracle_sample(w, x, budget, args.seed + i)
+        f, t, desc, thr = oracle_sample(w, x, budget, args.seed + i, backward)
         fl += f
         ts += t
-        rows += n
+        descs.append(desc)
     value = fl / ts / 1e12
-    f_step = fwd_flops(w, x["cu_seqlens"])
+    f_step = fwd_flops(w, x["cu_seqlens"]) * (3.5 if backward else 1.0)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(f_step / (value * 1e12) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic",
+        "data": "synthetic (seeded N(0,1) q, k, v, dO rounded to bf16)",
         "config": {"workload": args.workload, "total_tokens": w.total_tokens, "hq": w.hq,
                    "hkv": w.hkv, "head_dim": w.head_dim, "num_shards": w.num_shards,
-                   "pass": "fwd", "sampled": True},
+                   "pass": args.pass_, "sampled": True},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-                         "sample": f"{rows} random (head, row) outputs over {args.steps} steps, "
-                                   f"{ts:.1f} s"},
+                         "sample": f"per step: {descs[0]} (random head and row); "
+                                   f"{args.steps} steps, {ts:.1f} s"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -435,9 +494,11 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "fwdbwd"], default="fwdbwd",
+                    help="fwd: forward only; fwdbwd: forward then backward (the whole path)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=10.0,

@@ -8,7 +8,8 @@ compute function raises: there is no CPU fallback.
 
 Entry points (same names as the C ABI):
     ringattn_fwd, ringattn_fwd_stepwise, ringattn_bwd, attn_lse_merge,
-    ringattn_get_status, plan_fwd (host-only work-list introspection).
+    ringattn_get_status, plan_fwd / plan_bwd (host-only work-list
+    introspection), trace_enable / trace_collect (per-kernel device time).
 """
 from __future__ import annotations
 
@@ -55,6 +56,11 @@ class ra_dims(ctypes.Structure):
                 ("grad_fp32", ctypes.c_int)]
 
 
+class ra_trace_entry(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_char * 40), ("launches", ctypes.c_int),
+                ("total_ms", ctypes.c_double)]
+
+
 _vp = ctypes.c_void_p
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _ip = ctypes.POINTER(ctypes.c_int)
@@ -91,8 +97,11 @@ def library():
                                           ctypes.c_int, _i32p, ctypes.c_int, _i32p, ctypes.c_int,
                                           _ip, _ip]
         lib.ringattn_plan_bwd.argtypes = lib.ringattn_plan_fwd.argtypes
+        lib.ringattn_trace_enable.argtypes = [ctypes.c_int]
+        lib.ringattn_trace_collect.argtypes = [ctypes.POINTER(ra_trace_entry), ctypes.c_int, _ip]
         for fn in ("ringattn_fwd", "ringattn_fwd_stepwise", "ringattn_bwd", "attn_lse_merge",
-                   "ringattn_get_status", "ringattn_plan_fwd", "ringattn_plan_bwd"):
+                   "ringattn_get_status", "ringattn_plan_fwd", "ringattn_plan_bwd",
+                   "ringattn_trace_enable", "ringattn_trace_collect"):
             getattr(lib, fn).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -287,3 +296,19 @@ def plan_bwd(total_tokens, hq, hkv, num_shards, shard_layout, causal, cu_seqlens
     """Host-only: the key-side backward work list (items [n,8], segments [m,4])."""
     return _plan("ringattn_plan_bwd", PLAN_BWD_ITEM_FIELDS, total_tokens, hq, hkv, num_shards,
                  shard_layout, causal, cu_seqlens, heads_k_stride)
+
+
+def trace_enable(on: bool = True) -> None:
+    """Start (or stop) recording every kernel launch of the library between
+    two CUDA events on its launch stream."""
+    _check("ringattn_trace_enable", library().ringattn_trace_enable(int(bool(on))))
+
+
+def trace_collect() -> dict:
+    """Waits for the recorded launches; returns {kernel: (launches, total_ms)}
+    since the last collect and clears the record."""
+    n = ctypes.c_int(0)
+    buf = (ra_trace_entry * 64)()  # one entry per kernel name; the library has fewer
+    _check("ringattn_trace_collect", library().ringattn_trace_collect(buf, 64, ctypes.byref(n)))
+    return {buf[i].kernel.decode(): (int(buf[i].launches), float(buf[i].total_ms))
+            for i in range(n.value)}

@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 
 #include "launch.h"
+#include "trace.h"
 
 namespace ra {
 
@@ -69,6 +70,7 @@ cudaError_t launch_bwd_preprocess(const void* out, const void* dout, bool fp32, 
   if (rows == 0) return cudaSuccess;
   const long long threads = rows * (D / 8);
   const long long grid = (threads + 255) / 256;
+  TraceScope trace_scope(stream, "bwd_preprocess_kernel");
   if (fp32)
     bwd_preprocess_kernel<true><<<(unsigned)grid, 256, 0, stream>>>(out, dout, Dvec, T, hq, D, rows);
   else

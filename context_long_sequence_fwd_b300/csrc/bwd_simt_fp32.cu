@@ -14,6 +14,7 @@
 
 #include "device_common.cuh"
 #include "launch.h"
+#include "trace.h"
 
 namespace ra {
 
@@ -173,6 +174,7 @@ __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(BwdParams p) {
 
 cudaError_t launch_bwd_simt_fp32(const BwdParams& p, cudaStream_t stream) {
   if (p.num_items > 0) {
+    TraceScope trace_scope(stream, "bwd_dq_simt_kernel");
     if (p.D == 64)
       bwd_dq_simt_kernel<64><<<p.num_items, 256, 0, stream>>>(p);
     else
@@ -181,6 +183,7 @@ cudaError_t launch_bwd_simt_fp32(const BwdParams& p, cudaStream_t stream) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (p.num_bitems > 0) {
+    TraceScope trace_scope(stream, "bwd_dkdv_simt_kernel");
     if (p.D == 64)
       bwd_dkdv_simt_kernel<64><<<p.num_bitems, 128, 0, stream>>>(p);
     else

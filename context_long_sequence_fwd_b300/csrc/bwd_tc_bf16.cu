@@ -42,6 +42,7 @@
 #include "device_common.cuh"
 #include "launch.h"
 #include "sm103_ptx.cuh"
+#include "trace.h"
 
 namespace ra {
 
@@ -634,12 +635,16 @@ cudaError_t launch_bwd_tc_bf16(const BwdParams& p, const CUtensorMap& map_q,
     if (e != cudaSuccess) return e;
     g_configured = true;
   }
-  if (p.num_items > 0)
+  if (p.num_items > 0) {
+    TraceScope trace_scope(stream, "bwd_dq_kernel");
     bwd_dq_kernel<<<2 * p.num_items, kThreads, kSmemQ, stream>>>(map_q, map_k, map_v, map_do, p);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (p.num_bitems > 0)
+  if (p.num_bitems > 0) {
+    TraceScope trace_scope(stream, "bwd_dkdv_kernel");
     bwd_dkdv_kernel<<<p.num_bitems, kThreads, kSmemKV, stream>>>(map_q, map_k, map_v, map_do, p);
+  }
   return cudaGetLastError();
 }
 

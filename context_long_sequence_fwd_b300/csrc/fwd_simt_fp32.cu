@@ -14,6 +14,7 @@
 
 #include "device_common.cuh"
 #include "launch.h"
+#include "trace.h"
 
 namespace ra {
 
@@ -115,6 +116,7 @@ __global__ void __launch_bounds__(256) fwd_simt_fp32_kernel(FwdParams p) {
 
 cudaError_t launch_fwd_simt_fp32(const FwdParams& p, cudaStream_t stream) {
   if (p.num_items == 0) return cudaSuccess;
+  TraceScope trace_scope(stream, "fwd_simt_fp32_kernel");
   if (p.D == 64)
     fwd_simt_fp32_kernel<64><<<p.num_items, 256, 0, stream>>>(p);
   else

@@ -38,6 +38,7 @@
 #include "device_common.cuh"
 #include "launch.h"
 #include "sm103_ptx.cuh"
+#include "trace.h"
 
 namespace ra {
 
@@ -384,6 +385,7 @@ cudaError_t launch_fwd_tc_bf16(const FwdParams& p, const CUtensorMap& map_q,
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  TraceScope trace_scope(stream, "fwd_tc_bf16_kernel");
   fwd_tc_bf16_kernel<<<p.num_items, kThreads, kSmemBytes, stream>>>(map_q, map_k, map_v, p);
   return cudaGetLastError();
 }

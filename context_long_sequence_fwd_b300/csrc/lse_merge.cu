@@ -18,6 +18,7 @@
 #include <cmath>
 
 #include "launch.h"
+#include "trace.h"
 
 namespace ra {
 
@@ -119,6 +120,7 @@ cudaError_t launch_lse_merge(const void* o_a, bool a_fp32, const float* lse_a, c
   const long long threads = pairs * (D / 8);
   const int block = 256;
   const long long grid = (threads + block - 1) / block;
+  TraceScope trace_scope(stream, "lse_merge_kernel");
   lse_merge_kernel<<<(unsigned)grid, block, 0, stream>>>(o_a, a_fp32, lse_a, o_b, b_fp32, lse_b,
                                                          o_out, out_fp32, lse_out, rows, heads, D,
                                                          pairs);

@@ -1,0 +1,27 @@
+// Per-kernel timing of the library's own launches (host side).
+//
+// When tracing is on, every kernel launch is bracketed by two CUDA events
+// recorded on the stream it is launched on; ringattn_trace_collect() waits for
+// them and reports, per kernel, the number of launches and their summed
+// device time.  When tracing is off a launch pays one relaxed atomic load.
+#pragma once
+#include <cuda_runtime.h>
+
+namespace ra {
+
+bool trace_enabled();
+
+// Brackets one kernel launch: construct right before it, destroy right after.
+class TraceScope {
+ public:
+  TraceScope(cudaStream_t stream, const char* kernel);
+  ~TraceScope();
+  TraceScope(const TraceScope&) = delete;
+  TraceScope& operator=(const TraceScope&) = delete;
+
+ private:
+  cudaStream_t stream_;
+  int slot_ = -1;
+};
+
+}  // namespace ra

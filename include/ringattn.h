@@ -215,6 +215,26 @@ ra_status ringattn_plan_bwd(const int32_t* cu_seqlens, ra_dims dims, int num_sha
                             int32_t* segments, int max_segments, int* num_items,
                             int* num_segments);
 
+/*
+ * Per-kernel timing of this library's launches (profiling support; the pages
+ * ask for peak memory and timed steps when diagnosing a long-context run,
+ * archcrux interview page).  While tracing is on, every kernel launch is
+ * bracketed by two CUDA events recorded on the stream it is launched on.
+ * ringattn_trace_collect() waits for all recorded launches, fills one entry
+ * per kernel name (launch count and summed device milliseconds), clears the
+ * record and returns RA_OK; with too few entries it fills max_entries of
+ * them, still sets *num_entries to the number needed and returns
+ * RA_ERR_WORKSPACE.  Host-only bookkeeping: no device memory is allocated.
+ * At most 65536 launches are recorded between two collects.
+ */
+typedef struct {
+  char kernel[40];  /* kernel name, NUL-terminated */
+  int launches;
+  double total_ms;
+} ra_trace_entry;
+ra_status ringattn_trace_enable(int on);
+ra_status ringattn_trace_collect(ra_trace_entry* entries, int max_entries, int* num_entries);
+
 #ifdef __cplusplus
 }
 #endif

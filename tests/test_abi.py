@@ -83,3 +83,13 @@ def test_workspace_sizes(lib):
     d = dims(T=1024, hq=4, hkv=2)
     assert lib.ringattn_fwd_stepwise_workspace_size(d) >= 2 * (1024 * 4 * 128 * 4 + 4 * 1024 * 4)
     assert lib.ringattn_bwd_workspace_size(d) >= 4 * 1024 * 4   # the D_i vector
+
+
+def test_trace_without_launches(lib):
+    """Tracing is host bookkeeping: enabling it and collecting an empty record
+    needs no GPU."""
+    ra.trace_enable(True)
+    assert ra.trace_collect() == {}
+    ra.trace_enable(False)
+    n = ctypes.c_int(-1)
+    assert lib.ringattn_trace_collect(None, -1, ctypes.byref(n)) == -1
