@@ -390,20 +390,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ================================================================== dQ
+//
+// One CTA per 128-row query tile, key tiles of 128 in ring order.  Q and dO
+// stay in shared memory; K and V stream through separate rings (K: 3 slots,
+// since K(j) is read by S(j) and again by dQ(j); V: 2 slots).  Tensor memory:
+// S in two buffers (S(j) in buffer j % 2), dP in one, dQ in one:
+//   cols 0-127 S_0 | 128-255 S_1 | 256-383 dP | 384-511 dQ.
+// The MMA thread issues, per key tile j,
+//   dP(j+1) = dO V_{j+1}^T   once both warpgroups have read dP(j),
+//   dQ += dS(j) K_j          in two 64-key halves, as each warpgroup stores
+//                            its half of dS(j) (bf16, over its half of S(j)),
+//   S(j+2) = Q K_{j+2}^T     into the buffer dS(j) has just been read from,
+// so the elementwise work of tile j+1 is ready to start the moment tile j's
+// is done.  Warpgroup w (warps 4-7: w = 0, 8-11: w = 1) handles keys
+// [64 w, 64 w + 64) of every tile, one query row per thread.  Because dP(j+1)
+// is released before the MMA thread waits for dS(j), a warpgroup can finish
+// tile j+1 before that wait: dS(j) therefore signals on one of two barriers
+// per warpgroup (by j % 2), so no barrier runs two phases ahead of its waiter.
 
-constexpr int kQStages = 2;
+constexpr int kKSlots = 3;
+constexpr int kVSlots = 2;
 constexpr int kOffQ = 0;
 constexpr int kOffDO = kTileBytes;
-constexpr int kOffKVq = 2 * kTileBytes;  // per stage: K, V
-constexpr int kOffCtlQ = kOffKVq + kQStages * 2 * kTileBytes;
+constexpr int kOffKq = 2 * kTileBytes;
+constexpr int kOffVq = kOffKq + kKSlots * kTileBytes;
+constexpr int kOffCtlQ = kOffVq + kVSlots * kTileBytes;
 constexpr int kSmemQ = kOffCtlQ + 256 + 1024;
+static_assert(kSmemQ <= 232448, "dynamic shared memory of one CTA");
+
+constexpr uint32_t kIdescN128 = make_idesc_bf16(128, 128, false, false);
 
 struct CtlQ {
   uint64_t qd_full;
-  uint64_t kv_full[kQStages];
-  uint64_t kv_empty[kQStages];
-  uint64_t s_full[2];
-  uint64_t p_full[2];
+  uint64_t k_full[kKSlots];
+  uint64_t k_empty[kKSlots];
+  uint64_t v_full[kVSlots];
+  uint64_t v_empty[kVSlots];
+  uint64_t s_full[2];   // S(j) in buffer j % 2
+  uint64_t dp_full;     // dP(j)
+  uint64_t dp_free;     // every softmax thread has read dP(j)
+  uint64_t ds_full[2][2];  // [w][j % 2]: warpgroup w stored its half of dS(j)
   uint64_t acc_full;
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -411,24 +437,35 @@ struct CtlQ {
 };
 static_assert(sizeof(CtlQ) <= 256, "control block");
 
+// X[128 x 128] = A[128 x D] * B[128 x D]^T, both K-major, 128-row tiles.
+__device__ __forceinline__ void mma_rows_x_rows(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
+#pragma unroll
+  for (int kk = 0; kk < kD / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+    mma_bf16_ss(d_tmem, make_sdesc_sw128(a_smem + off, 16, 1024),
+                make_sdesc_sw128(b_smem + off, 16, 1024), kIdescN128, kk > 0);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                   const BwdParams p) {
   const PlanItem it = p.items[blockIdx.x >> 1];
-  const int tile = blockIdx.x & 1;
-  if (it.qlen[tile] == 0) return;  // whole CTA: this item has one query tile
+  const bool second = (blockIdx.x & 1) != 0;  // which of the item's two query tiles
+  const int qlen = second ? it.qlen[1] : it.qlen[0];
+  if (qlen == 0) return;  // whole CTA: this item has one query tile
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   CtlQ* ctl = reinterpret_cast<CtlQ*>(smem + kOffCtlQ);
   volatile int* abort = &ctl->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int head = it.head[tile];
+  const int head = second ? it.head[1] : it.head[0];
   const int g = head / p.group;
-  const int q0 = it.q0[tile];
+  const int q0 = second ? it.q0[1] : it.q0[0];
 
-  int n = 0;
+  int n = 0;  // key tiles
   for (int si = 0; si < it.seg_count; ++si) {
     const PlanSegment sg = p.segs[it.seg_begin + si];
     n += (sg.k1 - sg.k0 + kTile - 1) / kTile;
@@ -436,14 +473,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&ctl->qd_full, 1);
-    for (int s = 0; s < kQStages; ++s) {
-      mbar_init(&ctl->kv_full[s], 1);
-      mbar_init(&ctl->kv_empty[s], 1);
+    for (int s = 0; s < kKSlots; ++s) {
+      mbar_init(&ctl->k_full[s], 1);
+      mbar_init(&ctl->k_empty[s], 1);
+    }
+    for (int s = 0; s < kVSlots; ++s) {
+      mbar_init(&ctl->v_full[s], 1);
+      mbar_init(&ctl->v_empty[s], 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&ctl->s_full[x], 1);
-      mbar_init(&ctl->p_full[x], 128);
+      mbar_init(&ctl->ds_full[x][0], 128);
+      mbar_init(&ctl->ds_full[x][1], 128);
     }
+    mbar_init(&ctl->dp_full, 1);
+    mbar_init(&ctl->dp_free, 256);
     mbar_init(&ctl->acc_full, 1);
     mbar_init(&ctl->mma_done, 1);
     ctl->abort = 0;
@@ -459,84 +503,119 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ctl->tmem_base;
 
   if (warp == 0) {
+    // ---------------------------------------------------- TMA producer
     if (elect_one_sync() && n > 0) {
       tma_prefetch_map(&map_k);
       tma_prefetch_map(&map_v);
       mbar_arrive_expect_tx(&ctl->qd_full, 2 * kTileBytes);
       load_tile(smem + kOffQ, &map_q, &ctl->qd_full, head, q0);
       load_tile(smem + kOffDO, &map_do, &ctl->qd_full, head, q0);
-      int li = 0;
+      int j = 0, nk = 0, nv = 0;  // tiles visited, K and V loads issued
       bool ok = true;
       for (int si = 0; si < it.seg_count && ok; ++si) {
         const PlanSegment sg = p.segs[it.seg_begin + si];
-        for (int kt = sg.k0; kt < sg.k1; kt += kTile, ++li) {
-          const int slot = li % kQStages;
-          if (li >= kQStages &&
-              !mbar_wait(&ctl->kv_empty[slot], ((li / kQStages) - 1) & 1, p.status, abort)) {
+        for (int kt = sg.k0; kt < sg.k1; kt += kTile, ++j) {
+          const int ks = j % kKSlots, vs = j % kVSlots;
+          if (j >= kKSlots &&
+              !mbar_wait(&ctl->k_empty[ks], ((j / kKSlots) - 1) & 1, p.status, abort)) {
             ok = false;
             break;
           }
-          uint8_t* st = smem + kOffKVq + slot * 2 * kTileBytes;
-          mbar_arrive_expect_tx(&ctl->kv_full[slot], 2 * kTileBytes);
-          load_tile(st, &map_k, &ctl->kv_full[slot], g, kt);
-          load_tile(st + kTileBytes, &map_v, &ctl->kv_full[slot], g, kt);
+          mbar_arrive_expect_tx(&ctl->k_full[ks], kTileBytes);
+          load_tile(smem + kOffKq + ks * kTileBytes, &map_k, &ctl->k_full[ks], g, kt);
+          ++nk;
+          if (j >= kVSlots &&
+              !mbar_wait(&ctl->v_empty[vs], ((j / kVSlots) - 1) & 1, p.status, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&ctl->v_full[vs], kTileBytes);
+          load_tile(smem + kOffVq + vs * kTileBytes, &map_v, &ctl->v_full[vs], g, kt);
+          ++nv;
         }
       }
       if (!ok) *abort = 1;
-      for (int s = 0; s < kQStages && s < li; ++s) {
-        const int last = s + ((li - 1 - s) / kQStages) * kQStages;
-        mbar_wait(&ctl->kv_full[s], (last / kQStages) & 1, p.status, nullptr);
+      // let every copy this thread started land before the CTA can exit
+      for (int s = 0; s < kKSlots && s < nk; ++s) {
+        const int last = s + ((nk - 1 - s) / kKSlots) * kKSlots;
+        mbar_wait(&ctl->k_full[s], (last / kKSlots) & 1, p.status, nullptr);
+      }
+      for (int s = 0; s < kVSlots && s < nv; ++s) {
+        const int last = s + ((nv - 1 - s) / kVSlots) * kVSlots;
+        mbar_wait(&ctl->v_full[s], (last / kVSlots) & 1, p.status, nullptr);
       }
       mbar_wait(&ctl->qd_full, 0, p.status, nullptr);
     }
   } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA
     if (elect_one_sync() && n > 0) {
       const uint32_t sQ = smem_u32(smem + kOffQ), sdO = smem_u32(smem + kOffDO);
-      auto sK = [&](int li) { return smem_u32(smem + kOffKVq + (li % kQStages) * 2 * kTileBytes); };
-      const uint32_t tS[2] = {tmem + 0, tmem + 128};
-      const uint32_t tdP[2] = {tmem + 64, tmem + 192};
-      const uint32_t tdQ = tmem + 256;
-      auto kv_ready = [&](int li) {
-        return mbar_wait(&ctl->kv_full[li % kQStages], (li / kQStages) & 1, p.status, abort);
+      auto sK = [&](int j) { return smem_u32(smem + kOffKq + (j % kKSlots) * kTileBytes); };
+      auto sV = [&](int j) { return smem_u32(smem + kOffVq + (j % kVSlots) * kTileBytes); };
+      auto tS = [&](int j) { return tmem + static_cast<uint32_t>(j & 1) * 128u; };
+      const uint32_t tdP = tmem + 256, tdQ = tmem + 384;
+      auto k_ready = [&](int j) {
+        return mbar_wait(&ctl->k_full[j % kKSlots], (j / kKSlots) & 1, p.status, abort);
       };
-      auto issue_s = [&](int li, int x) {
-        mma_rows_x_half(tS[x], sQ, sK(li) + x * kRowsHalf);
-        mma_rows_x_half(tdP[x], sdO, sK(li) + kTileBytes + x * kRowsHalf);
-        mma_commit(&ctl->s_full[x]);
+      auto v_ready = [&](int j) {
+        return mbar_wait(&ctl->v_full[j % kVSlots], (j / kVSlots) & 1, p.status, abort);
       };
-      bool ok = mbar_wait(&ctl->qd_full, 0, p.status, abort) && kv_ready(0);
+      auto issue_s = [&](int j) {  // S(j) into buffer j % 2
+        mma_rows_x_rows(tS(j), sQ, sK(j));
+        mma_commit(&ctl->s_full[j & 1]);
+      };
+      auto issue_dp = [&](int j) {  // dP(j); V(j) is then no longer needed
+        mma_rows_x_rows(tdP, sdO, sV(j));
+        mma_commit(&ctl->dp_full);
+        mma_commit(&ctl->v_empty[j % kVSlots]);
+      };
+      bool ok = mbar_wait(&ctl->qd_full, 0, p.status, abort) && k_ready(0);
       if (ok) {
         tc_fence_after_sync();
-        issue_s(0, 0);
-        issue_s(0, 1);
+        issue_s(0);
+        ok = v_ready(0);
+      }
+      if (ok) {
+        tc_fence_after_sync();
+        issue_dp(0);
+        if (n > 1 && (ok = k_ready(1))) {
+          tc_fence_after_sync();
+          issue_s(1);
+        }
       }
       for (int j = 0; j < n && ok; ++j) {
-        const bool more = j + 1 < n;
-        if (!(ok = mbar_wait(&ctl->p_full[0], j & 1, p.status, abort))) break;
-        tc_fence_after_sync();
-        mma_tmem_x_rows(tdQ, tS[0], sK(j), j > 0);
-        if (more) {
-          if (!(ok = kv_ready(j + 1))) break;
+        if (j + 1 < n) {
+          if (!(ok = mbar_wait(&ctl->dp_free, j & 1, p.status, abort) && v_ready(j + 1))) break;
           tc_fence_after_sync();
-          issue_s(j + 1, 0);
+          issue_dp(j + 1);
         }
-        if (!(ok = mbar_wait(&ctl->p_full[1], j & 1, p.status, abort))) break;
-        tc_fence_after_sync();
-        mma_tmem_x_rows(tdQ, tS[1], sK(j) + kRowsHalf, true);
-        mma_commit(&ctl->kv_empty[j % kQStages]);
-        if (more) issue_s(j + 1, 1);
+        for (int w = 0; w < 2; ++w) {
+          if (!(ok = mbar_wait(&ctl->ds_full[w][j & 1], (j >> 1) & 1, p.status, abort))) break;
+          tc_fence_after_sync();
+          // dQ += dS(j)[:, 64 w : 64 w + 64] K_j[64 w : 64 w + 64, :]
+          mma_tmem_x_rows(tdQ, tS(j) + 64 * w, sK(j) + w * kRowsHalf, j > 0 || w > 0);
+        }
+        if (!ok) break;
+        mma_commit(&ctl->k_empty[j % kKSlots]);
+        if (j + 2 < n) {
+          if (!(ok = k_ready(j + 2))) break;
+          tc_fence_after_sync();
+          issue_s(j + 2);
+        }
       }
       if (ok) mma_commit(&ctl->acc_full);
       if (!ok) *abort = 1;
+      // every MMA this thread issued has completed before TMEM is released
       mma_commit(&ctl->mma_done);
       mbar_wait(&ctl->mma_done, 0, p.status, nullptr);
     }
   } else if (warp >= 4) {
-    const int x = (warp - 4) >> 2;  // key half of each tile
+    // -------------------------------------------- elementwise, key half w
+    const int w = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int row = q0 + r;
-    const bool valid = r < it.qlen[tile];
+    const bool valid = r < qlen;
     int lo = 0, hi = 0;
     float lse2 = 0.f, Dv = 0.f;
     if (valid) {
@@ -548,27 +627,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       Dv = p.Dvec[(size_t)head * p.T + row];
     }
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_off + x * 128;
-    const uint32_t tdP = tS + 64;
-    const int mlo = it.mask_lo[tile], mhi = it.mask_hi[tile];
+    const uint32_t tdP = tmem + lane_off + 256 + 64 * w;
+    const int mlo = second ? it.mask_lo[1] : it.mask_lo[0];
+    const int mhi = second ? it.mask_hi[1] : it.mask_hi[0];
     const float sl2 = p.scale_log2;
     bool ok = true;
-    int jj = 0;
+    int j = 0;
     for (int si = 0; si < it.seg_count && ok; ++si) {
       const PlanSegment sg = p.segs[it.seg_begin + si];
       const int a = max(lo, sg.k0), b = min(hi, sg.k1);
       const int full_lo = max(sg.k0, mlo), full_hi = min(sg.k1, mhi);
-      for (int kt = sg.k0; kt < sg.k1; kt += kTile, ++jj) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_full[x], jj & 1, p.status, abort));
+      for (int kt = sg.k0; kt < sg.k1; kt += kTile, ++j) {
+        // .sync.aligned TMEM accesses follow: keep the warp's decision uniform
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_full[j & 1], (j >> 1) & 1, p.status, abort));
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->dp_full, j & 1, p.status, abort));
         if (!ok) break;
         tc_fence_after_sync();
-        const int kb = kt + x * 64;  // first key of this half
+        uint32_t ud0[32], ud1[32];
+        tmem_load_32(tdP, ud0);
+        tmem_load_32(tdP + 32, ud1);
+        tc_fence_before_sync();
+        mbar_arrive(&ctl->dp_free);  // dP(j+1) may now overwrite dP(j)
+        const uint32_t tS = tmem + lane_off + (j & 1) * 128 + 64 * w;
+        const int kb = kt + 64 * w;  // first key of this half
         const bool full = kb >= full_lo && kb + 64 <= full_hi;
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t us[32], ud[32];
+          uint32_t us[32];
           tmem_load_32(tS + c2 * 32, us);
-          tmem_load_32(tdP + c2 * 32, ud);
           uint32_t pd[16];
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
@@ -578,27 +664,28 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int key = kb + c2 * 32 + c + e;
               const bool vis = full || (key >= a && key < b);
               const float pe = vis ? fast_exp2(fmaf(__uint_as_float(us[c + e]), sl2, -lse2)) : 0.f;
-              dv[e] = pe * (__uint_as_float(ud[c + e]) - Dv);
+              dv[e] = pe * (__uint_as_float(c2 == 0 ? ud0[c + e] : ud1[c + e]) - Dv);
             }
             pd[c / 2] = pack_bf16x2(dv[0], dv[1]);
           }
+          // dS over the first half of the columns this warpgroup just read
           tmem_store_16(tS + c2 * 16, pd);
         }
         tmem_store_wait();
         tc_fence_before_sync();
-        mbar_arrive(&ctl->p_full[x]);
+        mbar_arrive(&ctl->ds_full[w][j & 1]);
       }
     }
     if (!ok) *abort = 1;
     if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->acc_full, 0, p.status, abort));
     tc_fence_after_sync();
-    // epilogue: half x writes columns [64 x, 64 x + 64) of its row of dQ
-    const size_t off = ((size_t)row * p.hq + head) * kD + x * 64;
+    // epilogue: warpgroup w writes columns [64 w, 64 w + 64) of its row of dQ
+    const size_t off = ((size_t)row * p.hq + head) * kD + w * 64;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       uint32_t u[32];
       if (ok && n > 0) {
-        tmem_load_32(tmem + lane_off + 256 + x * 64 + c * 32, u);
+        tmem_load_32(tmem + lane_off + 384 + w * 64 + c * 32, u);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) u[i] = 0u;

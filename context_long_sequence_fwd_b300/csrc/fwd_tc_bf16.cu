@@ -145,10 +145,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&map_k);
       tma_prefetch_map(&map_v);
       mbar_arrive_expect_tx(&ctl->q_full, (has_b ? 2 : 1) * kTileBytes);
-      for (int x = 0; x < (has_b ? 2 : 1); ++x)
-        for (int hf = 0; hf < 2; ++hf)
-          tma_load_3d(smem + kOffQ + x * kTileBytes + hf * kHalfBytes, &map_q, &ctl->q_full,
-                      hf * 64, it.head[x], it.q0[x]);
+      for (int hf = 0; hf < 2; ++hf) {
+        tma_load_3d(smem + kOffQ + hf * kHalfBytes, &map_q, &ctl->q_full, hf * 64, it.head[0],
+                    it.q0[0]);
+        if (has_b)
+          tma_load_3d(smem + kOffQ + kTileBytes + hf * kHalfBytes, &map_q, &ctl->q_full, hf * 64,
+                      it.head[1], it.q0[1]);
+      }
       int li = 0;
       bool ok = true;
       for (int si = 0; si < it.seg_count && ok; ++si) {
@@ -240,15 +243,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     if (x == 0 || has_b) {
-      const int row = it.q0[x] + r;
-      const bool valid = r < it.qlen[x];
-      const int head = it.head[x];
+      // x is uniform per warp: select fields instead of indexing the item
+      const int row = (x ? it.q0[1] : it.q0[0]) + r;
+      const bool valid = r < (x ? it.qlen[1] : it.qlen[0]);
+      const int head = x ? it.head[1] : it.head[0];
       int lo = 0, hi = 0;
       if (valid) row_key_interval(p, row, &lo, &hi);
       const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
       const uint32_t tS = tmem + lane_off + x * 128;
       const uint32_t tO = tmem + lane_off + 256 + x * 128;
-      const int mlo = it.mask_lo[x], mhi = it.mask_hi[x];
+      const int mlo = x ? it.mask_lo[1] : it.mask_lo[0];
+      const int mhi = x ? it.mask_hi[1] : it.mask_hi[0];
       const float sl2 = p.scale_log2;
       float m2 = -INFINITY;  // running max, log2 units
       float l = 0.f;
