@@ -107,14 +107,55 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t
                       pack_bf16x2(__uint_as_float(u[8 * i + 6]) * mul, __uint_as_float(u[8 * i + 7]) * mul));
 }
 
-// ============================================================== dK / dV
-
-constexpr int kKvStages = 2;
+// Elementwise core of the backward for 32 score columns of one TMEM row:
+//   P = 2^(S scale log2(e) - lse log2(e)),  dS = P (dP - D),
+// with the columns the mask hides forced to P = 0 by an exponent of -inf
+// (2^-inf = +0): a select, never a branch around the exponential.  kMasked
+// is false for tiles every column of which is visible.  The per-column
+// statistics come from `col` (dK/dV: one query per column), or are the
+// thread's own (dQ: one query per row, col == nullptr).
 struct RowInfo {
   float lse2;  // lse_i * log2(e)
   float Dv;    // D_i
   int lo, hi;  // keys row i may see: [lo, hi); empty for rows outside the segment
 };
+
+template <bool kMasked, bool kWantP>
+__device__ __forceinline__ void bwd_elementwise32(const uint32_t (&us)[32], const uint32_t (&ud)[32],
+                                                  const RowInfo* col, float lse2, float Dv,
+                                                  int key, int key0, int a, int b, float sl2,
+                                                  uint32_t (&pp)[16], uint32_t (&pd)[16]) {
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    float pv[2], dv[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float l2 = lse2, d = Dv;
+      if (col != nullptr) {
+        l2 = col[c + e].lse2;
+        d = col[c + e].Dv;
+      }
+      float x = fmaf(__uint_as_float(us[c + e]), sl2, -l2);
+      if (kMasked) {
+        bool vis;
+        if (col != nullptr)  // fixed key row, one query per column
+          vis = key >= col[c + e].lo && key < col[c + e].hi;
+        else                 // fixed query row, one key per column
+          vis = key0 + c + e >= a && key0 + c + e < b;
+        x = vis ? x : -INFINITY;
+      }
+      const float pe = fast_exp2(x);
+      pv[e] = pe;
+      dv[e] = pe * (__uint_as_float(ud[c + e]) - d);
+    }
+    if (kWantP) pp[c / 2] = pack_bf16x2(pv[0], pv[1]);
+    pd[c / 2] = pack_bf16x2(dv[0], dv[1]);
+  }
+}
+
+// ============================================================== dK / dV
+
+constexpr int kKvStages = 2;
 constexpr int kOffK = 0;
 constexpr int kOffV = kTileBytes;
 constexpr int kOffStage = 2 * kTileBytes;                      // per stage: Q, dO
@@ -334,20 +375,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_load_32(tS + c2 * 32, us);
         tmem_load_32(tdP + c2 * 32, ud);
         uint32_t pp[16], pd[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const RowInfo ri = hinfo[c2 * 32 + c + e];
-            const bool vis = full || (j >= ri.lo && j < ri.hi);
-            const float pe = vis ? fast_exp2(fmaf(__uint_as_float(us[c + e]), sl2, -ri.lse2)) : 0.f;
-            pv[e] = pe;
-            dv[e] = pe * (__uint_as_float(ud[c + e]) - ri.Dv);
-          }
-          pp[c / 2] = pack_bf16x2(pv[0], pv[1]);
-          pd[c / 2] = pack_bf16x2(dv[0], dv[1]);
-        }
+        if (full)
+          bwd_elementwise32<false, true>(us, ud, hinfo + c2 * 32, 0.f, 0.f, j, 0, 0, 0, sl2, pp, pd);
+        else
+          bwd_elementwise32<true, true>(us, ud, hinfo + c2 * 32, 0.f, 0.f, j, 0, 0, 0, sl2, pp, pd);
         tmem_store_16(tS + c2 * 16, pp);
         tmem_store_16(tdP + c2 * 16, pd);
       }
@@ -655,19 +686,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c2 = 0; c2 < 2; ++c2) {
           uint32_t us[32];
           tmem_load_32(tS + c2 * 32, us);
-          uint32_t pd[16];
-#pragma unroll
-          for (int c = 0; c < 32; c += 2) {
-            float dv[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int key = kb + c2 * 32 + c + e;
-              const bool vis = full || (key >= a && key < b);
-              const float pe = vis ? fast_exp2(fmaf(__uint_as_float(us[c + e]), sl2, -lse2)) : 0.f;
-              dv[e] = pe * (__uint_as_float(c2 == 0 ? ud0[c + e] : ud1[c + e]) - Dv);
-            }
-            pd[c / 2] = pack_bf16x2(dv[0], dv[1]);
-          }
+          uint32_t pp[16], pd[16];  // pp unused: dQ needs dS only
+          if (full)
+            bwd_elementwise32<false, false>(us, c2 == 0 ? ud0 : ud1, nullptr, lse2, Dv, 0,
+                                            kb + c2 * 32, a, b, sl2, pp, pd);
+          else
+            bwd_elementwise32<true, false>(us, c2 == 0 ? ud0 : ud1, nullptr, lse2, Dv, 0,
+                                           kb + c2 * 32, a, b, sl2, pp, pd);
           // dS over the first half of the columns this warpgroup just read
           tmem_store_16(tS + c2 * 16, pd);
         }
