@@ -30,8 +30,8 @@
 //     TMEM: S_a 0-63, dP_a 64-127, S_b 128-191, dP_b 192-255, dQ 256-383.
 //
 // Roles in both kernels (384 threads): warp 0 TMA producer, warp 1 TMEM
-// allocation and the single MMA-issuing thread, warp 2 (dK/dV only) loads the
-// per-query-row values (lse, D, visible key range) of each stage, warps 4-7
+// allocation and the single MMA-issuing thread, warps 2-3 (dK/dV only) load
+// the per-query-row values (lse, D, visible key range) of each stage, warps 4-7
 // and 8-11 the two softmax warpgroups.  Every barrier wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -204,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&ctl->kv_full, 1);
     for (int s = 0; s < kKvStages; ++s) {
       mbar_init(&ctl->q_full[s], 1);
-      mbar_init(&ctl->info_full[s], 32);
+      mbar_init(&ctl->info_full[s], 64);
       mbar_init(&ctl->stage_empty[s], 1);
     }
     for (int x = 0; x < 2; ++x) {
@@ -259,13 +259,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mbar_wait(&ctl->kv_full, 0, p.status, nullptr);
     }
-  } else if (warp == 2) {
-    // -------------------------------------- per-row values of each stage
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------ per-row values of each stage
+    // warp 2 fills rows 0-63, warp 3 rows 64-127; each lane's two rows are
+    // loaded together so their global-memory latencies overlap
+    const int rbase = (warp - 2) * 64;
     int li = 0;
     bool ok = true;
     for (int si = 0; si < it.seg_count && ok; ++si) {
       const BwdSegment sg = p.bsegs[it.seg_begin + si];
       for (int i0 = sg.q0; i0 < sg.q1 && ok; i0 += kTile) {
+        // the document of the stage's first row; rows past its end search again
+        int ds0, de0;
+        doc_bounds(p.cu, p.num_docs, i0, &ds0, &de0);
         for (int h = g * G; h < (g + 1) * G; ++h, ++li) {
           const int slot = li % kKvStages;
           if (li >= kKvStages) {
@@ -274,15 +280,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
           }
           RowInfo* info = reinterpret_cast<RowInfo*>(smem + kOffInfo + slot * ((kInfoBytes + 127) / 128 * 128));
+          float lv[2], dv[2];
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int i = i0 + rbase + lane + 32 * k;
+            const bool valid = i < sg.q1;
+            lv[k] = valid ? p.lse[(size_t)h * p.T + i] : 0.f;
+            dv[k] = valid ? p.Dvec[(size_t)h * p.T + i] : 0.f;
+          }
           bool full = true;
-          for (int r = lane; r < kTile; r += 32) {
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int r = rbase + lane + 32 * k;
             const int i = i0 + r;
             RowInfo ri{0.f, 0.f, 0, 0};
             if (i < sg.q1) {
-              int ds, de;
-              doc_bounds(p.cu, p.num_docs, i, &ds, &de);
-              ri.lse2 = p.lse[(size_t)h * p.T + i] * kLog2e;
-              ri.Dv = p.Dvec[(size_t)h * p.T + i];
+              int ds = ds0, de = de0;
+              if (i >= de0) doc_bounds(p.cu, p.num_docs, i, &ds, &de);
+              ri.lse2 = lv[k] * kLog2e;
+              ri.Dv = dv[k];
               ri.lo = ds;
               ri.hi = p.causal ? i + 1 : de;
             }
@@ -292,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             info[r] = ri;
           }
           full = __all_sync(0xffffffffu, full);
-          if (lane == 0) reinterpret_cast<int*>(info + kTile)[0] = full ? 1 : 0;
+          if (lane == 0) reinterpret_cast<int*>(info + kTile)[warp - 2] = full ? 1 : 0;
           __syncwarp();
           mbar_arrive(&ctl->info_full[slot]);
         }
@@ -367,7 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after_sync();
       const RowInfo* info = reinterpret_cast<const RowInfo*>(smem + kOffInfo + slot * ((kInfoBytes + 127) / 128 * 128));
-      const bool full = reinterpret_cast<const int*>(info + kTile)[0] != 0;
+      const int* flags = reinterpret_cast<const int*>(info + kTile);
+      const bool full = flags[0] != 0 && flags[1] != 0;
       const RowInfo* hinfo = info + x * 64;
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
