@@ -44,6 +44,7 @@ struct CachedPlan {
   PlanItem* items = nullptr;
   PlanSegment* segs = nullptr;
   int32_t* cu = nullptr;
+  int num_ctas = 0;  // grid of the persistent forward: min(items, SMs)
   cudaEvent_t last_use = nullptr;
   // key-side backward schedule, built on the first backward call
   BwdPlan bwd;
@@ -174,6 +175,11 @@ ra_status get_plan(int dev, const PlanInput& in, cudaStream_t stream, CachedPlan
   cp.dev = dev;
   cp.key = in;
   cp.plan = build_fwd_plan(in);
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return RA_ERR_CUDA;
+  const int n_items = static_cast<int>(cp.plan.items.size());
+  cp.num_ctas = n_items < sms ? n_items : sms;
   const size_t nb_items = cp.plan.items.size() * sizeof(PlanItem);
   const size_t nb_segs = cp.plan.segs.size() * sizeof(PlanSegment);
   const size_t nb_cu = cp.plan.cu.size() * sizeof(int32_t);
@@ -244,6 +250,8 @@ FwdParams make_params(const void* q, const void* k, const void* v, void* out, fl
   p.causal = causal ? 1 : 0;
   p.scale = 1.0f / std::sqrt(static_cast<float>(d.head_dim));
   p.scale_log2 = p.scale * 1.4426950408889634f;
+  p.work_counter = nullptr;  // set by launch_fwd for the persistent launch
+  p.num_ctas = cp.num_ctas;
   p.step_filter = -1;
   p.out_fp32 = d.dtype == RA_FP32 ? 1 : 0;
   p.status = status;
@@ -253,6 +261,53 @@ FwdParams make_params(const void* q, const void* k, const void* v, void* out, fl
 struct Maps {
   CUtensorMap q, k, v;
 };
+
+// Work counters of the persistent forward.  Each launch takes a slot whose
+// previous launch has finished (its event has completed), zeroes it on the
+// launch stream and records the slot's event after the launch, so launches
+// in flight on different streams never share a counter.  Caller holds g_mu.
+constexpr int kCounterSlots = 64;
+__device__ int g_work_counters[kCounterSlots];
+struct CounterPool {
+  int* base = nullptr;
+  cudaEvent_t ev[kCounterSlots] = {};
+  int next = 0;
+};
+CounterPool g_counters[kMaxDevices];
+
+ra_status claim_counter(int dev, cudaStream_t s, int** counter, cudaEvent_t* ev) {
+  CounterPool& pool = g_counters[dev];
+  if (!pool.base) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_work_counters) != cudaSuccess) return RA_ERR_CUDA;
+    pool.base = static_cast<int*>(a);
+  }
+  int slot = -1;
+  for (int t = 0; t < kCounterSlots && slot < 0; ++t) {
+    const int c = (pool.next + t) % kCounterSlots;
+    if (!pool.ev[c]) {
+      if (cudaEventCreateWithFlags(&pool.ev[c], cudaEventDisableTiming) != cudaSuccess)
+        return RA_ERR_CUDA;
+      slot = c;
+    } else {
+      const cudaError_t q = cudaEventQuery(pool.ev[c]);
+      if (q == cudaSuccess) slot = c;
+      else if (q != cudaErrorNotReady) return RA_ERR_CUDA;
+    }
+  }
+  // a busy slot is not an error: clear it from the last-error state
+  const cudaError_t last = cudaGetLastError();
+  if (last != cudaSuccess && last != cudaErrorNotReady) return RA_ERR_CUDA;
+  if (slot < 0) {  // every slot busy: wait for the oldest
+    slot = pool.next;
+    if (cudaEventSynchronize(pool.ev[slot]) != cudaSuccess) return RA_ERR_CUDA;
+  }
+  pool.next = (slot + 1) % kCounterSlots;
+  if (cudaMemsetAsync(pool.base + slot, 0, sizeof(int), s) != cudaSuccess) return RA_ERR_CUDA;
+  *counter = pool.base + slot;
+  *ev = pool.ev[slot];
+  return RA_OK;
+}
 
 ra_status launch_fwd(const FwdParams& p, const ra_dims& d, const Maps* maps, cudaStream_t stream) {
   cudaError_t e;
@@ -301,9 +356,14 @@ ra_status ringattn_fwd(const void* q, const void* k, const void* v, const int32_
   if ((st = prepare_maps(q, k, v, dims, &maps)) != RA_OK) return st;
   CachedPlan* cp;
   if ((st = get_plan(dev, in, static_cast<cudaStream_t>(stream), &cp)) != RA_OK) return st;
-  const FwdParams p = make_params(q, k, v, out, lse, dims, causal, *cp, ds->status);
+  FwdParams p = make_params(q, k, v, out, lse, dims, causal, *cp, ds->status);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaEvent_t counter_ev = nullptr;
+  if (dims.dtype == RA_BF16 && p.num_items > 0 &&
+      (st = claim_counter(dev, s, &p.work_counter, &counter_ev)) != RA_OK)
+    return st;
   if ((st = launch_fwd(p, dims, &maps, s)) != RA_OK) return st;
+  if (counter_ev && cudaEventRecord(counter_ev, s) != cudaSuccess) return RA_ERR_CUDA;
   if (cudaEventRecord(cp->last_use, s) != cudaSuccess) return RA_ERR_CUDA;
   return RA_OK;
 }
@@ -348,6 +408,7 @@ ra_status ringattn_fwd_stepwise(const void* q, const void* k, const void* v,
     float* l_dst = step == 0 ? (last ? lse : acc_l) : stp_l;
     FwdParams p = make_params(q, k, v, o_dst, l_dst, dims, causal, *cp, ds->status);
     p.step_filter = step;
+
     p.out_fp32 = (step == 0 && last) ? (out_fp32 ? 1 : 0) : 1;
     if ((st = launch_fwd(p, dims, &maps, s)) != RA_OK) return st;
     if (step > 0) {
@@ -453,6 +514,7 @@ extern "C" ra_status ringattn_fwd_stepwise_noalloc(const void* q, const void* k,
     float* l_dst = step == 0 ? (last ? lse : acc_l) : stp_l;
     FwdParams p = make_params(q, k, v, o_dst, l_dst, dims, causal, cp, ds->status);
     p.step_filter = step;
+
     p.out_fp32 = (step == 0 && last) ? (out_fp32 ? 1 : 0) : 1;
     if ((st = launch_fwd(p, dims, &maps, s)) != RA_OK) return st;
     if (step > 0) {

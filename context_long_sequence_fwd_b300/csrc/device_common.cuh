@@ -23,6 +23,9 @@ struct FwdParams {
   int causal;
   float scale;            // 1 / sqrt(D)
   float scale_log2;       // scale * log2(e)
+  int* work_counter;       // persistent launch: next unclaimed item, zeroed before the launch
+                          // (nullptr: CTA i runs item i)
+  int num_ctas;           // grid of the persistent launch
   int step_filter;        // -1: every ring step; s >= 0: only segments of step s
   int out_fp32;           // 1: out is fp32, 0: out is bf16
   int* status;            // device status word (first error wins)

@@ -1,16 +1,20 @@
 // bf16 ring-attention forward on the sm_103a tensor cores (tcgen05 + TMEM).
 //
-// One CTA takes one planner item: two 128-row query tiles (A and B) that read
-// the same key/value head, and the item's key ranges in ring order (ring
+// Persistent: one CTA per SM claims the planner's items, longest first, from
+// a work counter as it becomes free (one item per CTA in stepwise mode).  An
+// item is two 128-row query tiles (A and B) that read the same key/value head,
+// and the item's key ranges in ring order (ring
 // step s visits the K/V shard of rank (r - s) mod P; axolotl "Sequence
 // Parallelism" page, introduction; aicassindra "tm_sp_math", "Context
 // parallelism is the axis that is independent").  No T x T score matrix is
 // formed: each 128 x 128 block of scores lives in tensor memory only while
 // its softmax runs (FlashAttention-style tiling, archcrux interview page).
 //
-// Roles (384 threads):
-//   warp 0      TMA producer: Q_A, Q_B once, then K_j, V_j into a ring of
-//               five 32 KB shared-memory slots (128 B swizzle).
+// Roles (384 threads), each looping over the CTA's items:
+//   warp 0      TMA producer: Q_A, Q_B once per item (as soon as the previous
+//               item's last S MMAs have read the Q buffer), then K_j, V_j into
+//               a ring of five 32 KB shared-memory slots (128 B swizzle) that
+//               runs on across items.
 //   warp 1      allocates TMEM; one thread issues every tcgen05.mma:
 //                 S_X = Q_X K_j^T      (SS, both operands K-major)
 //                 O_X += P_X V_j       (TS: P from TMEM, V MN-major)
@@ -21,7 +25,10 @@
 // TMEM columns: S_A 0-127, S_B 128-255, O_A 256-383, O_B 384-511.  P (bf16,
 // two per column) overwrites the first 64 columns of its S block; tcgen05
 // MMAs of one thread execute in issue order, so S_X(j+1) cannot overwrite
-// P_X(j) before PV_X(j) has read it.
+// P_X(j) before PV_X(j) has read it.  At an item boundary the next item's
+// S_X(0) follows the current item's last PV_X at once, while the softmax warps
+// run the epilogue; the next item's first P_X, and with it the PV_X that
+// overwrites O_X, comes only after the epilogue has read O_X.
 //
 // Online softmax, in the log2 domain (scores pre-multiplied by
 // scale * log2 e): the running maximum is only raised when a tile's maximum
@@ -55,18 +62,23 @@ constexpr int kOffKV = 2 * kTileBytes;       // K/V ring
 constexpr int kOffCtl = kOffKV + kStages * kTileBytes;
 constexpr int kSmemBytes = kOffCtl + 256 + 1024;  // control block + alignment slack
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
+constexpr int kSchedSlots = 4;               // item indices in flight inside a CTA
 
 constexpr uint32_t kIdescQK = make_idesc_bf16(128, 128, false, false);
 constexpr uint32_t kIdescPV = make_idesc_bf16(128, 128, false, true);
 
 struct Ctl {
   uint64_t q_full;
+  uint64_t q_empty;  // the item's last S MMAs have read Q
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_full[2];
   uint64_t mma_done;
+  uint64_t sched_full[kSchedSlots];   // item index published by the producer
+  uint64_t sched_empty[kSchedSlots];  // read by the MMA thread and the 8 softmax warps
+  int sched[kSchedSlots];             // item index, -1 = no more items
   uint32_t tmem_base;
   int abort;
 };
@@ -90,6 +102,16 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
   }
 }
 
+// Number of K/V tiles an item visits (the same count in every role).
+__device__ __forceinline__ int item_tiles(const PlanItem& it, const FwdParams& p) {
+  int n = 0;
+  for (int si = 0; si < it.seg_count; ++si) {
+    const PlanSegment sg = p.segs[it.seg_begin + si];
+    if (seg_selected(sg, p.step_filter)) n += (sg.k1 - sg.k0 + kBN - 1) / kBN;
+  }
+  return n;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_bf16_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
@@ -101,21 +123,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = smem_u32(smem + kOffQ);
   const uint32_t sKV = smem_u32(smem + kOffKV);
   volatile int* abort = &ctl->abort;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const PlanItem it = p.items[blockIdx.x];
-  const bool has_b = it.qlen[1] > 0;
-  const int g = it.head[0] / p.group;
-
-  // K/V tiles this item visits (same count in every role)
-  int n = 0;
-  for (int si = 0; si < it.seg_count; ++si) {
-    const PlanSegment sg = p.segs[it.seg_begin + si];
-    if (seg_selected(sg, p.step_filter)) n += (sg.k1 - sg.k0 + kBN - 1) / kBN;
-  }
 
   if (threadIdx.x == 0) {
     mbar_init(&ctl->q_full, 1);
+    mbar_init(&ctl->q_empty, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&ctl->kv_full[s], 1);
       mbar_init(&ctl->kv_empty[s], 1);
@@ -126,6 +138,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->o_full[x], 1);
     }
     mbar_init(&ctl->mma_done, 1);
+    for (int s = 0; s < kSchedSlots; ++s) {
+      mbar_init(&ctl->sched_full[s], 1);
+      mbar_init(&ctl->sched_empty[s], 9);
+    }
     ctl->abort = 0;
     fence_barrier_init();
   }
@@ -138,38 +154,86 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = ctl->tmem_base;
 
+  // Items: with a work counter (persistent launch) the producer claims the
+  // next item of the longest-first list with an atomic add whenever it is
+  // ready for one, and publishes its index to the other roles through a small
+  // ring in shared memory (-1 ends the list); without one, CTA i runs item i.
+  // Items with no K/V tile in the selected ring step take part in no barrier.
+  auto next_item = [&](int* spos, bool* ok) -> int {  // consumers of the ring
+    const int s = *spos % kSchedSlots;
+    *ok = __all_sync(__activemask(), mbar_wait(&ctl->sched_full[s], (*spos / kSchedSlots) & 1,
+                                               p.status, abort));
+    if (!*ok) return -1;
+    const int k = *reinterpret_cast<volatile int*>(&ctl->sched[s]);
+    __syncwarp(__activemask());
+    if (warp == 1 || lane == 0) mbar_arrive(&ctl->sched_empty[s]);
+    ++*spos;
+    return k;
+  };
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (elect_one_sync() && n > 0) {
+    if (elect_one_sync()) {
       tma_prefetch_map(&map_q);
       tma_prefetch_map(&map_k);
       tma_prefetch_map(&map_v);
-      mbar_arrive_expect_tx(&ctl->q_full, (has_b ? 2 : 1) * kTileBytes);
-      for (int hf = 0; hf < 2; ++hf) {
-        tma_load_3d(smem + kOffQ + hf * kHalfBytes, &map_q, &ctl->q_full, hf * 64, it.head[0],
-                    it.q0[0]);
-        if (has_b)
-          tma_load_3d(smem + kOffQ + kTileBytes + hf * kHalfBytes, &map_q, &ctl->q_full, hf * 64,
-                      it.head[1], it.q0[1]);
-      }
-      int li = 0;
+      int li = 0;      // K/V ring position, continued across items
+      int items = 0;   // items with work so far (Q buffer uses)
+      int spos = 0;    // item-index ring position
       bool ok = true;
-      for (int si = 0; si < it.seg_count && ok; ++si) {
-        const PlanSegment sg = p.segs[it.seg_begin + si];
-        if (!seg_selected(sg, p.step_filter)) continue;
-        for (int kt = sg.k0; kt < sg.k1 && ok; kt += kBN) {
-          for (int kv = 0; kv < 2; ++kv, ++li) {
-            const int slot = li % kStages;
-            if (li >= kStages &&
-                !mbar_wait(&ctl->kv_empty[slot], ((li / kStages) - 1) & 1, p.status, abort)) {
-              ok = false;
-              break;
+      for (bool first = true; ok; first = false) {
+        int k = -1;
+        if (p.work_counter) {
+          k = atomicAdd(p.work_counter, 1);
+          if (k >= p.num_items) k = -1;
+        } else if (first) {
+          k = blockIdx.x;
+        }
+        const int s = spos % kSchedSlots;
+        if (spos >= kSchedSlots &&
+            !mbar_wait(&ctl->sched_empty[s], ((spos / kSchedSlots) - 1) & 1, p.status, abort)) {
+          ok = false;
+          break;
+        }
+        ctl->sched[s] = k;
+        mbar_arrive(&ctl->sched_full[s]);
+        ++spos;
+        if (k < 0) break;
+        const PlanItem it = p.items[k];
+        const int n = item_tiles(it, p);
+        if (n == 0) continue;
+        const bool has_b = it.qlen[1] > 0;
+        const int g = it.head[0] / p.group;
+        // the previous item's last S MMAs have read the Q buffer
+        if (items > 0 && !mbar_wait(&ctl->q_empty, (items - 1) & 1, p.status, abort)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&ctl->q_full, (has_b ? 2 : 1) * kTileBytes);
+        for (int hf = 0; hf < 2; ++hf) {
+          tma_load_3d(smem + kOffQ + hf * kHalfBytes, &map_q, &ctl->q_full, hf * 64, it.head[0],
+                      it.q0[0]);
+          if (has_b)
+            tma_load_3d(smem + kOffQ + kTileBytes + hf * kHalfBytes, &map_q, &ctl->q_full,
+                        hf * 64, it.head[1], it.q0[1]);
+        }
+        ++items;
+        for (int si = 0; si < it.seg_count && ok; ++si) {
+          const PlanSegment sg = p.segs[it.seg_begin + si];
+          if (!seg_selected(sg, p.step_filter)) continue;
+          for (int kt = sg.k0; kt < sg.k1 && ok; kt += kBN) {
+            for (int kv = 0; kv < 2; ++kv, ++li) {
+              const int slot = li % kStages;
+              if (li >= kStages &&
+                  !mbar_wait(&ctl->kv_empty[slot], ((li / kStages) - 1) & 1, p.status, abort)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&ctl->kv_full[slot], kTileBytes);
+              const CUtensorMap* map = kv == 0 ? &map_k : &map_v;
+              for (int hf = 0; hf < 2; ++hf)
+                tma_load_3d(smem + kOffKV + slot * kTileBytes + hf * kHalfBytes, map,
+                            &ctl->kv_full[slot], hf * 64, g, kt);
             }
-            mbar_arrive_expect_tx(&ctl->kv_full[slot], kTileBytes);
-            const CUtensorMap* map = kv == 0 ? &map_k : &map_v;
-            for (int hf = 0; hf < 2; ++hf)
-              tma_load_3d(smem + kOffKV + slot * kTileBytes + hf * kHalfBytes, map,
-                          &ctl->kv_full[slot], hf * 64, g, kt);
           }
         }
       }
@@ -179,58 +243,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int last = s + ((li - 1 - s) / kStages) * kStages;
         mbar_wait(&ctl->kv_full[s], (last / kStages) & 1, p.status, nullptr);
       }
-      mbar_wait(&ctl->q_full, 0, p.status, nullptr);
+      if (items > 0) mbar_wait(&ctl->q_full, (items - 1) & 1, p.status, nullptr);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
-    if (elect_one_sync() && n > 0) {
+    if (elect_one_sync()) {
       const uint32_t tS[2] = {tmem + 0, tmem + 128};
       const uint32_t tO[2] = {tmem + 256, tmem + 384};
       const uint32_t sQx[2] = {sQ, sQ + kTileBytes};
-      bool ok = mbar_wait(&ctl->q_full, 0, p.status, abort);
-      tc_fence_after_sync();
       auto kv_ready = [&](int li) {
         return mbar_wait(&ctl->kv_full[li % kStages], (li / kStages) & 1, p.status, abort);
       };
       auto slot_addr = [&](int li) { return sKV + (li % kStages) * kTileBytes; };
-      if (ok && (ok = kv_ready(0))) {
+      int li = 0;            // K/V ring position
+      int items = 0;         // items with work so far
+      int done[2] = {0, 0};  // P tiles consumed so far, per query tile (p_full phases)
+      int spos = 0;
+      bool ok = true;
+      for (;;) {
+        const int k = next_item(&spos, &ok);
+        if (k < 0) break;
+        const PlanItem it = p.items[k];
+        const int n = item_tiles(it, p);
+        if (n == 0) continue;
+        const bool has_b = it.qlen[1] > 0;
+        if (!(ok = mbar_wait(&ctl->q_full, items & 1, p.status, abort) && kv_ready(li))) break;
         tc_fence_after_sync();
-        issue_qk(tS[0], sQx[0], slot_addr(0));
+        issue_qk(tS[0], sQx[0], slot_addr(li));
         mma_commit(&ctl->s_full[0]);
         if (has_b) {
-          issue_qk(tS[1], sQx[1], slot_addr(0));
+          issue_qk(tS[1], sQx[1], slot_addr(li));
           mma_commit(&ctl->s_full[1]);
         }
-        mma_commit(&ctl->kv_empty[0]);
-      }
-      for (int j = 0; j < n && ok; ++j) {
-        const int liV = 2 * j + 1, liK = 2 * j + 2;
-        if (!(ok = kv_ready(liV))) break;
-        if (!(ok = mbar_wait(&ctl->p_full[0], j & 1, p.status, abort))) break;
-        tc_fence_after_sync();
-        issue_pv(tO[0], tS[0], slot_addr(liV), j > 0);
-        if (j == n - 1) mma_commit(&ctl->o_full[0]);
-        const bool more = j + 1 < n;
-        if (more) {
-          if (!(ok = kv_ready(liK))) break;
+        mma_commit(&ctl->kv_empty[li % kStages]);
+        if (n == 1) mma_commit(&ctl->q_empty);  // no further S of this item reads Q
+        for (int j = 0; j < n && ok; ++j) {
+          const int liV = li + 2 * j + 1, liK = li + 2 * j + 2;
+          if (!(ok = kv_ready(liV))) break;
+          if (!(ok = mbar_wait(&ctl->p_full[0], done[0] & 1, p.status, abort))) break;
+          ++done[0];
           tc_fence_after_sync();
-          issue_qk(tS[0], sQx[0], slot_addr(liK));
-          mma_commit(&ctl->s_full[0]);
-        }
-        if (has_b) {
-          if (!(ok = mbar_wait(&ctl->p_full[1], j & 1, p.status, abort))) break;
-          tc_fence_after_sync();
-          issue_pv(tO[1], tS[1], slot_addr(liV), j > 0);
-          if (j == n - 1) mma_commit(&ctl->o_full[1]);
-        }
-        mma_commit(&ctl->kv_empty[liV % kStages]);
-        if (more) {
-          if (has_b) {
-            issue_qk(tS[1], sQx[1], slot_addr(liK));
-            mma_commit(&ctl->s_full[1]);
+          issue_pv(tO[0], tS[0], slot_addr(liV), j > 0);
+          if (j == n - 1) mma_commit(&ctl->o_full[0]);
+          const bool more = j + 1 < n;
+          if (more) {
+            if (!(ok = kv_ready(liK))) break;
+            tc_fence_after_sync();
+            issue_qk(tS[0], sQx[0], slot_addr(liK));
+            mma_commit(&ctl->s_full[0]);
           }
-          mma_commit(&ctl->kv_empty[liK % kStages]);
+          if (has_b) {
+            if (!(ok = mbar_wait(&ctl->p_full[1], done[1] & 1, p.status, abort))) break;
+            ++done[1];
+            tc_fence_after_sync();
+            issue_pv(tO[1], tS[1], slot_addr(liV), j > 0);
+            if (j == n - 1) mma_commit(&ctl->o_full[1]);
+          }
+          mma_commit(&ctl->kv_empty[liV % kStages]);
+          if (more) {
+            if (has_b) {
+              issue_qk(tS[1], sQx[1], slot_addr(liK));
+              mma_commit(&ctl->s_full[1]);
+            }
+            mma_commit(&ctl->kv_empty[liK % kStages]);
+            if (j + 2 == n) mma_commit(&ctl->q_empty);  // that was the item's last S
+          }
         }
+        li += 2 * n;
+        ++items;
       }
       if (!ok) *abort = 1;
       // every MMA this thread issued has completed before TMEM is released
@@ -242,31 +322,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int x = (warp - 4) >> 2;  // query tile
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
-    if (x == 0 || has_b) {
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_off + x * 128;
+    const uint32_t tO = tmem + lane_off + 256 + x * 128;
+    const float sl2 = p.scale_log2;
+    int seen = 0;   // S tiles of this query-tile slot so far (s_full phases)
+    int items = 0;  // items of this slot with work so far (o_full phases)
+    int spos = 0;
+    bool ok = true;
+    for (;;) {
+      const int k = next_item(&spos, &ok);
+      if (k < 0) break;
+      const PlanItem it = p.items[k];
+      if (x == 1 && it.qlen[1] == 0) continue;
+      const int n = item_tiles(it, p);
       // x is uniform per warp: select fields instead of indexing the item
       const int row = (x ? it.q0[1] : it.q0[0]) + r;
       const bool valid = r < (x ? it.qlen[1] : it.qlen[0]);
       const int head = x ? it.head[1] : it.head[0];
       int lo = 0, hi = 0;
       if (valid) row_key_interval(p, row, &lo, &hi);
-      const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-      const uint32_t tS = tmem + lane_off + x * 128;
-      const uint32_t tO = tmem + lane_off + 256 + x * 128;
       const int mlo = x ? it.mask_lo[1] : it.mask_lo[0];
       const int mhi = x ? it.mask_hi[1] : it.mask_hi[0];
-      const float sl2 = p.scale_log2;
       float m2 = -INFINITY;  // running max, log2 units
       float l = 0.f;
-      bool ok = true;
       int j = 0;
       for (int si = 0; si < it.seg_count && ok; ++si) {
         const PlanSegment sg = p.segs[it.seg_begin + si];
         if (!seg_selected(sg, p.step_filter)) continue;
         const int a = max(lo, sg.k0), b = min(hi, sg.k1);
         const int full_lo = max(sg.k0, mlo), full_hi = min(sg.k1, mhi);
-        for (int kt = sg.k0; kt < sg.k1; kt += kBN, ++j) {
+        for (int kt = sg.k0; kt < sg.k1; kt += kBN, ++j, ++seen) {
           // .sync.aligned TMEM accesses follow: keep the warp's decision uniform
-          ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_full[x], j & 1, p.status, abort));
+          ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_full[x], seen & 1, p.status, abort));
           if (!ok) break;
           tc_fence_after_sync();
           float s[kBN];
@@ -323,8 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive(&ctl->p_full[x]);
         }
       }
-      if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->o_full[x], 0, p.status, abort));
-      if (!ok) *abort = 1;
+      if (ok && n > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->o_full[x], items & 1, p.status, abort));
+        ++items;
+      }
+      if (!ok) break;
       tc_fence_after_sync();
       // ------------------------------------------------------- epilogue
       const bool empty = !(l > 0.f);
@@ -333,13 +424,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t u[32];
-        if (ok && n > 0) {
+        if (n > 0) {
           tmem_load_32(tO + c * 32, u);
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) u[i] = 0u;
         }
-        if (valid && ok) {
+        if (valid) {
           if (p.out_fp32) {
             float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + ob + c * 32);
 #pragma unroll
@@ -363,10 +454,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (valid && ok)
+      if (valid)
         p.lse[(size_t)head * p.T + row] =
             empty ? -INFINITY : (m2 + log2f(l)) * 0.69314718055994530942f;
+      // the epilogue's TMEM reads precede the next item's first P (and with
+      // it the PV MMA that overwrites O)
+      tc_fence_before_sync();
     }
+    if (!ok) *abort = 1;
   }
 
   tc_fence_before_sync();
@@ -390,8 +485,12 @@ cudaError_t launch_fwd_tc_bf16(const FwdParams& p, const CUtensorMap& map_q,
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  // persistent: one CTA per SM (shared memory and TMEM allow no more), each
+  // claiming items from the work counter; without one, one item per CTA
+  const int grid = p.work_counter ? p.num_ctas : p.num_items;
+  if (grid == 0) return cudaSuccess;
   TraceScope trace_scope(stream, "fwd_tc_bf16_kernel");
-  fwd_tc_bf16_kernel<<<p.num_items, kThreads, kSmemBytes, stream>>>(map_q, map_k, map_v, p);
+  fwd_tc_bf16_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_q, map_k, map_v, p);
   return cudaGetLastError();
 }
 
