@@ -242,8 +242,9 @@ def oracle_sample(w, inputs, budget_s: float, seed: int, backward: bool):
     parts = [("forward rows", run_fwd)] + ([("dQ rows", run_bwd)] if backward else [])
     flops, secs, desc = 0.0, 0.0, []
     for name, fn in parts:
-        f0, t0 = fn(32)                               # calibrate
-        n = int(min(max(budget_s / len(parts) / max(t0 / 32, 1e-6), 32), 200000))
+        fn(32)                                        # warm the thread pool
+        f0, t0 = fn(128)                              # calibrate
+        n = int(min(max(budget_s / len(parts) / max(t0 / 128, 1e-6), 32), 400000))
         f1, t1 = fn(n)
         flops += f1
         secs += t1
@@ -520,7 +521,7 @@ def main():
                     help="fwd: forward only; fwdbwd: forward then backward (the whole path)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--cpu-budget", type=float, default=10.0,
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -1,0 +1,87 @@
+"""Host-side logic of bench.py, without a GPU: the FLOP accounting and the
+multi-process path (replicas: a barrier, the max of the ranks' times, and
+rank 0 alone printing), run as world-size-2 gloo ranks on the CPU."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from context_long_sequence_fwd_b300.workloads import WORKLOADS  # noqa: E402
+
+
+def test_flop_accounting():
+    w = WORKLOADS["causal_gqa_t32768_p8_zigzag"]
+    # causal: 4 Hq D T^2 / 2 (two matmuls of 2 flops per multiply-add, half the pairs)
+    assert bench.fwd_flops(w, None) == 4.0 * 32 * 128 * 32768 ** 2 / 2
+    assert bench.visible_pairs(w, None) == 32768 * 32769 // 2
+    t = WORKLOADS["tiny_fp32_noncausal_t256"]
+    assert bench.fwd_flops(t, None) == 4.0 * 2 * 64 * 256 ** 2
+    # packed documents: the sum over documents of L^2
+    v = WORKLOADS["varlen_causal_gqa_t65536_p8_contiguous"]
+    cu = [0, 1000, 1000, 65536]
+    assert bench.fwd_flops(v, cu) == 4.0 * 32 * 128 * (1000 ** 2 + 64536 ** 2) / 2
+    assert bench.visible_pairs(v, cu) == 1000 * 1001 // 2 + 64536 * 64537 // 2
+
+
+def free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    bench.barrier(world)
+    # the slowest rank's time is the job's time
+    q.put((rank, bench.max_over_ranks(10.0 + rank, world)))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == {0: 11.0, 1: 11.0}
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Two ranks of the reference arm: rank 0 alone times the oracle and
+    prints one JSON line; rank 1 exits 0 without work."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(free_port()), "bench.py",
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3",
+           "--cpu-budget", "0.5", "--workload", "tiny_fp32_noncausal_t256", "--pass", "fwd"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_ours_refuses_without_gpu():
+    """The product arm never falls back to the CPU."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    r = subprocess.run([sys.executable, "bench.py", "--steps", "1", "--warmup", "3"], cwd=ROOT,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0 and "needs a CUDA device" in (r.stdout + r.stderr)

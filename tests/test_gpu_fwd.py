@@ -170,3 +170,26 @@ def test_causal_gqa_t32768_p8_zigzag():
 
 def test_varlen_causal_gqa_t65536_p8_contiguous():
     sampled_check("varlen_causal_gqa_t65536_p8_contiguous", 384)
+
+
+def test_concurrent_launches_reuse_work_counters():
+    """140 fused forwards on two streams at once (more launches than the
+    library's 64 work-counter slots): every result equals the first one bit
+    for bit -- each item is computed by exactly one CTA, whichever claims it."""
+    T, hq, hkv, P = 2048, 4, 2, 4
+    q, k, v = (t.to(DEV) for t in make_qkv(T, hq, hkv, 128, "bf16", seed=9))
+    ref_o, ref_l = ra.ringattn_fwd(q, k, v, None, P, ra.ZIGZAG, True)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    results = []
+    for i in range(140):
+        st = streams[i % 2]
+        with torch.cuda.stream(st):
+            o = torch.empty_like(q)
+            l = torch.empty(hq, T, device=DEV)
+            ra.ringattn_fwd(q, k, v, None, P, ra.ZIGZAG, True, o, l, stream=st)
+            results.append((o, l))
+    torch.cuda.synchronize()
+    assert ra.ringattn_get_status() == 0
+    for o, l in results:
+        assert torch.equal(o, ref_o) and torch.equal(l, ref_l)
