@@ -338,6 +338,36 @@ def run_ours(args):
     clk = clocks.summary()
     peak_mem = torch.cuda.max_memory_allocated(dev)
 
+    # The memory-bound kernels, against the measured copy bandwidth: the
+    # backward preprocess (from the trace of the timed region) and the
+    # standalone log-sum-exp merge of two bf16 partial results of this
+    # workload's size (timed here on its own; the fused forward merges in
+    # registers and TMEM, the stepwise forward and multi-GPU callers use it).
+    hbm = {}
+    T_, H_, D_ = w.total_tokens, w.hq, w.head_dim
+    if backward and "bwd_preprocess_kernel" in kernels:
+        n, ms = kernels["bwd_preprocess_kernel"]
+        nbytes = 2 * T_ * H_ * D_ * 2 + H_ * T_ * 4  # read O, dO (bf16); write D (fp32)
+        hbm["bwd_preprocess_kernel"] = {"bytes_per_launch": nbytes, "avg_ms": round(ms / n, 4),
+                                        "gbs": round(nbytes / (ms / n * 1e-3) / 1e9, 1)}
+    oa, ob = torch.randn_like(out), torch.randn_like(out)
+    la = torch.randn(H_, T_, device=dev)
+    lb = torch.randn(H_, T_, device=dev)
+    for _ in range(3):
+        ra.attn_lse_merge(oa, la, ob, lb, stream)
+    m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 10
+    m0.record(stream)
+    for _ in range(reps):
+        ra.attn_lse_merge(oa, la, ob, lb, stream)
+    m1.record(stream)
+    torch.cuda.synchronize()
+    mms = m0.elapsed_time(m1) / reps
+    nbytes = 3 * T_ * H_ * D_ * 2 + 3 * H_ * T_ * 4  # read o_a, o_b, lse_a, lse_b; write o_a, lse_a
+    hbm["lse_merge_kernel"] = {"bytes_per_launch": nbytes, "avg_ms": round(mms, 4),
+                               "gbs": round(nbytes / (mms * 1e-3) / 1e9, 1)}
+    del oa, ob, la, lb
+
     # End to end through the public API from pinned host memory: every step
     # copies its inputs in and all of its outputs back.  Two buffer sets and
     # two copy streams pipeline the steps, the way a caller overlaps transfers
@@ -457,6 +487,10 @@ def run_ours(args):
                 "pipelining": "2 buffer sets; copies on 2 streams overlap the previous "
                               "and next steps' compute"},
         "gpu_launches": sum(n for n, _ in kernels.values()),
+        "hbm_kernels": {**{k: {**v, "frac": round(v["gbs"] / float(peaks["hbm_gbs"]), 4)}
+                           for k, v in hbm.items()},
+                        "peak_gbs": float(peaks["hbm_gbs"]),
+                        "peak_source": peaks["source"] + " hbm_gbs (copy)"},
         "clocks": clk,
         "peak_mem_gb": round(peak_mem / 1e9, 3),
         "status": ra.STATUS.get(status, status),

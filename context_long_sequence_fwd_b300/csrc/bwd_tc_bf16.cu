@@ -109,47 +109,52 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t
 
 // Elementwise core of the backward for 32 score columns of one TMEM row:
 //   P = 2^(S scale log2(e) - lse log2(e)),  dS = P (dP - D),
-// with the columns the mask hides forced to P = 0 by an exponent of -inf
-// (2^-inf = +0): a select, never a branch around the exponential.  kMasked
-// is false for tiles every column of which is visible.  The per-column
-// statistics come from `col` (dK/dV: one query per column), or are the
-// thread's own (dQ: one query per row, col == nullptr).
-struct RowInfo {
-  float lse2;  // lse_i * log2(e)
-  float Dv;    // D_i
-  int lo, hi;  // keys row i may see: [lo, hi); empty for rows outside the segment
-};
-
+// two columns per paired fp32 instruction, with the columns the mask hides
+// forced to P = 0 by an exponent of -inf (2^-inf = +0): a select, never a
+// branch around the exponential.  kMasked is false for tiles every column of
+// which is visible.  The per-column statistics come from `stat` (dK/dV: one
+// query per column, stored per column pair as (-lse log2 e, -lse log2 e,
+// -D, -D) and read with one 16-byte load) and `range` (its visible keys), or
+// are the thread's own (dQ: one query per row, stat == nullptr).
 template <bool kMasked, bool kWantP>
 __device__ __forceinline__ void bwd_elementwise32(const uint32_t (&us)[32], const uint32_t (&ud)[32],
-                                                  const RowInfo* col, float lse2, float Dv,
-                                                  int key, int key0, int a, int b, float sl2,
-                                                  uint32_t (&pp)[16], uint32_t (&pd)[16]) {
+                                                  const float4* stat, const int2* range,
+                                                  float lse2, float Dv, int key, int key0, int a,
+                                                  int b, float sl2, uint32_t (&pp)[16],
+                                                  uint32_t (&pd)[16]) {
+  const uint64_t sl2x2 = f32x2(sl2, sl2);
+  const uint64_t own_nl2 = f32x2(-lse2, -lse2), own_nd = f32x2(-Dv, -Dv);
 #pragma unroll
   for (int c = 0; c < 32; c += 2) {
-    float pv[2], dv[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      float l2 = lse2, d = Dv;
-      if (col != nullptr) {
-        l2 = col[c + e].lse2;
-        d = col[c + e].Dv;
-      }
-      float x = fmaf(__uint_as_float(us[c + e]), sl2, -l2);
-      if (kMasked) {
-        bool vis;
-        if (col != nullptr)  // fixed key row, one query per column
-          vis = key >= col[c + e].lo && key < col[c + e].hi;
-        else                 // fixed query row, one key per column
-          vis = key0 + c + e >= a && key0 + c + e < b;
-        x = vis ? x : -INFINITY;
-      }
-      const float pe = fast_exp2(x);
-      pv[e] = pe;
-      dv[e] = pe * (__uint_as_float(ud[c + e]) - d);
+    uint64_t nl2 = own_nl2, nd = own_nd;
+    if (stat != nullptr) {
+      const float4 st = stat[c / 2];
+      nl2 = f32x2(st.x, st.y);
+      nd = f32x2(st.z, st.w);
     }
-    if (kWantP) pp[c / 2] = pack_bf16x2(pv[0], pv[1]);
-    pd[c / 2] = pack_bf16x2(dv[0], dv[1]);
+    float x[2];
+    f32x2_split(ffma2(f32x2(__uint_as_float(us[c]), __uint_as_float(us[c + 1])), sl2x2, nl2),
+                &x[0], &x[1]);
+    if (kMasked) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        bool vis;
+        if (stat != nullptr) {  // fixed key row, one query per column
+          const int2 rg = range[c + e];
+          vis = key >= rg.x && key < rg.y;
+        } else {                // fixed query row, one key per column
+          vis = key0 + c + e >= a && key0 + c + e < b;
+        }
+        x[e] = vis ? x[e] : -INFINITY;
+      }
+    }
+    const float p0 = fast_exp2(x[0]), p1 = fast_exp2(x[1]);
+    const uint64_t pv = f32x2(p0, p1);
+    const uint64_t t = fadd2(f32x2(__uint_as_float(ud[c]), __uint_as_float(ud[c + 1])), nd);
+    float d0, d1;
+    f32x2_split(fmul2(pv, t), &d0, &d1);
+    if (kWantP) pp[c / 2] = pack_bf16x2(p0, p1);
+    pd[c / 2] = pack_bf16x2(d0, d1);
   }
 }
 
@@ -160,8 +165,10 @@ constexpr int kOffK = 0;
 constexpr int kOffV = kTileBytes;
 constexpr int kOffStage = 2 * kTileBytes;                      // per stage: Q, dO
 constexpr int kStageBytes = 2 * kTileBytes;
-constexpr int kOffInfo = kOffStage + kKvStages * kStageBytes;  // per stage: 128 RowInfo + flag
-constexpr int kInfoBytes = 128 * sizeof(RowInfo) + 16;
+constexpr int kOffInfo = kOffStage + kKvStages * kStageBytes;  // per stage: row values + flags
+// per stage: (-lse log2 e, -D) of the 128 query rows, interleaved by column
+// pair | their visible key ranges | 2 flags
+constexpr int kInfoBytes = 128 * sizeof(float2) + 128 * sizeof(int2) + 16;
 constexpr int kOffCtlKV = kOffInfo + kKvStages * ((kInfoBytes + 127) / 128 * 128);
 constexpr int kSmemKV = kOffCtlKV + 256 + 1024;
 
@@ -279,7 +286,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                    p.status, abort));
             if (!ok) break;
           }
-          RowInfo* info = reinterpret_cast<RowInfo*>(smem + kOffInfo + slot * ((kInfoBytes + 127) / 128 * 128));
+          uint8_t* info = smem + kOffInfo + slot * ((kInfoBytes + 127) / 128 * 128);
+          float* stat = reinterpret_cast<float*>(info);  // [64 pairs][nl2 a, nl2 b, nd a, nd b]
+          int2* range = reinterpret_cast<int2*>(info + 128 * sizeof(float2));
           float lv[2], dv[2];
 #pragma unroll
           for (int k = 0; k < 2; ++k) {
@@ -293,22 +302,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 2; ++k) {
             const int r = rbase + lane + 32 * k;
             const int i = i0 + r;
-            RowInfo ri{0.f, 0.f, 0, 0};
+            float2 st = make_float2(0.f, 0.f);  // (lse log2 e, D)
+            int2 rg = make_int2(0, 0);  // rows outside the segment see no key
             if (i < sg.q1) {
               int ds = ds0, de = de0;
               if (i >= de0) doc_bounds(p.cu, p.num_docs, i, &ds, &de);
-              ri.lse2 = lv[k] * kLog2e;
-              ri.Dv = dv[k];
-              ri.lo = ds;
-              ri.hi = p.causal ? i + 1 : de;
+              st = make_float2(lv[k] * kLog2e, dv[k]);
+              rg = make_int2(ds, p.causal ? i + 1 : de);
             }
             // the tile needs no mask if every row is in the segment and sees
             // every key of the tile
-            full = full && (i < sg.q1) && ri.lo <= it.k0 && ri.hi >= kend;
-            info[r] = ri;
+            full = full && (i < sg.q1) && rg.x <= it.k0 && rg.y >= kend;
+            stat[(r >> 1) * 4 + (r & 1)] = -st.x;
+            stat[(r >> 1) * 4 + 2 + (r & 1)] = -st.y;
+            range[r] = rg;
           }
           full = __all_sync(0xffffffffu, full);
-          if (lane == 0) reinterpret_cast<int*>(info + kTile)[warp - 2] = full ? 1 : 0;
+          if (lane == 0)
+            reinterpret_cast<int*>(info + 128 * (sizeof(float2) + sizeof(int2)))[warp - 2] =
+                full ? 1 : 0;
           __syncwarp();
           mbar_arrive(&ctl->info_full[slot]);
         }
@@ -382,20 +394,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_full[x], jj & 1, p.status, abort));
       if (!ok) break;
       tc_fence_after_sync();
-      const RowInfo* info = reinterpret_cast<const RowInfo*>(smem + kOffInfo + slot * ((kInfoBytes + 127) / 128 * 128));
-      const int* flags = reinterpret_cast<const int*>(info + kTile);
+      const uint8_t* info = smem + kOffInfo + slot * ((kInfoBytes + 127) / 128 * 128);
+      const int* flags = reinterpret_cast<const int*>(info + 128 * (sizeof(float2) + sizeof(int2)));
       const bool full = flags[0] != 0 && flags[1] != 0;
-      const RowInfo* hinfo = info + x * 64;
+      const float4* hstat = reinterpret_cast<const float4*>(info) + x * 32;
+      const int2* hrange = reinterpret_cast<const int2*>(info + 128 * sizeof(float2)) + x * 64;
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
         uint32_t us[32], ud[32];
-        tmem_load_32(tS + c2 * 32, us);
-        tmem_load_32(tdP + c2 * 32, ud);
+        tmem_load_2x32(tS + c2 * 32, us, tdP + c2 * 32, ud);
         uint32_t pp[16], pd[16];
         if (full)
-          bwd_elementwise32<false, true>(us, ud, hinfo + c2 * 32, 0.f, 0.f, j, 0, 0, 0, sl2, pp, pd);
+          bwd_elementwise32<false, true>(us, ud, hstat + c2 * 16, hrange + c2 * 32, 0.f, 0.f, j,
+                                         0, 0, 0, sl2, pp, pd);
         else
-          bwd_elementwise32<true, true>(us, ud, hinfo + c2 * 32, 0.f, 0.f, j, 0, 0, 0, sl2, pp, pd);
+          bwd_elementwise32<true, true>(us, ud, hstat + c2 * 16, hrange + c2 * 32, 0.f, 0.f, j,
+                                        0, 0, 0, sl2, pp, pd);
         tmem_store_16(tS + c2 * 16, pp);
         tmem_store_16(tdP + c2 * 16, pd);
       }
@@ -691,9 +705,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->dp_full, j & 1, p.status, abort));
         if (!ok) break;
         tc_fence_after_sync();
-        uint32_t ud0[32], ud1[32];
-        tmem_load_32(tdP, ud0);
-        tmem_load_32(tdP + 32, ud1);
+        uint32_t ud[64];  // this warpgroup's 64 dP columns, one load
+        tmem_load_64(tdP, ud);
         tc_fence_before_sync();
         mbar_arrive(&ctl->dp_free);  // dP(j+1) may now overwrite dP(j)
         const uint32_t tS = tmem + lane_off + (j & 1) * 128 + 64 * w;
@@ -704,12 +717,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t us[32];
           tmem_load_32(tS + c2 * 32, us);
           uint32_t pp[16], pd[16];  // pp unused: dQ needs dS only
+          const uint32_t(&udc)[32] = *reinterpret_cast<const uint32_t(*)[32]>(ud + c2 * 32);
           if (full)
-            bwd_elementwise32<false, false>(us, c2 == 0 ? ud0 : ud1, nullptr, lse2, Dv, 0,
-                                            kb + c2 * 32, a, b, sl2, pp, pd);
+            bwd_elementwise32<false, false>(us, udc, nullptr, nullptr, lse2, Dv, 0, kb + c2 * 32,
+                                            a, b, sl2, pp, pd);
           else
-            bwd_elementwise32<true, false>(us, c2 == 0 ? ud0 : ud1, nullptr, lse2, Dv, 0,
-                                           kb + c2 * 32, a, b, sl2, pp, pd);
+            bwd_elementwise32<true, false>(us, udc, nullptr, nullptr, lse2, Dv, 0, kb + c2 * 32,
+                                           a, b, sl2, pp, pd);
           // dS over the first half of the columns this warpgroup just read
           tmem_store_16(tS + c2 * 16, pd);
         }

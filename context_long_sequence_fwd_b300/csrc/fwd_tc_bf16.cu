@@ -358,12 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after_sync();
           float s[kBN];
+          {
+            uint32_t u[kBN];  // one load of the row's 128 scores, one wait
+            tmem_load_128(tS, u);
 #pragma unroll
-          for (int c = 0; c < kBN / 32; ++c) {
-            uint32_t u[32];
-            tmem_load_32(tS + c * 32, u);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(u[i]);
+            for (int i = 0; i < kBN; ++i) s[i] = __uint_as_float(u[i]);
           }
           // keys outside [a, b) are hidden unless the whole tile is visible
           // to every row of this query tile
@@ -374,9 +373,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (key < a || key >= b) s[c] = -INFINITY;
             }
           }
-          float mx = s[0];
+          // row max: four interleaved chains of 3-input maxes
+          float m4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-          for (int c = 1; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+          for (int c = 4; c < kBN - 4; c += 8) {
+            m4[0] = fmax3(m4[0], s[c], s[c + 1]);
+            m4[1] = fmax3(m4[1], s[c + 2], s[c + 3]);
+            m4[2] = fmax3(m4[2], s[c + 4], s[c + 5]);
+            m4[3] = fmax3(m4[3], s[c + 6], s[c + 7]);
+          }
+          m4[0] = fmax3(m4[0], s[kBN - 4], s[kBN - 3]);
+          m4[1] = fmax3(m4[1], s[kBN - 2], s[kBN - 1]);
+          const float mx = fmax3(fmaxf(m4[0], m4[1]), m4[2], m4[3]);
           const float m_new = fmaxf(m2, mx * sl2);
           const bool resc = m_new > m2 + kRescaleThreshold;
           float alpha = 1.f;
@@ -385,14 +393,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             m2 = m_new;
           }
           const float m_use = (m2 == -INFINITY) ? 0.f : m2;
-          float sum = 0.f;
+          // P = 2^(S scale log2 e - m), two columns per paired FMA and add
+          const uint64_t sl2x2 = f32x2(sl2, sl2), negm2 = f32x2(-m_use, -m_use);
+          uint64_t acc[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
           uint32_t pk[kBN / 2];
 #pragma unroll
           for (int c = 0; c < kBN / 2; ++c) {
-            const float p0 = fast_exp2(fmaf(s[2 * c], sl2, -m_use));
-            const float p1 = fast_exp2(fmaf(s[2 * c + 1], sl2, -m_use));
-            sum += p0 + p1;
+            float x0, x1;
+            f32x2_split(ffma2(f32x2(s[2 * c], s[2 * c + 1]), sl2x2, negm2), &x0, &x1);
+            const float p0 = fast_exp2(x0);
+            const float p1 = fast_exp2(x1);
+            acc[c & 1] = fadd2(acc[c & 1], f32x2(p0, p1));
             pk[c] = pack_bf16x2(p0, p1);
+          }
+          float sum;
+          {
+            float a0, a1, b0, b1;
+            f32x2_split(acc[0], &a0, &a1);
+            f32x2_split(acc[1], &b0, &b1);
+            sum = (a0 + b0) + (a1 + b1);
           }
           l = l * alpha + sum;
           tmem_store_64(tS, pk);

@@ -193,3 +193,22 @@ def test_concurrent_launches_reuse_work_counters():
     assert ra.ringattn_get_status() == 0
     for o, l in results:
         assert torch.equal(o, ref_o) and torch.equal(l, ref_l)
+
+
+def test_causal_gqa_t32768_full_rows_of_two_kv_groups():
+    """Every output of the first and last kv-head groups (q heads 0-3 and
+    28-31) on three 256-row blocks: the sequence start, the boundary between
+    zigzag chunks 0 and 1, and the end (heads are independent, so these rows
+    check the whole schedule a query tile of those heads goes through)."""
+    w = WORKLOADS["causal_gqa_t32768_p8_zigzag"]
+    x = make_inputs(w, seed=0)
+    o, l = run_fwd(x["q"], x["k"], x["v"], None, w.num_shards, w.layout, w.causal)
+    C = w.total_tokens // (2 * w.num_shards)
+    rows = np.concatenate([np.arange(0, 256), np.arange(C - 128, C + 128),
+                           np.arange(w.total_tokens - 256, w.total_tokens)]).astype(np.int32)
+    heads = np.array([0, 1, 2, 3, 28, 29, 30, 31], np.int32)
+    hs = np.repeat(heads, rows.size)
+    is_ = np.tile(rows, heads.size)
+    ro, rl = oracle.fwd_rows(x["q"], x["k"], x["v"], hs, is_, causal=True)
+    assert max_err(o[is_, hs], ro) <= TOL_BF16_O
+    assert max_err(l[hs, is_], rl) <= TOL_BF16_LSE
