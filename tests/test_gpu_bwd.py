@@ -69,6 +69,9 @@ def test_fp32_backward(case):
     check_full(q, k, v, do, cu, P, layout, causal, TOL_FP32_GRAD)
 
 
+# 44 packed documents of 1 to 97 tokens (seeded draw), several per 128-row tile
+MANY_DOCS = [0, 79, 88, 106, 129, 147, 225, 310, 367, 371, 381, 414, 457, 518, 565, 591, 607, 675, 747, 751, 763, 807, 845, 932, 983, 1024, 1066, 1131, 1188, 1205, 1277, 1351, 1444, 1521, 1549, 1581, 1644, 1708, 1776, 1861, 1890, 1982, 1983, 1991, 2048]
+
 BF16_CASES = [
     # T, hq, hkv, P, layout, causal, cu
     (256, 2, 2, 1, ra.CONTIGUOUS, False, None),
@@ -81,6 +84,9 @@ BF16_CASES = [
     (2048, 4, 2, 8, ra.CONTIGUOUS, True, [0, 300, 301, 900, 1500, 2048]),
     (2048, 4, 4, 2, ra.ZIGZAG, False, [0, 128, 640, 641, 2048]),
     (1024, 2, 2, 2, ra.CONTIGUOUS, True, [0, 200, 200, 700, 1024]),
+    (2048, 4, 2, 16, ra.ZIGZAG, True, None),             # 32 chunks of 64: half tiles
+    (1024, 1, 1, 4, ra.ZIGZAG, True, None),              # a single head
+    (2048, 4, 2, 4, ra.CONTIGUOUS, True, MANY_DOCS),     # 44 documents shorter than a tile
 ]
 
 
