@@ -290,11 +290,11 @@ def run_ours(args):
 
     def fwd():
         ra.ringattn_fwd(q, k, v, cu, w.num_shards, w.layout, w.causal, out, lse, stream,
-                        w.heads_k_stride)
+                        w.heads_k_stride, w.kv_exchange)
 
     def bwd():
         ra.ringattn_bwd(q, k, v, out, lse, do, cu, w.num_shards, w.layout, w.causal, dq, dk,
-                        dv, ws, stream, w.heads_k_stride)
+                        dv, ws, stream, w.heads_k_stride, kv_exchange=w.kv_exchange)
 
     f_fwd = fwd_flops(w, cu)
     f_step = f_fwd * (3.5 if backward else 1.0)
@@ -400,11 +400,11 @@ def run_ours(args):
         if i >= 2:
             stream.wait_event(ev_out[i % 2])       # step i-2's outputs have left this set
         ra.ringattn_fwd(b["q"], b["k"], b["v"], cu, w.num_shards, w.layout, w.causal, b["out"],
-                        b["lse"], stream, w.heads_k_stride)
+                        b["lse"], stream, w.heads_k_stride, w.kv_exchange)
         if backward:
             ra.ringattn_bwd(b["q"], b["k"], b["v"], b["out"], b["lse"], b["do"], cu,
                             w.num_shards, w.layout, w.causal, b["dq"], b["dk"], b["dv"], ws,
-                            stream, w.heads_k_stride)
+                            stream, w.heads_k_stride, kv_exchange=w.kv_exchange)
         ev_done[i % 2].record(stream)
         with torch.cuda.stream(cout):
             cout.wait_event(ev_done[i % 2])
@@ -469,6 +469,8 @@ def run_ours(args):
                    "hkv": w.hkv, "head_dim": w.head_dim, "num_shards": w.num_shards,
                    "layout": "zigzag" if w.layout == 1 else "contiguous",
                    "causal": w.causal, "varlen_docs": None if cu is None else len(cu) - 1,
+                   "kv_exchange": "allgather" if w.kv_exchange else "ring",
+                   "heads_k_stride": w.heads_k_stride,
                    "pass": args.pass_, "flops_per_step": f_step,
                    "visible_pairs_per_head": visible_pairs(w, cu),
                    "parallelism": f"replicas{world}" if world > 1 else "1gpu",

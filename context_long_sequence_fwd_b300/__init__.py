@@ -20,6 +20,8 @@ import numpy as np
 
 CONTIGUOUS = 0
 ZIGZAG = 1
+RING = 0        # ring_attn_func batch_ring: K/V shards visited in ring order
+ALLGATHER = 1   # ring_attn_func varlen_llama3: gathered K/V in token order
 RA_BF16 = 0
 RA_FP32 = 1
 
@@ -53,7 +55,7 @@ class ra_dims(ctypes.Structure):
     _fields_ = [("total_tokens", ctypes.c_int), ("num_seqs", ctypes.c_int),
                 ("hq", ctypes.c_int), ("hkv", ctypes.c_int), ("head_dim", ctypes.c_int),
                 ("dtype", ctypes.c_int), ("heads_k_stride", ctypes.c_int),
-                ("grad_fp32", ctypes.c_int)]
+                ("grad_fp32", ctypes.c_int), ("kv_exchange", ctypes.c_int)]
 
 
 class ra_trace_entry(ctypes.Structure):
@@ -140,10 +142,10 @@ def _cu_host(cu_seqlens):
     return arr.ctypes.data_as(_i32p), arr.size - 1, arr
 
 
-def make_dims(q, k, num_seqs=0, heads_k_stride=1, grad_fp32=False) -> ra_dims:
+def make_dims(q, k, num_seqs=0, heads_k_stride=1, grad_fp32=False, kv_exchange=RING) -> ra_dims:
     T, hq, d = q.shape
     return ra_dims(T, num_seqs, hq, k.shape[1], d, _dtype_code(q), heads_k_stride,
-                   int(bool(grad_fp32)))
+                   int(bool(grad_fp32)), int(kv_exchange))
 
 
 def _need(t, name, shape=None, dtype=None):
@@ -165,7 +167,7 @@ def _check_qkv(q, k, v):
 
 
 def ringattn_fwd(q, k, v, cu_seqlens=None, num_shards=1, shard_layout=CONTIGUOUS, causal=True,
-                 out=None, lse=None, stream=None, heads_k_stride=1):
+                 out=None, lse=None, stream=None, heads_k_stride=1, kv_exchange=RING):
     """Fused ring-attention forward; returns (out [T,Hq,D], lse fp32 [Hq,T])."""
     import torch
     _check_qkv(q, k, v)
@@ -177,7 +179,7 @@ def ringattn_fwd(q, k, v, cu_seqlens=None, num_shards=1, shard_layout=CONTIGUOUS
     _need(out, "out", q.shape, q.dtype)
     _need(lse, "lse", (hq, T), torch.float32)
     cu_p, nseq, _keep = _cu_host(cu_seqlens)
-    dims = make_dims(q, k, nseq, heads_k_stride)
+    dims = make_dims(q, k, nseq, heads_k_stride, kv_exchange=kv_exchange)
     _check("ringattn_fwd", library().ringattn_fwd(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), cu_p, dims, int(num_shards),
         int(shard_layout), int(bool(causal)), out.data_ptr(), lse.data_ptr(), _stream(stream)))
@@ -190,7 +192,7 @@ def fwd_stepwise_workspace_size(q, k, heads_k_stride=1) -> int:
 
 def ringattn_fwd_stepwise(q, k, v, cu_seqlens=None, num_shards=1, shard_layout=CONTIGUOUS,
                           causal=True, out=None, lse=None, workspace=None, stream=None,
-                          heads_k_stride=1):
+                          heads_k_stride=1, kv_exchange=RING):
     """Ring forward as one launch per ring step plus a log-sum-exp merge."""
     import torch
     _check_qkv(q, k, v)
@@ -205,7 +207,7 @@ def ringattn_fwd_stepwise(q, k, v, cu_seqlens=None, num_shards=1, shard_layout=C
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     cu_p, nseq, _keep = _cu_host(cu_seqlens)
-    dims = make_dims(q, k, nseq, heads_k_stride)
+    dims = make_dims(q, k, nseq, heads_k_stride, kv_exchange=kv_exchange)
     _check("ringattn_fwd_stepwise", library().ringattn_fwd_stepwise(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), cu_p, dims, int(num_shards), int(shard_layout),
         int(bool(causal)), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
@@ -219,7 +221,8 @@ def bwd_workspace_size(q, k, heads_k_stride=1) -> int:
 
 def ringattn_bwd(q, k, v, out, lse, dout, cu_seqlens=None, num_shards=1,
                  shard_layout=CONTIGUOUS, causal=True, dq=None, dk=None, dv=None,
-                 workspace=None, stream=None, heads_k_stride=1, grad_fp32=False):
+                 workspace=None, stream=None, heads_k_stride=1, grad_fp32=False,
+                 kv_exchange=RING):
     """Ring-attention backward; returns (dq, dk, dv) (fp32 if grad_fp32)."""
     import torch
     _check_qkv(q, k, v)
@@ -238,7 +241,7 @@ def ringattn_bwd(q, k, v, out, lse, dout, cu_seqlens=None, num_shards=1,
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     cu_p, nseq, _keep = _cu_host(cu_seqlens)
-    dims = make_dims(q, k, nseq, heads_k_stride, grad_fp32)
+    dims = make_dims(q, k, nseq, heads_k_stride, grad_fp32, kv_exchange)
     _check("ringattn_bwd", library().ringattn_bwd(
         q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
         dout.data_ptr(), cu_p, dims, int(num_shards), int(shard_layout), int(bool(causal)),
@@ -267,9 +270,9 @@ def ringattn_get_status(stream=None) -> int:
 
 
 def _plan(fn_name, item_fields, total_tokens, hq, hkv, num_shards, shard_layout, causal,
-          cu_seqlens, heads_k_stride):
+          cu_seqlens, heads_k_stride, kv_exchange=RING):
     cu_p, nseq, _keep = _cu_host(cu_seqlens)
-    dims = ra_dims(total_tokens, nseq, hq, hkv, 64, RA_FP32, heads_k_stride, 0)
+    dims = ra_dims(total_tokens, nseq, hq, hkv, 64, RA_FP32, heads_k_stride, 0, kv_exchange)
     ni, ns = ctypes.c_int(0), ctypes.c_int(0)
     fn = getattr(library(), fn_name)
     code = fn(cu_p, dims, num_shards, shard_layout, int(bool(causal)), None, 0, None, 0,
@@ -285,17 +288,17 @@ def _plan(fn_name, item_fields, total_tokens, hq, hkv, num_shards, shard_layout,
 
 
 def plan_fwd(total_tokens, hq, hkv, num_shards, shard_layout, causal, cu_seqlens=None,
-             heads_k_stride=1):
+             heads_k_stride=1, kv_exchange=RING):
     """Host-only: the forward work list as (items [n,16], segments [m,4]) int32 arrays."""
     return _plan("ringattn_plan_fwd", PLAN_ITEM_FIELDS, total_tokens, hq, hkv, num_shards,
-                 shard_layout, causal, cu_seqlens, heads_k_stride)
+                 shard_layout, causal, cu_seqlens, heads_k_stride, kv_exchange)
 
 
 def plan_bwd(total_tokens, hq, hkv, num_shards, shard_layout, causal, cu_seqlens=None,
-             heads_k_stride=1):
+             heads_k_stride=1, kv_exchange=RING):
     """Host-only: the key-side backward work list (items [n,8], segments [m,4])."""
     return _plan("ringattn_plan_bwd", PLAN_BWD_ITEM_FIELDS, total_tokens, hq, hkv, num_shards,
-                 shard_layout, causal, cu_seqlens, heads_k_stride)
+                 shard_layout, causal, cu_seqlens, heads_k_stride, kv_exchange)
 
 
 def trace_enable(on: bool = True) -> None:

@@ -58,7 +58,7 @@ std::list<CachedPlan> g_plans;  // most recently used first
 bool same_key(const PlanInput& a, const PlanInput& b) {
   return a.T == b.T && a.hq == b.hq && a.hkv == b.hkv && a.num_shards == b.num_shards &&
          a.layout == b.layout && a.causal == b.causal && a.heads_k_stride == b.heads_k_stride &&
-         a.cu == b.cu;
+         a.exchange == b.exchange && a.cu == b.cu;
 }
 
 // Checks the current device once: it must be an sm_103 part.
@@ -122,6 +122,7 @@ PlanInput make_input(const int32_t* cu_seqlens, const ra_dims& d, int P, int lay
   in.layout = layout;
   in.causal = causal ? 1 : 0;
   in.heads_k_stride = d.heads_k_stride == 0 ? 1 : d.heads_k_stride;
+  in.exchange = d.kv_exchange;
   if (cu_seqlens && d.num_seqs >= 1) {
     in.cu.assign(cu_seqlens, cu_seqlens + d.num_seqs + 1);
   } else {
@@ -401,8 +402,10 @@ ra_status ringattn_fwd_stepwise(const void* q, const void* k, const void* v,
   float* stp_o = reinterpret_cast<float*>(w + fp32_o_bytes(dims) + lse_bytes(dims));
   float* stp_l = reinterpret_cast<float*>(w + 2 * fp32_o_bytes(dims) + lse_bytes(dims));
   const bool out_fp32 = dims.dtype == RA_FP32;
-  for (int step = 0; step < num_shards; ++step) {
-    const bool last = step == num_shards - 1;
+  // ring steps; an all-gather exchange is one step
+  const int num_steps = dims.kv_exchange == RA_ALLGATHER ? 1 : num_shards;
+  for (int step = 0; step < num_steps; ++step) {
+    const bool last = step == num_steps - 1;
     // step 0 starts the accumulator; one shard writes the result directly
     void* o_dst = step == 0 ? (last ? out : static_cast<void*>(acc_o)) : stp_o;
     float* l_dst = step == 0 ? (last ? lse : acc_l) : stp_l;
@@ -508,8 +511,10 @@ extern "C" ra_status ringattn_fwd_stepwise_noalloc(const void* q, const void* k,
   float* stp_o = reinterpret_cast<float*>(base + fp32_o_bytes(dims) + lse_bytes(dims));
   float* stp_l = reinterpret_cast<float*>(base + 2 * fp32_o_bytes(dims) + lse_bytes(dims));
   const bool out_fp32 = dims.dtype == RA_FP32;
-  for (int step = 0; step < num_shards; ++step) {
-    const bool last = step == num_shards - 1;
+  // ring steps; an all-gather exchange is one step
+  const int num_steps = dims.kv_exchange == RA_ALLGATHER ? 1 : num_shards;
+  for (int step = 0; step < num_steps; ++step) {
+    const bool last = step == num_steps - 1;
     void* o_dst = step == 0 ? (last ? out : static_cast<void*>(acc_o)) : stp_o;
     float* l_dst = step == 0 ? (last ? lse : acc_l) : stp_l;
     FwdParams p = make_params(q, k, v, o_dst, l_dst, dims, causal, cp, ds->status);

@@ -37,6 +37,7 @@ std::string plan_check(const PlanInput& in) {
   if (in.num_shards < 1 || in.num_shards > 65536) return "num_shards out of range";
   if (in.layout != 0 && in.layout != 1) return "unknown shard layout";
   if (in.heads_k_stride < 1 || in.hkv % in.heads_k_stride) return "heads_k_stride must divide hkv";
+  if (in.exchange != 0 && in.exchange != 1) return "unknown K/V exchange";
   if (in.cu.size() < 2) return "cu_seqlens needs at least two entries";
   if (in.cu.front() != 0 || in.cu.back() != in.T) return "cu_seqlens must run from 0 to T";
   for (size_t i = 1; i < in.cu.size(); ++i)
@@ -107,16 +108,24 @@ Plan build_fwd_plan(const PlanInput& in) {
               it.rank = r;
               it.pass = pass;
               int cost = 0;
-              for (int s = 0; s < P; ++s) {
-                const int src = ((r - s) % P + P) % P;
-                int kch[2][2], nk;
-                rank_chunks(in.T, P, in.layout, src, kch, &nk);
-                for (int kc = 0; kc < nk; ++kc) {
-                  const int k0 = std::max(kch[kc][0], lo);
-                  const int k1 = std::min(kch[kc][1], hi);
-                  if (k0 >= k1) continue;  // fully masked at this step: skipped
-                  plan.segs.push_back(PlanSegment{k0, k1, s, src});
-                  cost += (k1 - k0 + kTileRows - 1) / kTileRows;
+              if (in.exchange == 1) {
+                // all-gathered K/V: the visible keys in token order, one range
+                if (lo < hi) {
+                  plan.segs.push_back(PlanSegment{lo, hi, 0, -1});
+                  cost += (hi - lo + kTileRows - 1) / kTileRows;
+                }
+              } else {
+                for (int s = 0; s < P; ++s) {
+                  const int src = ((r - s) % P + P) % P;
+                  int kch[2][2], nk;
+                  rank_chunks(in.T, P, in.layout, src, kch, &nk);
+                  for (int kc = 0; kc < nk; ++kc) {
+                    const int k0 = std::max(kch[kc][0], lo);
+                    const int k1 = std::min(kch[kc][1], hi);
+                    if (k0 >= k1) continue;  // fully masked at this step: skipped
+                    plan.segs.push_back(PlanSegment{k0, k1, s, src});
+                    cost += (k1 - k0 + kTileRows - 1) / kTileRows;
+                  }
                 }
               }
               it.seg_count = static_cast<int32_t>(plan.segs.size()) - it.seg_begin;
@@ -162,16 +171,24 @@ BwdPlan build_bwd_plan(const PlanInput& in) {
             const int lo = in.causal ? k0 : docs.start(k0);
             const int hi = docs.end(k_last);
             int cost = 0;
-            for (int s = 0; s < P; ++s) {
-              const int r = (src + s) % P;
-              int qch[2][2], nq;
-              rank_chunks(in.T, P, in.layout, r, qch, &nq);
-              for (int qc = 0; qc < nq; ++qc) {
-                const int q0 = std::max(qch[qc][0], lo);
-                const int q1 = std::min(qch[qc][1], hi);
-                if (q0 >= q1) continue;  // fully masked at this step: skipped
-                plan.segs.push_back(BwdSegment{q0, q1, s, r});
-                cost += (q1 - q0 + kTileRows - 1) / kTileRows * G;
+            if (in.exchange == 1) {
+              // all-gathered: the queries that see the tile, in token order
+              if (lo < hi) {
+                plan.segs.push_back(BwdSegment{lo, hi, 0, -1});
+                cost += (hi - lo + kTileRows - 1) / kTileRows * G;
+              }
+            } else {
+              for (int s = 0; s < P; ++s) {
+                const int r = (src + s) % P;
+                int qch[2][2], nq;
+                rank_chunks(in.T, P, in.layout, r, qch, &nq);
+                for (int qc = 0; qc < nq; ++qc) {
+                  const int q0 = std::max(qch[qc][0], lo);
+                  const int q1 = std::min(qch[qc][1], hi);
+                  if (q0 >= q1) continue;  // fully masked at this step: skipped
+                  plan.segs.push_back(BwdSegment{q0, q1, s, r});
+                  cost += (q1 - q0 + kTileRows - 1) / kTileRows * G;
+                }
               }
             }
             it.seg_count = static_cast<int32_t>(plan.segs.size()) - it.seg_begin;

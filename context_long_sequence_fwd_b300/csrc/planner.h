@@ -31,7 +31,8 @@ struct PlanItem {
 };
 static_assert(sizeof(PlanItem) == 16 * 4, "PlanItem is 16 int32");
 
-// Keys [k0, k1) of rank `src`, visited at ring step `step`.
+// Keys [k0, k1) of rank `src`, visited at ring step `step` (all-gather
+// exchange: one step 0 and src -1, the keys gathered from every rank).
 struct PlanSegment {
   int32_t k0, k1, step, src;
 };
@@ -39,6 +40,7 @@ struct PlanSegment {
 struct PlanInput {
   int T = 0, hq = 0, hkv = 0;
   int num_shards = 1, layout = 0, causal = 0, heads_k_stride = 1;
+  int exchange = 0;  // 0: ring order of K/V shards; 1: all-gathered, token order
   std::vector<int32_t> cu;  // num_docs + 1 offsets (always filled: one doc if none given)
 };
 
@@ -63,7 +65,8 @@ struct BwdItem {
 };
 static_assert(sizeof(BwdItem) == 8 * 4, "BwdItem is 8 int32");
 
-// Queries [q0, q1) of rank `rank`, visited at ring step `step`.
+// Queries [q0, q1) of rank `rank`, visited at ring step `step` (all-gather
+// exchange: step 0 and rank -1, every rank's queries in token order).
 struct BwdSegment {
   int32_t q0, q1, step, rank;
 };

@@ -46,6 +46,7 @@ class Workload:
     doc_hi: int = 8192
     backward: bool = False
     heads_k_stride: int = 1
+    kv_exchange: int = 0  # 0: ring (batch_ring), 1: all-gather (varlen_llama3)
 
 
 WORKLOADS = {
@@ -58,6 +59,10 @@ WORKLOADS = {
                  True, "bf16"),
         Workload("varlen_causal_gqa_t65536_p8_contiguous", 65536, 32, 8, 128, 8,
                  CONTIGUOUS, True, "bf16", varlen=True),
+        # the same packed workload with the page's default exchange under sample
+        # packing (varlen_llama3: K/V gathered, heads_k_stride heads at a time)
+        Workload("varlen_causal_gqa_t65536_p8_contiguous_allgather", 65536, 32, 8, 128, 8,
+                 CONTIGUOUS, True, "bf16", varlen=True, heads_k_stride=2, kv_exchange=1),
         Workload("causal_gqa_fwdbwd_t65536_p8_zigzag", 65536, 32, 8, 128, 8,
                  ZIGZAG, True, "bf16", backward=True),
     ]

@@ -73,6 +73,19 @@ typedef enum {
 typedef enum { RA_BF16 = 0, RA_FP32 = 1 } ra_dtype;
 typedef enum { RA_CONTIGUOUS = 0, RA_ZIGZAG = 1 } ra_layout;
 
+/*
+ * The two ring_attn_func choices of the axolotl page ("Configuration"):
+ *   RA_RING (batch_ring): at ring step s rank r holds the K/V shard of rank
+ *     (r - s) mod P, and its partial results are merged step by step;
+ *   RA_ALLGATHER (varlen_llama3): every rank gathers the K/V of all shards,
+ *     heads_k_stride key/value heads at a time, and attends to them in token
+ *     order in one pass (the page's default with sample packing).
+ * On one GPU both read K/V where it already lies; they differ in the order
+ * the key tiles are visited, not in the result.  The stepwise forward runs
+ * RA_ALLGATHER as a single step.
+ */
+typedef enum { RA_RING = 0, RA_ALLGATHER = 1 } ra_exchange;
+
 typedef struct {
   int total_tokens;   /* T >= 0 */
   int num_seqs;       /* packed documents; ignored when cu_seqlens is NULL */
@@ -84,6 +97,7 @@ typedef struct {
   int grad_fp32;      /* backward only: 1 = dq, dk, dv are fp32 whatever dtype
                          is (bf16 cannot hold gradients of magnitude >= 4 to
                          within 1/64); 0 = they are in dtype */
+  int kv_exchange;    /* ra_exchange: how a rank reaches the other shards' K/V */
 } ra_dims;
 
 /*

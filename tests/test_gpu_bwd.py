@@ -23,13 +23,14 @@ TOL_FP32_GRAD = 1e-4
 TOL_BF16_GRAD = TOL_BF16_O
 
 
-def run_fwd_bwd(q, k, v, do, cu, P, layout, causal, hks=1, grad_fp32=False):
+def run_fwd_bwd(q, k, v, do, cu, P, layout, causal, hks=1, grad_fp32=False, exchange=ra.RING):
     qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
-    out, lse = ra.ringattn_fwd(qd, kd, vd, cu, P, layout, causal, heads_k_stride=hks)
+    out, lse = ra.ringattn_fwd(qd, kd, vd, cu, P, layout, causal, heads_k_stride=hks,
+                               kv_exchange=exchange)
     gdt = torch.float32 if grad_fp32 else qd.dtype
     dq, dk, dv = (torch.full(t.shape, float("nan"), dtype=gdt, device=DEV) for t in (qd, kd, vd))
     ra.ringattn_bwd(qd, kd, vd, out, lse, dod, cu, P, layout, causal, dq, dk, dv,
-                    heads_k_stride=hks, grad_fp32=grad_fp32)
+                    heads_k_stride=hks, grad_fp32=grad_fp32, kv_exchange=exchange)
     assert ra.ringattn_get_status() == 0
     return to_np(dq), to_np(dk), to_np(dv)
 
@@ -42,8 +43,9 @@ def bf16_output_bound(ref, tol):
     return tol + np.where(a > 0, 2.0 ** (e - 8), 0.0)
 
 
-def check_full(q, k, v, do, cu, P, layout, causal, tol, hks=1, grad_fp32=False):
-    dq, dk, dv = run_fwd_bwd(q, k, v, do, cu, P, layout, causal, hks, grad_fp32)
+def check_full(q, k, v, do, cu, P, layout, causal, tol, hks=1, grad_fp32=False,
+               exchange=ra.RING):
+    dq, dk, dv = run_fwd_bwd(q, k, v, do, cu, P, layout, causal, hks, grad_fp32, exchange)
     rq, rk, rv, _, _ = oracle.attention_bwd(q, k, v, do, causal=causal, cu_seqlens=cu)
     errs = (max_err(dq, rq), max_err(dk, rk), max_err(dv, rv))
     if grad_fp32 or q.dtype == torch.float32:
@@ -137,3 +139,12 @@ def test_bwd_unsupported_is_loud():
     with pytest.raises(ra.RingAttnError) as e:
         ra.ringattn_bwd(q, q, q, q, lse, q, None, 2, ra.CONTIGUOUS, True)
     assert e.value.code == -3
+
+
+@pytest.mark.parametrize("case", [BF16_CASES[i] for i in (2, 4, 7, 12)], ids=str)
+def test_allgather_backward(case):
+    """Backward with the gathered-K/V exchange (varlen_llama3 style)."""
+    T, hq, hkv, P, layout, causal, cu = case
+    q, k, v, do = make_qkv(T, hq, hkv, 128, "bf16", seed=22, with_dout=True)
+    check_full(q, k, v, do, cu, P, layout, causal, TOL_BF16_GRAD, grad_fp32=True,
+               exchange=ra.ALLGATHER)

@@ -21,20 +21,23 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-def run_fwd(q, k, v, cu, P, layout, causal, stepwise=False, hks=1):
+def run_fwd(q, k, v, cu, P, layout, causal, stepwise=False, hks=1, exchange=ra.RING):
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
     out = nan_like(qd)
     lse = torch.full((q.shape[1], q.shape[0]), float("nan"), device=DEV)
     if stepwise:
-        ra.ringattn_fwd_stepwise(qd, kd, vd, cu, P, layout, causal, out, lse, heads_k_stride=hks)
+        ra.ringattn_fwd_stepwise(qd, kd, vd, cu, P, layout, causal, out, lse, heads_k_stride=hks,
+                                 kv_exchange=exchange)
     else:
-        ra.ringattn_fwd(qd, kd, vd, cu, P, layout, causal, out, lse, heads_k_stride=hks)
+        ra.ringattn_fwd(qd, kd, vd, cu, P, layout, causal, out, lse, heads_k_stride=hks,
+                        kv_exchange=exchange)
     assert ra.ringattn_get_status() == 0
     return to_np(out), to_np(lse)
 
 
-def check_full(q, k, v, cu, P, layout, causal, tol_o, tol_l, stepwise=False, hks=1):
-    o, l = run_fwd(q, k, v, cu, P, layout, causal, stepwise, hks)
+def check_full(q, k, v, cu, P, layout, causal, tol_o, tol_l, stepwise=False, hks=1,
+               exchange=ra.RING):
+    o, l = run_fwd(q, k, v, cu, P, layout, causal, stepwise, hks, exchange)
     ro, rl = oracle.attention_fwd(q, k, v, causal=causal, cu_seqlens=cu)
     eo, el = max_err(o, ro), max_err(l, rl)
     assert eo <= tol_o and el <= tol_l, (eo, el)
@@ -150,7 +153,8 @@ def sampled_check(name, n_rows, seed=0):
     w = WORKLOADS[name]
     x = make_inputs(w, seed=seed)
     cu = x["cu_seqlens"]
-    o, l = run_fwd(x["q"], x["k"], x["v"], cu, w.num_shards, w.layout, w.causal)
+    o, l = run_fwd(x["q"], x["k"], x["v"], cu, w.num_shards, w.layout, w.causal,
+                   hks=w.heads_k_stride, exchange=w.kv_exchange)
     # rows at shard and zigzag-chunk boundaries, the ends, plus random rows
     C = w.total_tokens // (2 * w.num_shards)
     edges = sorted({0, 1, 127, 128, w.total_tokens - 1} |
@@ -218,3 +222,19 @@ def test_causal_gqa_t32768_full_rows_of_two_kv_groups():
     ro, rl = oracle.fwd_rows(x["q"], x["k"], x["v"], hs, is_, causal=True)
     assert max_err(o[is_, hs], ro) <= TOL_BF16_O
     assert max_err(l[hs, is_], rl) <= TOL_BF16_LSE
+
+
+@pytest.mark.parametrize("case", [BF16_CASES[i] for i in (2, 4, 7, 9, 12)], ids=str)
+@pytest.mark.parametrize("stepwise", [False, True])
+def test_allgather_exchange(case, stepwise):
+    """varlen_llama3-style exchange: gathered K/V in token order, with two
+    key/value heads per pass where the heads allow it."""
+    T, hq, hkv, P, layout, causal, cu = case
+    q, k, v = make_qkv(T, hq, hkv, 128, "bf16", seed=21)
+    hks = 2 if hkv % 2 == 0 else 1
+    check_full(q, k, v, cu, P, layout, causal, TOL_BF16_O, TOL_BF16_LSE, stepwise, hks,
+               exchange=ra.ALLGATHER)
+
+
+def test_varlen_causal_gqa_t65536_p8_contiguous_allgather():
+    sampled_check("varlen_causal_gqa_t65536_p8_contiguous_allgather", 384)

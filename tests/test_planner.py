@@ -53,20 +53,26 @@ CASES = [
 ]
 
 
-def check_plan(T, hq, hkv, P, layout, causal, cu, hks=1):
-    items, segs = ra.plan_fwd(T, hq, hkv, P, layout, causal, cu, heads_k_stride=hks)
+def check_plan(T, hq, hkv, P, layout, causal, cu, hks=1, exchange=ra.RING):
+    items, segs = ra.plan_fwd(T, hq, hkv, P, layout, causal, cu, heads_k_stride=hks,
+                              kv_exchange=exchange)
     doc = doc_index(T, cu)
     G = hq // hkv
     seen = np.zeros((hq, T), np.int64)
     for it in items:
         (q0a, q0b, qla, qlb, ha, hb, sb, sc, rank, cost, mla, mlb, mha, mhb, pas, _) = it
         my = segs[sb:sb + sc]
-        # ring order and shard ownership of every segment
-        assert np.all(np.diff(my[:, 2]) >= 0), "segments out of ring order"
+        if exchange == ra.ALLGATHER:
+            # gathered K/V: at most one range, in token order, in step 0
+            assert sc <= 1 and np.all(my[:, 2] == 0) and np.all(my[:, 3] == -1)
+        else:
+            # ring order and shard ownership of every segment
+            assert np.all(np.diff(my[:, 2]) >= 0), "segments out of ring order"
         for k0, k1, step, src in my:
-            assert src == (rank - step) % P
             assert k0 < k1
-            assert any(a <= k0 and k1 <= b for a, b in rank_chunks(T, P, layout, src))
+            if exchange == ra.RING:
+                assert src == (rank - step) % P
+                assert any(a <= k0 and k1 <= b for a, b in rank_chunks(T, P, layout, src))
         keys = np.concatenate([np.arange(k0, k1) for k0, k1, _, _ in my]) if len(my) else \
             np.zeros(0, np.int64)
         assert len(np.unique(keys)) == len(keys), "a key is visited twice"
@@ -213,3 +219,34 @@ def check_bwd_plan(T, hq, hkv, P, layout, causal, cu, hks=1):
 @pytest.mark.parametrize("case", CASES[:8], ids=[str(i) for i in range(8)])
 def test_bwd_plan_covers_exactly_the_mask(case):
     check_bwd_plan(*case)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
+def test_allgather_plan_covers_exactly_the_mask(case):
+    """The all-gather exchange (varlen_llama3) visits the same keys as the
+    ring, in token order."""
+    T, hq, hkv, P, layout, causal, cu = case
+    items, segs = check_plan(T, hq, hkv, P, layout, causal, cu, exchange=ra.ALLGATHER)
+    ring_items, _ = check_plan(T, hq, hkv, P, layout, causal, cu)
+    # the same query tiles; gathered keys are one range, so whole tiles can
+    # span shard boundaries and an item never visits more K/V tiles
+    key = lambda a: sorted(map(tuple, a[:, [0, 1, 2, 3, 4, 5]].tolist()))
+    assert key(items) == key(ring_items)
+    assert items[:, 9].sum() <= ring_items[:, 9].sum()
+
+
+def test_allgather_bwd_plan_covers_exactly_the_mask():
+    for case in CASES[:8]:
+        T, hq, hkv, P, layout, causal, cu = case
+        items, segs = ra.plan_bwd(T, hq, hkv, P, layout, causal, cu, kv_exchange=ra.ALLGATHER)
+        ring, _ = ra.plan_bwd(T, hq, hkv, P, layout, causal, cu)
+        assert items[:, 6].sum() <= ring[:, 6].sum()  # never more work than the ring
+        doc = doc_index(T, cu)
+        for k0, klen, g, src, sb, sc, cost, _ in items:
+            assert sc <= 1
+            for q0, q1, step, rank in segs[sb:sb + sc]:
+                assert step == 0 and rank == -1
+                # exactly the queries that see some key of the tile
+                want = [i for i in range(T)
+                        if any(np.isin(np.arange(k0, k0 + klen), visible_keys(i, doc, causal)))]
+                assert list(range(q0, q1)) == want
