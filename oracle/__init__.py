@@ -5,8 +5,9 @@ leg may import this package.  The product path (the CUDA library and its
 binding) never imports, links or calls it, and it imports nothing from the
 product package.
 
-The arithmetic lives in ``attention_fp64.c`` (plain C, OpenMP over rows); this
-module compiles it with gcc on first use and marshals numpy/torch arrays to it.
+The arithmetic lives in ``attention_fp64.c`` and ``ssd_fp64.c`` (plain C,
+OpenMP over rows / heads); this module compiles them with gcc on first use and
+marshals numpy/torch arrays to them.
 Every function computes the plain definition of attention over the whole,
 unsharded sequence (the ring schedule is an exact re-ordering of that sum,
 axolotl "Sequence Parallelism" page, introduction and "Implementation
@@ -23,7 +24,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "attention_fp64.c")
+_SRCS = [os.path.join(_HERE, "attention_fp64.c"), os.path.join(_HERE, "ssd_fp64.c")]
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
 _lock = threading.Lock()
@@ -38,11 +39,11 @@ def build(force: bool = False) -> str:
     """Compile the oracle with gcc -O2 -fopenmp (no fast-math: IEEE fp64)."""
     os.makedirs(_BUILD, exist_ok=True)
     stale = (not os.path.exists(_LIB_PATH)
-             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC))
+             or os.path.getmtime(_LIB_PATH) < max(os.path.getmtime(f) for f in _SRCS))
     if force or stale:
         tmp = _LIB_PATH + f".{os.getpid()}.tmp"
         subprocess.run(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared",
-                        "-std=c11", "-o", tmp, _SRC, "-lm"], check=True)
+                        "-std=c11", "-o", tmp] + _SRCS + ["-lm"], check=True)
         os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
 
@@ -67,6 +68,9 @@ def _load():
             lib.oracle_lse_merge.argtypes = [ctypes.c_int, ctypes.c_int,
                                              _dp, _dp, _dp, _dp]
             lib.oracle_lse_merge.restype = None
+            lib.oracle_ssd_scan.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _ip, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, _dp, _dp, _dp]
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -243,3 +247,29 @@ def lse_merge(o_a, lse_a, o_b, lse_b):
     _load().oracle_lse_merge(n, d, _ptr(oa2, _dp), _ptr(la2, _dp),
                              _ptr(ob2, _dp), _ptr(lb2, _dp))
     return oa2.reshape(oa.shape), la2.reshape(la.shape)
+
+
+def ssd_scan(x, dt, A, B, C, D=None, position_ids=None, h0=None):
+    """Mamba2 selective scan over the whole sequence, fp64 (ssd_fp64.c).
+
+    x [T, H, P], dt [T, H], A [H], B and C [T, G, N], D [H] or None,
+    position_ids [T] or None (a token with position 0 starts a packed sample
+    and resets the state), h0 [H, P, N] or None.  Returns (y [T, H, P],
+    final state [H, P, N]).
+    """
+    x, dt, A, B, C = _f64(x), _f64(dt), _f64(A), _f64(B), _f64(C)
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    if dt.shape != (T, H) or A.shape != (H,) or B.shape != (T, G, N) or C.shape != B.shape \
+            or H % G:
+        raise ValueError("ssd_scan shapes: x [T,H,P], dt [T,H], A [H], B, C [T,G,N]")
+    Dd = None if D is None else _f64(D)
+    pos = None if position_ids is None else _i32(position_ids)
+    h0d = None if h0 is None else _f64(h0)
+    y = np.zeros((T, H, P), np.float64)
+    hT = np.zeros((H, P, N), np.float64)
+    _check(_load().oracle_ssd_scan(
+        _ptr(x, _dp), _ptr(dt, _dp), _ptr(A, _dp), _ptr(B, _dp), _ptr(C, _dp),
+        None if Dd is None else _ptr(Dd, _dp), None if pos is None else _ptr(pos, _ip),
+        T, H, P, N, G, None if h0d is None else _ptr(h0d, _dp), _ptr(y, _dp), _ptr(hT, _dp)))
+    return y, hT
