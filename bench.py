@@ -505,6 +505,131 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------- Mamba2 selective scan (CP)
+
+SSD_METRIC = "mamba2 CP selective-scan fwd TFLOP/s (fp32 CUDA cores) at 1 B300"
+# fp32 FMA throughput: 148 SMs x 128 lanes x 2 flops x clock
+FP32_LANES_PER_SM = 128
+
+
+def ssd_flops(T, H, P, N) -> float:
+    """The scan's algorithmic flops: per token, head and state entry one
+    multiply-add into the state and one into the output."""
+    return 4.0 * T * H * P * N
+
+
+def run_ssd(args):
+    import torch
+
+    import context_long_sequence_fwd_b300 as ra
+    from context_long_sequence_fwd_b300.workloads import SSD_WORKLOADS, make_ssd_inputs
+
+    world, rank, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (B300)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = SSD_WORKLOADS[args.workload]
+    inp = make_ssd_inputs(w.total_tokens, w.heads, w.head_dim, w.state_dim, w.groups,
+                          args.seed, w.packed, w.doc_lo, w.doc_hi)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    stream = torch.cuda.current_stream(dev)
+    y = torch.empty_like(d["x"])
+    hT = torch.empty(w.heads, w.head_dim, w.state_dim, device=dev)
+    ws = torch.empty(ra.ssd_cp_workspace_size(d["x"], d["B"], w.num_shards), dtype=torch.uint8,
+                     device=dev)
+
+    def step(x=d["x"]):
+        ra.ssd_cp_fwd(x, d["dt"], d["A"], d["B"], d["C"], d["D"], d["position_ids"],
+                      w.num_shards, y, hT, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ra.trace_collect()
+    barrier(world)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ra.trace_enable(True)
+    with ClockSampler(local) as clocks:
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ra.trace_enable(False)
+    kernels = ra.trace_collect()
+    ms = max_over_ranks(t0.elapsed_time(t1) / args.steps, world)
+    status = ra.ringattn_get_status()
+    # end to end: inputs in from pinned host memory, y and the final state back
+    h_in = {k: v.pin_memory() for k, v in inp.items() if v is not None}
+    h_y = torch.empty(y.shape).pin_memory()
+    h_s = torch.empty(hT.shape).pin_memory()
+    x2 = torch.empty_like(d["x"])
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(2, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for k, v in h_in.items():
+            d[k].copy_(v, non_blocking=True)
+        step()
+        h_y.copy_(y, non_blocking=True)
+        h_s.copy_(hT, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    del x2
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        heads = max(1, min(w.heads, int(args.cpu_budget * 2)))  # about 0.5 s per head
+        t_c = time.perf_counter()
+        oracle.ssd_scan(inp["x"][:, :heads], inp["dt"][:, :heads], inp["A"][:heads],
+                        inp["B"][:, :1], inp["C"][:, :1], inp["D"][:heads],
+                        inp["position_ids"])
+        dt_c = time.perf_counter() - t_c
+        cpu = {"value": round(ssd_flops(w.total_tokens, heads, w.head_dim, w.state_dim) /
+                              dt_c / 1e12, 6),
+               "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{heads} of {w.heads} heads over all {w.total_tokens} tokens, fp64, "
+                         f"{dt_c:.1f} s"}
+    if rank != 0:
+        return
+    f = ssd_flops(w.total_tokens, w.heads, w.head_dim, w.state_dim)
+    clk = clocks.summary()
+    peak = 148 * FP32_LANES_PER_SM * 2 * 2.032e9 / 1e12
+    ktab = {k: {"launches": n, "avg_ms": round(t / n, 4)} for k, (n, t) in kernels.items()}
+    scan_ms = ktab.get("ssd_chunk_scan_kernel", {}).get("avg_ms", ms)
+    achieved = f / (scan_ms * 1e-3) / 1e12
+    h2d = sum(v.numel() * v.element_size() for v in h_in.values())
+    line = {
+        "metric": SSD_METRIC, "value": round(world * f / (ms * 1e-3) / 1e12, 3),
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; Mamba2 parameter ranges, packed samples)",
+        "config": {"workload": w.name, "total_tokens": w.total_tokens, "heads": w.heads,
+                   "head_dim": w.head_dim, "state_dim": w.state_dim, "groups": w.groups,
+                   "num_shards": w.num_shards, "packed": w.packed,
+                   "parallelism": f"replicas{world}" if world > 1 else "1gpu",
+                   "l2": "inputs larger than L2 (%.0f MB), no flush" % (h2d / 1e6)},
+        "roofline": {"bound": "alu", "kernel": "ssd_chunk_scan_kernel",
+                     "achieved": round(achieved, 3), "peak": round(peak, 1),
+                     "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_source": "148 SMs x 128 fp32 lanes x 2 flops x 2.032 GHz",
+                     "traffic": None, "flops_per_launch": f},
+        "kernels": ktab,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(world * f / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": h_y.numel() * 4 + h_s.numel() * 4,
+                "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": sum(n for n, _ in kernels.values()),
+        "clocks": clk,
+        "status": ra.STATUS.get(status, status),
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------- reference
 
 def run_reference(args):
@@ -564,7 +689,12 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     sys.path.insert(0, ROOT)
-    if args.impl == "reference":
+    from context_long_sequence_fwd_b300.workloads import SSD_WORKLOADS
+    if args.workload in SSD_WORKLOADS:
+        if args.impl == "reference":
+            raise SystemExit("the SSD workload's reference arm is its cpu_baseline entry")
+        run_ssd(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -9,7 +9,8 @@ compute function raises: there is no CPU fallback.
 Entry points (same names as the C ABI):
     ringattn_fwd, ringattn_fwd_stepwise, ringattn_bwd, attn_lse_merge,
     ringattn_get_status, plan_fwd / plan_bwd (host-only work-list
-    introspection), trace_enable / trace_collect (per-kernel device time).
+    introspection), trace_enable / trace_collect (per-kernel device time),
+    ssd_cp_fwd (context-parallel Mamba2 selective scan).
 """
 from __future__ import annotations
 
@@ -58,6 +59,12 @@ class ra_dims(ctypes.Structure):
                 ("grad_fp32", ctypes.c_int), ("kv_exchange", ctypes.c_int)]
 
 
+class ssd_dims(ctypes.Structure):
+    _fields_ = [("total_tokens", ctypes.c_int), ("heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("state_dim", ctypes.c_int),
+                ("groups", ctypes.c_int)]
+
+
 class ra_trace_entry(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_char * 40), ("launches", ctypes.c_int),
                 ("total_ms", ctypes.c_double)]
@@ -99,6 +106,11 @@ def library():
                                           ctypes.c_int, _i32p, ctypes.c_int, _i32p, ctypes.c_int,
                                           _ip, _ip]
         lib.ringattn_plan_bwd.argtypes = lib.ringattn_plan_fwd.argtypes
+        lib.ssd_cp_workspace_size.argtypes = [ssd_dims, ctypes.c_int]
+        lib.ssd_cp_workspace_size.restype = ctypes.c_size_t
+        lib.ssd_cp_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ssd_dims, ctypes.c_int,
+                                   _vp, _vp, _vp, ctypes.c_size_t, _vp]
+        lib.ssd_cp_fwd.restype = ctypes.c_int
         lib.ringattn_trace_enable.argtypes = [ctypes.c_int]
         lib.ringattn_trace_collect.argtypes = [ctypes.POINTER(ra_trace_entry), ctypes.c_int, _ip]
         for fn in ("ringattn_fwd", "ringattn_fwd_stepwise", "ringattn_bwd", "attn_lse_merge",
@@ -315,3 +327,47 @@ def trace_collect() -> dict:
     _check("ringattn_trace_collect", library().ringattn_trace_collect(buf, 64, ctypes.byref(n)))
     return {buf[i].kernel.decode(): (int(buf[i].launches), float(buf[i].total_ms))
             for i in range(n.value)}
+
+
+def _ssd_dims(x, B):
+    T, H, P = x.shape
+    return ssd_dims(T, H, P, B.shape[2], B.shape[1])
+
+
+def ssd_cp_workspace_size(x, B, num_shards) -> int:
+    return int(library().ssd_cp_workspace_size(_ssd_dims(x, B), int(num_shards)))
+
+
+def ssd_cp_fwd(x, dt, A, B, C, D=None, position_ids=None, num_shards=1, y=None,
+               final_state=None, workspace=None, stream=None, want_final_state=False):
+    """Context-parallel Mamba2 selective scan (fp32): returns (y [T,H,64],
+    final state [H,64,N] or None).  position_ids: int32 device tensor [T] or
+    None; a token at position 0 starts a packed sample."""
+    import torch
+    for t, n in ((x, "x"), (dt, "dt"), (A, "A"), (B, "B"), (C, "C")):
+        _need(t, n, dtype=torch.float32)
+    T, H, P = x.shape
+    G, N = B.shape[1], B.shape[2]
+    _need(dt, "dt", (T, H))
+    _need(A, "A", (H,))
+    _need(C, "C", B.shape)
+    if D is not None:
+        _need(D, "D", (H,), torch.float32)
+    if position_ids is not None:
+        _need(position_ids, "position_ids", (T,), torch.int32)
+    if y is None:
+        y = torch.empty_like(x)
+    _need(y, "y", x.shape, torch.float32)
+    if final_state is None and want_final_state:
+        final_state = torch.empty(H, P, N, dtype=torch.float32, device=x.device)
+    if final_state is not None:
+        _need(final_state, "final_state", (H, P, N), torch.float32)
+    need = ssd_cp_workspace_size(x, B, num_shards)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=x.device)
+    ptr = lambda t: None if t is None else t.data_ptr()
+    _check("ssd_cp_fwd", library().ssd_cp_fwd(
+        x.data_ptr(), dt.data_ptr(), A.data_ptr(), B.data_ptr(), C.data_ptr(), ptr(D),
+        ptr(position_ids), _ssd_dims(x, B), int(num_shards), y.data_ptr(), ptr(final_state),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream(stream)))
+    return y, final_state

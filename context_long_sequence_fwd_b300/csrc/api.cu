@@ -628,6 +628,61 @@ ra_status attn_lse_merge(void* o_a, float* lse_a, const void* o_b, const float* 
   return e == cudaSuccess ? RA_OK : RA_ERR_CUDA;
 }
 
+size_t ssd_cp_workspace_size(ssd_dims dims, int num_shards) {
+  if (dims.total_tokens < 0 || dims.heads < 1 || dims.state_dim < 1 || num_shards < 1) return 0;
+  const size_t states = (size_t)num_shards * dims.heads * 64 * dims.state_dim * sizeof(float);
+  const size_t carry = (size_t)num_shards * dims.heads * sizeof(float);
+  return 2 * ((states + 255) & ~size_t(255)) + ((carry + 255) & ~size_t(255));
+}
+
+ra_status ssd_cp_fwd(const float* x, const float* dt, const float* A, const float* B,
+                     const float* C, const float* D, const int32_t* position_ids, ssd_dims dims,
+                     int num_shards, float* y, float* final_state, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  if (dims.total_tokens < 0 || dims.heads < 1 || dims.groups < 1 || num_shards < 1)
+    return RA_ERR_INVALID_ARG;
+  if (dims.heads % dims.groups) return RA_ERR_INVALID_ARG;
+  if (dims.head_dim != 64 || (dims.state_dim != 64 && dims.state_dim != 128))
+    return RA_ERR_UNSUPPORTED;
+  if (dims.total_tokens % num_shards) return RA_ERR_NOT_DIVISIBLE;
+  if ((long long)dims.total_tokens * dims.heads * 64 >= (1LL << 40)) return RA_ERR_UNSUPPORTED;
+  if (dims.total_tokens == 0) return RA_OK;
+  if (!x || !dt || !A || !B || !C || !y) return RA_ERR_INVALID_ARG;
+  const size_t need = ssd_cp_workspace_size(dims, num_shards);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return RA_ERR_WORKSPACE;
+  int dev;
+  DeviceState* ds;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    ra_status st = current_device(&dev, &ds);
+    if (st != RA_OK) return st;
+  }
+  const size_t states = ((size_t)num_shards * dims.heads * 64 * dims.state_dim * sizeof(float) +
+                         255) & ~size_t(255);
+  char* w = static_cast<char*>(workspace);
+  SsdParams p{};
+  p.x = x;
+  p.dt = dt;
+  p.A = A;
+  p.B = B;
+  p.C = C;
+  p.D = D;
+  p.pos = position_ids;
+  p.y = y;
+  p.final_state = final_state;
+  p.chunk_state = reinterpret_cast<float*>(w);
+  p.incoming = reinterpret_cast<float*>(w + states);
+  p.carry = reinterpret_cast<float*>(w + 2 * states);
+  p.T = dims.total_tokens;
+  p.H = dims.heads;
+  p.G = dims.groups;
+  p.N = dims.state_dim;
+  p.R = num_shards;
+  return launch_ssd_cp(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? RA_OK
+                                                                            : RA_ERR_CUDA;
+}
+
 ra_status ringattn_get_status(void* stream) {
   int dev;
   DeviceState* ds;

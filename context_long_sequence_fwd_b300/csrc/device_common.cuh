@@ -57,6 +57,23 @@ struct BwdParams {
   int* status;
 };
 
+// Context-parallel selective scan (Mamba2 SSD), fp32.
+struct SsdParams {
+  const float* x;        // [T, H, P]
+  const float* dt;       // [T, H], > 0
+  const float* A;        // [H], < 0
+  const float* B;        // [T, G, N]
+  const float* C;        // [T, G, N]
+  const float* D;        // [H] or nullptr
+  const int32_t* pos;    // [T] position ids (0 starts a packed sample) or nullptr
+  float* y;              // [T, H, P]
+  float* final_state;    // [H, P, N] or nullptr
+  float* chunk_state;    // workspace [R, H, P, N]: each rank's final state from zero
+  float* incoming;       // workspace [R, H, P, N]: the state each rank receives
+  float* carry;          // workspace [R, H]: how much of an incoming state survives a chunk
+  int T, H, G, N, R;     // tokens, heads, groups, state size, ranks (shards)
+};
+
 // Start and end of the document holding token t (binary search over cu).
 __device__ __forceinline__ void doc_bounds(const int32_t* cu, int num_docs, int t, int* start,
                                            int* end) {

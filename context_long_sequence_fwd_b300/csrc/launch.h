@@ -37,4 +37,8 @@ cudaError_t launch_bwd_tc_bf16(const BwdParams& p, const CUtensorMap& map_q,
 // fp32 backward on CUDA cores (D = 64 or 128).
 cudaError_t launch_bwd_simt_fp32(const BwdParams& p, cudaStream_t stream);
 
+// Context-parallel selective scan (Mamba2 SSD): chunk scans, state passing
+// and the additive correction (head_dim 64, state size 64 or 128).
+cudaError_t launch_ssd_cp(const SsdParams& p, cudaStream_t stream);
+
 }  // namespace ra

@@ -118,3 +118,57 @@ def make_inputs(w: Workload, seed: int = 0, with_dout: bool | None = None):
         out["cu_seqlens"] = cu_seqlens_from_lengths(
             doc_lengths(w.total_tokens, w.doc_lo, w.doc_hi, seed + 1))
     return out
+
+
+
+# ------------------------------------------------- Mamba2 selective scan
+#
+# Hybrid models (Nemotron-H, Falcon-H1, Granite; axolotl page, "Mamba/SSM
+# Hybrid Models") put Mamba2 layers next to attention.  The synthetic inputs
+# follow a Mamba2 layer's usual parameter ranges: dt log-uniform in
+# [0.001, 0.1] (the range dt_bias is initialised for), A = -a with a uniform
+# in [1, 16] (A_log initialised as log of that range), D = 1, x, B, C standard
+# normal; packed samples have the attention workloads' length recipe and
+# positions that restart at 0 in each sample.
+
+@dataclasses.dataclass(frozen=True)
+class SsdWorkload:
+    name: str
+    total_tokens: int
+    heads: int
+    head_dim: int
+    state_dim: int
+    groups: int
+    num_shards: int
+    packed: bool = True
+    doc_lo: int = 512
+    doc_hi: int = 8192
+
+
+SSD_WORKLOADS = {
+    w.name: w for w in [
+        # d_inner 8192 (d_model 4096, expand 2) in heads of 64, state 128, 8 groups
+        SsdWorkload("mamba2_ssd_t32768_h128_n128_p8", 32768, 128, 64, 128, 8, 8),
+    ]
+}
+
+
+def position_ids_from_lengths(lengths) -> torch.Tensor:
+    return torch.cat([torch.arange(int(n), dtype=torch.int32) for n in lengths])
+
+
+def make_ssd_inputs(T, H, P, N, G, seed, packed=True, doc_lo=512, doc_hi=8192):
+    """x [T,H,P], dt [T,H], A [H], B, C [T,G,N], D [H] (fp32, CPU) and
+    position_ids [T] int32 (None when not packed)."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    x = torch.randn(T, H, P, generator=g)
+    lo, hi = torch.log(torch.tensor(1e-3)), torch.log(torch.tensor(1e-1))
+    dt = torch.exp(lo + (hi - lo) * torch.rand(T, H, generator=g))
+    A = -(1.0 + 15.0 * torch.rand(H, generator=g))
+    B = torch.randn(T, G, N, generator=g)
+    C = torch.randn(T, G, N, generator=g)
+    D = torch.ones(H)
+    pos = None
+    if packed:
+        pos = position_ids_from_lengths(doc_lengths(T, doc_lo, doc_hi, seed + 1))
+    return {"x": x, "dt": dt, "A": A, "B": B, "C": C, "D": D, "position_ids": pos}

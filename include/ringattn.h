@@ -186,6 +186,43 @@ ra_status ringattn_bwd(const void* q, const void* k, const void* v, const void* 
 ra_status attn_lse_merge(void* o_a, float* lse_a, const void* o_b, const float* lse_b, int rows,
                          int heads, int head_dim, int dtype, void* stream);
 
+/*
+ * Context-parallel selective scan of a Mamba2 layer (the SSD recurrence),
+ * fp32.  The axolotl "Sequence Parallelism" page ("Mamba/SSM Hybrid Models")
+ * runs hybrid models' SSM layers under context parallelism: each rank scans
+ * its chunk of the sequence, passes its final hidden state to the next rank,
+ * and an additive correction accounts for the state it did not start from
+ * (the recurrence is linear in its initial state, so no second forward pass
+ * is needed); packed samples reset the state where they start, found from
+ * position_ids.  Per head h of group g = h / (heads / groups) and token t:
+ *   S <- 0 when position_ids[t] == 0 (a packed sample starts);
+ *   S <- exp(dt[t,h] A[h]) S + dt[t,h] x[t,h,:] B[t,g,:]^T;
+ *   y[t,h,:] = S C[t,g,:] + D[h] x[t,h,:],
+ * starting from S = 0.  All num_shards ranks (contiguous chunks of T /
+ * num_shards tokens; T must divide, else RA_ERR_NOT_DIVISIBLE) run on this
+ * GPU: chunk scans from zero, the ring of states, then the correction.
+ *   x, y: [T, heads, 64] fp32;  dt: [T, heads];  A, D: [heads] (D may be
+ *   NULL);  B, C: [T, groups, state_dim] fp32, state_dim 64 or 128;
+ *   position_ids: DEVICE int32 [T], or NULL for one sample;
+ *   final_state: [heads, 64, state_dim] fp32 or NULL -- the state after the
+ *   last token (what a following chunk would receive).
+ * Device pointers owned by the caller; asynchronous on `stream`; needs a
+ * device workspace of ssd_cp_workspace_size(dims, num_shards) bytes (each
+ * rank's final state, the states passed along the ring, the carry factors).
+ */
+typedef struct {
+  int total_tokens; /* T >= 0 */
+  int heads;        /* H */
+  int head_dim;     /* 64 */
+  int state_dim;    /* N: 64 or 128 */
+  int groups;       /* G: divides heads (B and C are shared inside a group) */
+} ssd_dims;
+size_t ssd_cp_workspace_size(ssd_dims dims, int num_shards);
+ra_status ssd_cp_fwd(const float* x, const float* dt, const float* A, const float* B,
+                     const float* C, const float* D, const int32_t* position_ids, ssd_dims dims,
+                     int num_shards, float* y, float* final_state, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
 /* Synchronises `stream`, returns the first kernel-side error recorded since
  * the last call (RA_OK if none) and clears it. */
 ra_status ringattn_get_status(void* stream);

@@ -1,0 +1,123 @@
+"""GPU parity of the context-parallel Mamba2 selective scan against the fp64
+oracle's scan over the whole, unsharded sequence.
+
+Every case runs through the C ABI (ssd_cp_fwd): the chunks of num_shards
+virtual ranks are scanned from a zero state, the final states are passed
+along the ring and the additive correction is applied (axolotl page,
+"Mamba/SSM Hybrid Models").  Outputs are pre-filled with NaN.
+"""
+import numpy as np
+import pytest
+import torch
+
+import context_long_sequence_fwd_b300 as ra
+import oracle
+from context_long_sequence_fwd_b300.workloads import (SSD_WORKLOADS, make_ssd_inputs,
+                                                      position_ids_from_lengths)
+from tests._util import max_err, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+# fp32 arithmetic against fp64: each output sums at most a few hundred
+# decayed terms of magnitude ~1 (dt <= 0.1, |A| >= 1), so the rounding of the
+# fp32 path stays below 1e-5 relative to the outputs' scale.
+REL_TOL = 2e-5
+
+
+def run(inp, R, want_state=True):
+    t = {k: (None if v is None else v.to(DEV)) for k, v in inp.items()}
+    y = torch.full(t["x"].shape, float("nan"), device=DEV)
+    y, hT = ra.ssd_cp_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["position_ids"], R,
+                          y=y, want_final_state=want_state)
+    assert ra.ringattn_get_status() == 0
+    return to_np(y), None if hT is None else to_np(hT)
+
+
+def check(inp, R):
+    y, hT = run(inp, R)
+    ry, rh = oracle.ssd_scan(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                             inp["position_ids"])
+    scale = max(1.0, float(np.max(np.abs(ry))))
+    assert max_err(y, ry) <= REL_TOL * scale, (max_err(y, ry), scale)
+    hs = max(1.0, float(np.max(np.abs(rh))))
+    assert max_err(hT, rh) <= REL_TOL * hs, (max_err(hT, rh), hs)
+
+
+CASES = [
+    # T, H, N, G, R, packed lengths (None: one sample)
+    (256, 2, 64, 1, 1, None),
+    (256, 4, 64, 2, 2, None),
+    (1000, 4, 128, 2, 4, None),                  # chunks of 250: ragged token blocks
+    (2048, 4, 128, 4, 8, [300, 5, 1, 700, 1042]),
+    (2048, 8, 64, 2, 8, [100] * 20 + [48]),       # samples shorter than a chunk
+    (1536, 2, 128, 1, 3, [1536]),                 # positions from 0, one sample
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[str(i) for i in range(len(CASES))])
+def test_scan_matches_oracle(case):
+    T, H, N, G, R, lengths = case
+    inp = make_ssd_inputs(T, H, 64, N, G, seed=3, packed=False)
+    if lengths is not None:
+        inp["position_ids"] = position_ids_from_lengths(lengths)
+    check(inp, R)
+
+
+def test_chunk_starting_mid_sample():
+    """Positions that do not start at 0: the first sample began before this
+    sequence, and its state is taken as zero (nothing before token 0)."""
+    T = 1024
+    inp = make_ssd_inputs(T, 4, 64, 64, 2, seed=5, packed=False)
+    inp["position_ids"] = torch.cat([torch.arange(300, 600, dtype=torch.int32),
+                                     torch.arange(724, dtype=torch.int32)])
+    check(inp, 4)
+
+
+def test_without_skip_term():
+    inp = make_ssd_inputs(512, 2, 64, 64, 1, seed=6, packed=False)
+    inp["D"] = None
+    check(inp, 4)
+
+
+def test_shards_do_not_change_the_result():
+    inp = make_ssd_inputs(4096, 4, 64, 128, 2, seed=7)
+    y1, h1 = run(inp, 1)
+    for R in (2, 8, 16):
+        yR, hR = run(inp, R)
+        scale = max(1.0, float(np.max(np.abs(y1))))
+        assert max_err(yR, y1) <= REL_TOL * scale
+
+
+def test_mamba2_workload_sampled_heads():
+    """The full 32K-token, 128-head workload; the oracle scans 12 heads (of
+    all 8 groups' first and last heads) over the whole sequence."""
+    w = SSD_WORKLOADS["mamba2_ssd_t32768_h128_n128_p8"]
+    inp = make_ssd_inputs(w.total_tokens, w.heads, w.head_dim, w.state_dim, w.groups, seed=0)
+    y, hT = run(inp, w.num_shards)
+    per = w.heads // w.groups
+    heads = sorted({0, 1, per - 1, per, w.heads - per, w.heads - 1} |
+                   {g * per for g in range(w.groups)} | {w.heads - 2})
+    for h in heads:
+        g = h // per
+        sub = {"x": inp["x"][:, h:h + 1], "dt": inp["dt"][:, h:h + 1], "A": inp["A"][h:h + 1],
+               "B": inp["B"][:, g:g + 1], "C": inp["C"][:, g:g + 1], "D": inp["D"][h:h + 1]}
+        ry, rh = oracle.ssd_scan(sub["x"], sub["dt"], sub["A"], sub["B"], sub["C"], sub["D"],
+                                 inp["position_ids"])
+        scale = max(1.0, float(np.max(np.abs(ry))))
+        assert max_err(y[:, h:h + 1], ry) <= REL_TOL * scale, h
+        assert max_err(hT[h:h + 1], rh) <= REL_TOL * max(1.0, float(np.max(np.abs(rh)))), h
+    assert np.all(np.isfinite(y))
+
+
+def test_bad_arguments_are_loud():
+    x = torch.zeros(100, 2, 64, device=DEV)
+    dt = torch.zeros(100, 2, device=DEV)
+    A = torch.zeros(2, device=DEV)
+    B = torch.zeros(100, 1, 64, device=DEV)
+    with pytest.raises(ra.RingAttnError) as e:
+        ra.ssd_cp_fwd(x, dt, A, B, B, num_shards=3)
+    assert e.value.code == -2
+    B2 = torch.zeros(100, 1, 32, device=DEV)
+    with pytest.raises(ra.RingAttnError) as e:
+        ra.ssd_cp_fwd(x, dt, A, B2, B2, num_shards=2)
+    assert e.value.code == -3
