@@ -19,11 +19,12 @@
 //   3. ssd_correction_kernel  (head, rank >= 1): y_t += exp(A sum_{chunk start
 //      <= u <= t} dt_u) H_r C_t for the chunk's tokens before its first sample
 //      start.
-// Threads: 256 per CTA; the P = 64 rows of the state are spread over 4
-// threads each: thread `sub` of a row owns columns 16 j + 4 sub + e (j < N/16,
-// e < 4), so it reads B and C with 16-byte loads and the four threads of a
-// row read 64 contiguous bytes (no bank conflicts).  A row's output is a
-// 4-lane shuffle sum.  Inputs are staged in shared memory 32 tokens at a
+// Threads: 256 per CTA.  A thread owns two rows of the state (2 rp, 2 rp + 1)
+// and N / 8 of their columns: thread cs of a row pair holds columns
+// 32 j + 4 cs + e (e < 4), so each B or C value it reads from shared memory
+// feeds two rows, it reads them with 16-byte loads, and the eight threads of
+// a row pair read 128 contiguous bytes (no bank conflicts).  A row's output is
+// an 8-lane shuffle sum.  Inputs are staged in shared memory 32 tokens at a
 // time, with each token's decay exp(dt A) computed once.
 #include <cuda_runtime.h>
 
@@ -51,9 +52,9 @@ struct Stage {
   float y[kTok][kP];
 };
 
-// Column of the state a thread's i-th entry holds (see the layout above).
-__device__ __forceinline__ int ssd_col(int sub, int i) {
-  return 16 * (i >> 2) + 4 * sub + (i & 3);
+// Column of the state a thread's i-th entry (of each of its rows) holds.
+__device__ __forceinline__ int ssd_col(int cs, int i) {
+  return 32 * (i >> 2) + 4 * cs + (i & 3);
 }
 
 // Loads tokens [t0, t0 + n) of head h (group g) into shared memory.
@@ -83,17 +84,17 @@ template <int N>
 __global__ void __launch_bounds__(kThreads) ssd_chunk_scan_kernel(const SsdParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Stage<N>& st = *reinterpret_cast<Stage<N>*>(smem_raw);
-  constexpr int kCols = N / 4;
+  constexpr int kCols = N / 8;  // columns per thread, for each of its two rows
   const int h = blockIdx.x, r = blockIdx.y;
   const int g = h / (p.H / p.G);
-  const int row = threadIdx.x >> 2, sub = threadIdx.x & 3;
+  const int rp = threadIdx.x >> 3, cs = threadIdx.x & 7;
   const int L = p.T / p.R;
   const int c0 = r * L;
   const float A = p.A[h];
   const float Dh = p.D ? p.D[h] : 0.f;
-  float S[kCols];
+  float S0[kCols], S1[kCols];  // rows 2 rp and 2 rp + 1
 #pragma unroll
-  for (int i = 0; i < kCols; ++i) S[i] = 0.f;
+  for (int i = 0; i < kCols; ++i) S0[i] = S1[i] = 0.f;
   float logcarry = 0.f;  // A * sum dt over the chunk
   bool reset = false;    // a sample starts inside the chunk
   for (int t0 = c0; t0 < c0 + L; t0 += kTok) {
@@ -104,31 +105,40 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_scan_kernel(const SsdParam
     for (int k = 0; k < n; ++k) {
       if (st.pos[k] == 0) {
 #pragma unroll
-        for (int i = 0; i < kCols; ++i) S[i] = 0.f;
+        for (int i = 0; i < kCols; ++i) S0[i] = S1[i] = 0.f;
         reset = true;
         logcarry = 0.f;
       }
       const float d = st.dt[k];
       const float a = st.decay[k];
       logcarry += d * A;
-      const float dx = d * st.x[k][row];
-      float acc4[4] = {0.f, 0.f, 0.f, 0.f};  // four chains: the sum is not one long dependency
+      const float2 x2 = *reinterpret_cast<const float2*>(&st.x[k][2 * rp]);
+      const float dx0 = d * x2.x, dx1 = d * x2.y;
+      float acc0[2] = {0.f, 0.f}, acc1[2] = {0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < kCols / 4; ++j) {
-        const float4 b4 = *reinterpret_cast<const float4*>(&st.B[k][ssd_col(sub, 4 * j)]);
-        const float4 c4 = *reinterpret_cast<const float4*>(&st.C[k][ssd_col(sub, 4 * j)]);
+        const float4 b4 = *reinterpret_cast<const float4*>(&st.B[k][ssd_col(cs, 4 * j)]);
+        const float4 c4 = *reinterpret_cast<const float4*>(&st.C[k][ssd_col(cs, 4 * j)]);
         const float bb[4] = {b4.x, b4.y, b4.z, b4.w}, cc[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          float& s_ = S[4 * j + e];
-          s_ = fmaf(a, s_, dx * bb[e]);
-          acc4[e] = fmaf(s_, cc[e], acc4[e]);
+          float& u0 = S0[4 * j + e];
+          float& u1 = S1[4 * j + e];
+          u0 = fmaf(a, u0, dx0 * bb[e]);
+          u1 = fmaf(a, u1, dx1 * bb[e]);
+          acc0[e & 1] = fmaf(u0, cc[e], acc0[e & 1]);
+          acc1[e & 1] = fmaf(u1, cc[e], acc1[e & 1]);
         }
       }
-      float acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      if (sub == 0) st.y[k][row] = fmaf(Dh, st.x[k][row], acc);
+      float y0 = acc0[0] + acc0[1], y1 = acc1[0] + acc1[1];
+#pragma unroll
+      for (int m = 1; m < 8; m <<= 1) {
+        y0 += __shfl_xor_sync(0xffffffffu, y0, m);
+        y1 += __shfl_xor_sync(0xffffffffu, y1, m);
+      }
+      if (cs == 0)
+        *reinterpret_cast<float2*>(&st.y[k][2 * rp]) =
+            make_float2(fmaf(Dh, x2.x, y0), fmaf(Dh, x2.y, y1));
     }
     __syncthreads();
     for (int i = threadIdx.x; i < n * kP; i += kThreads) {
@@ -137,9 +147,12 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_scan_kernel(const SsdParam
     }
   }
   // the chunk's final state and the factor an incoming state survives with
-  float* Sout = p.chunk_state + (((size_t)r * p.H + h) * kP + row) * N;
+  float* Sout = p.chunk_state + (((size_t)r * p.H + h) * kP + 2 * rp) * N;
 #pragma unroll
-  for (int i = 0; i < kCols; ++i) Sout[ssd_col(sub, i)] = S[i];
+  for (int i = 0; i < kCols; ++i) {
+    Sout[ssd_col(cs, i)] = S0[i];
+    Sout[N + ssd_col(cs, i)] = S1[i];
+  }
   if (threadIdx.x == 0) p.carry[(size_t)r * p.H + h] = reset ? 0.f : expf(logcarry);
 }
 
@@ -166,17 +179,20 @@ template <int N>
 __global__ void __launch_bounds__(kThreads) ssd_correction_kernel(const SsdParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Stage<N>& st = *reinterpret_cast<Stage<N>*>(smem_raw);
-  constexpr int kCols = N / 4;
+  constexpr int kCols = N / 8;
   const int h = blockIdx.x, r = blockIdx.y + 1;
   const int g = h / (p.H / p.G);
-  const int row = threadIdx.x >> 2, sub = threadIdx.x & 3;
+  const int rp = threadIdx.x >> 3, cs = threadIdx.x & 7;
   const int L = p.T / p.R;
   const int c0 = r * L;
   const float A = p.A[h];
-  float Hin[kCols];
-  const float* src = p.incoming + (((size_t)r * p.H + h) * kP + row) * N;
+  float H0[kCols], H1[kCols];  // rows 2 rp, 2 rp + 1 of the state rank r receives
+  const float* src = p.incoming + (((size_t)r * p.H + h) * kP + 2 * rp) * N;
 #pragma unroll
-  for (int i = 0; i < kCols; ++i) Hin[i] = src[ssd_col(sub, i)];
+  for (int i = 0; i < kCols; ++i) {
+    H0[i] = src[ssd_col(cs, i)];
+    H1[i] = src[N + ssd_col(cs, i)];
+  }
   float lam = 0.f;  // A * sum dt from the chunk start
   bool done = false;
   for (int t0 = c0; t0 < c0 + L && !done; t0 += kTok) {
@@ -193,19 +209,24 @@ __global__ void __launch_bounds__(kThreads) ssd_correction_kernel(const SsdParam
       }
       lam = fmaf(st.dt[k], A, lam);
       const float decay = expf(lam);
-      float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc0[2] = {0.f, 0.f}, acc1[2] = {0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < kCols / 4; ++j) {
-        const float4 c4 = *reinterpret_cast<const float4*>(&st.C[k][ssd_col(sub, 4 * j)]);
-        acc4[0] = fmaf(Hin[4 * j], c4.x, acc4[0]);
-        acc4[1] = fmaf(Hin[4 * j + 1], c4.y, acc4[1]);
-        acc4[2] = fmaf(Hin[4 * j + 2], c4.z, acc4[2]);
-        acc4[3] = fmaf(Hin[4 * j + 3], c4.w, acc4[3]);
+        const float4 c4 = *reinterpret_cast<const float4*>(&st.C[k][ssd_col(cs, 4 * j)]);
+        const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc0[e & 1] = fmaf(H0[4 * j + e], cc[e], acc0[e & 1]);
+          acc1[e & 1] = fmaf(H1[4 * j + e], cc[e], acc1[e & 1]);
+        }
       }
-      float acc = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      if (sub == 0) st.y[k][row] = decay * acc;
+      float y0 = acc0[0] + acc0[1], y1 = acc1[0] + acc1[1];
+#pragma unroll
+      for (int mm = 1; mm < 8; mm <<= 1) {
+        y0 += __shfl_xor_sync(0xffffffffu, y0, mm);
+        y1 += __shfl_xor_sync(0xffffffffu, y1, mm);
+      }
+      if (cs == 0) *reinterpret_cast<float2*>(&st.y[k][2 * rp]) = make_float2(decay * y0, decay * y1);
     }
     __syncthreads();
     for (int i = threadIdx.x; i < m * kP; i += kThreads) {
