@@ -31,6 +31,7 @@
 #include <cmath>
 
 #include "launch.h"
+#include "sm103_ptx.cuh"
 #include "trace.h"
 
 namespace ra {
@@ -92,9 +93,11 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_scan_kernel(const SsdParam
   const int c0 = r * L;
   const float A = p.A[h];
   const float Dh = p.D ? p.D[h] : 0.f;
-  float S0[kCols], S1[kCols];  // rows 2 rp and 2 rp + 1
+  // rows 2 rp and 2 rp + 1, two adjacent columns per 64-bit register pair:
+  // the update and the read-out run on paired fp32 instructions
+  uint64_t S0[kCols / 2], S1[kCols / 2];
 #pragma unroll
-  for (int i = 0; i < kCols; ++i) S0[i] = S1[i] = 0.f;
+  for (int i = 0; i < kCols / 2; ++i) S0[i] = S1[i] = f32x2(0.f, 0.f);
   float logcarry = 0.f;  // A * sum dt over the chunk
   bool reset = false;    // a sample starts inside the chunk
   for (int t0 = c0; t0 < c0 + L; t0 += kTok) {
@@ -105,7 +108,7 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_scan_kernel(const SsdParam
     for (int k = 0; k < n; ++k) {
       if (st.pos[k] == 0) {
 #pragma unroll
-        for (int i = 0; i < kCols; ++i) S0[i] = S1[i] = 0.f;
+        for (int i = 0; i < kCols / 2; ++i) S0[i] = S1[i] = f32x2(0.f, 0.f);
         reset = true;
         logcarry = 0.f;
       }
@@ -113,24 +116,28 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_scan_kernel(const SsdParam
       const float a = st.decay[k];
       logcarry += d * A;
       const float2 x2 = *reinterpret_cast<const float2*>(&st.x[k][2 * rp]);
-      const float dx0 = d * x2.x, dx1 = d * x2.y;
-      float acc0[2] = {0.f, 0.f}, acc1[2] = {0.f, 0.f};
+      const uint64_t aa = f32x2(a, a);
+      const uint64_t dx0 = f32x2(d * x2.x, d * x2.x), dx1 = f32x2(d * x2.y, d * x2.y);
+      uint64_t acc0 = f32x2(0.f, 0.f), acc1 = f32x2(0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < kCols / 4; ++j) {
         const float4 b4 = *reinterpret_cast<const float4*>(&st.B[k][ssd_col(cs, 4 * j)]);
         const float4 c4 = *reinterpret_cast<const float4*>(&st.C[k][ssd_col(cs, 4 * j)]);
-        const float bb[4] = {b4.x, b4.y, b4.z, b4.w}, cc[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float& u0 = S0[4 * j + e];
-          float& u1 = S1[4 * j + e];
-          u0 = fmaf(a, u0, dx0 * bb[e]);
-          u1 = fmaf(a, u1, dx1 * bb[e]);
-          acc0[e & 1] = fmaf(u0, cc[e], acc0[e & 1]);
-          acc1[e & 1] = fmaf(u1, cc[e], acc1[e & 1]);
-        }
+        const uint64_t b01 = f32x2(b4.x, b4.y), b23 = f32x2(b4.z, b4.w);
+        const uint64_t c01 = f32x2(c4.x, c4.y), c23 = f32x2(c4.z, c4.w);
+        S0[2 * j] = ffma2(aa, S0[2 * j], fmul2(dx0, b01));
+        S0[2 * j + 1] = ffma2(aa, S0[2 * j + 1], fmul2(dx0, b23));
+        S1[2 * j] = ffma2(aa, S1[2 * j], fmul2(dx1, b01));
+        S1[2 * j + 1] = ffma2(aa, S1[2 * j + 1], fmul2(dx1, b23));
+        acc0 = ffma2(S0[2 * j], c01, acc0);
+        acc0 = ffma2(S0[2 * j + 1], c23, acc0);
+        acc1 = ffma2(S1[2 * j], c01, acc1);
+        acc1 = ffma2(S1[2 * j + 1], c23, acc1);
       }
-      float y0 = acc0[0] + acc0[1], y1 = acc1[0] + acc1[1];
+      float p0, p1, q0, q1;
+      f32x2_split(acc0, &p0, &p1);
+      f32x2_split(acc1, &q0, &q1);
+      float y0 = p0 + p1, y1 = q0 + q1;
 #pragma unroll
       for (int m = 1; m < 8; m <<= 1) {
         y0 += __shfl_xor_sync(0xffffffffu, y0, m);
@@ -149,9 +156,12 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_scan_kernel(const SsdParam
   // the chunk's final state and the factor an incoming state survives with
   float* Sout = p.chunk_state + (((size_t)r * p.H + h) * kP + 2 * rp) * N;
 #pragma unroll
-  for (int i = 0; i < kCols; ++i) {
-    Sout[ssd_col(cs, i)] = S0[i];
-    Sout[N + ssd_col(cs, i)] = S1[i];
+  for (int i = 0; i < kCols / 2; ++i) {  // pair i holds columns ssd_col(cs, 2 i), + 1
+    float lo, hi;
+    f32x2_split(S0[i], &lo, &hi);
+    *reinterpret_cast<float2*>(&Sout[ssd_col(cs, 2 * i)]) = make_float2(lo, hi);
+    f32x2_split(S1[i], &lo, &hi);
+    *reinterpret_cast<float2*>(&Sout[N + ssd_col(cs, 2 * i)]) = make_float2(lo, hi);
   }
   if (threadIdx.x == 0) p.carry[(size_t)r * p.H + h] = reset ? 0.f : expf(logcarry);
 }
@@ -186,12 +196,15 @@ __global__ void __launch_bounds__(kThreads) ssd_correction_kernel(const SsdParam
   const int L = p.T / p.R;
   const int c0 = r * L;
   const float A = p.A[h];
-  float H0[kCols], H1[kCols];  // rows 2 rp, 2 rp + 1 of the state rank r receives
+  // rows 2 rp, 2 rp + 1 of the state rank r receives, in column pairs
+  uint64_t H0[kCols / 2], H1[kCols / 2];
   const float* src = p.incoming + (((size_t)r * p.H + h) * kP + 2 * rp) * N;
 #pragma unroll
-  for (int i = 0; i < kCols; ++i) {
-    H0[i] = src[ssd_col(cs, i)];
-    H1[i] = src[N + ssd_col(cs, i)];
+  for (int i = 0; i < kCols / 2; ++i) {
+    const float2 u = *reinterpret_cast<const float2*>(&src[ssd_col(cs, 2 * i)]);
+    const float2 w = *reinterpret_cast<const float2*>(&src[N + ssd_col(cs, 2 * i)]);
+    H0[i] = f32x2(u.x, u.y);
+    H1[i] = f32x2(w.x, w.y);
   }
   float lam = 0.f;  // A * sum dt from the chunk start
   bool done = false;
@@ -209,18 +222,20 @@ __global__ void __launch_bounds__(kThreads) ssd_correction_kernel(const SsdParam
       }
       lam = fmaf(st.dt[k], A, lam);
       const float decay = expf(lam);
-      float acc0[2] = {0.f, 0.f}, acc1[2] = {0.f, 0.f};
+      uint64_t acc0 = f32x2(0.f, 0.f), acc1 = f32x2(0.f, 0.f);
 #pragma unroll
       for (int j = 0; j < kCols / 4; ++j) {
         const float4 c4 = *reinterpret_cast<const float4*>(&st.C[k][ssd_col(cs, 4 * j)]);
-        const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc0[e & 1] = fmaf(H0[4 * j + e], cc[e], acc0[e & 1]);
-          acc1[e & 1] = fmaf(H1[4 * j + e], cc[e], acc1[e & 1]);
-        }
+        const uint64_t c01 = f32x2(c4.x, c4.y), c23 = f32x2(c4.z, c4.w);
+        acc0 = ffma2(H0[2 * j], c01, acc0);
+        acc0 = ffma2(H0[2 * j + 1], c23, acc0);
+        acc1 = ffma2(H1[2 * j], c01, acc1);
+        acc1 = ffma2(H1[2 * j + 1], c23, acc1);
       }
-      float y0 = acc0[0] + acc0[1], y1 = acc1[0] + acc1[1];
+      float p0, p1, q0, q1;
+      f32x2_split(acc0, &p0, &p1);
+      f32x2_split(acc1, &q0, &q1);
+      float y0 = p0 + p1, y1 = q0 + q1;
 #pragma unroll
       for (int mm = 1; mm < 8; mm <<= 1) {
         y0 += __shfl_xor_sync(0xffffffffu, y0, mm);

@@ -238,3 +238,17 @@ def test_allgather_exchange(case, stepwise):
 
 def test_varlen_causal_gqa_t65536_p8_contiguous_allgather():
     sampled_check("varlen_causal_gqa_t65536_p8_contiguous_allgather", 384)
+
+
+def test_ulysses_head_partition_equals_ring():
+    """DeepSpeed-Ulysses shards heads instead of tokens: each of P ranks
+    attends over the whole sequence for Hkv / P key/value heads (and their
+    query heads).  On one GPU that is the all-gather exchange with
+    heads_k_stride = Hkv / P (one pass per rank's head group); it must equal
+    the ring's result."""
+    T, hq, hkv, P = 2048, 8, 4, 2
+    q, k, v = make_qkv(T, hq, hkv, 128, "bf16", seed=31)
+    ring_o, ring_l = run_fwd(q, k, v, None, P, ra.CONTIGUOUS, True)
+    uly_o, uly_l = run_fwd(q, k, v, None, P, ra.CONTIGUOUS, True, hks=hkv // P,
+                           exchange=ra.ALLGATHER)
+    assert max_err(uly_o, ring_o) <= 2e-2 and max_err(uly_l, ring_l) <= 1e-4
