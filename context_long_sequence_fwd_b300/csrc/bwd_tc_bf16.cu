@@ -763,21 +763,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-bool g_configured = false;
+bool g_dkdv_configured[64] = {};
+bool g_dq_configured[64] = {};
 
 }  // namespace
 
 cudaError_t launch_bwd_tc_bf16(const BwdParams& p, const CUtensorMap& map_q,
                                const CUtensorMap& map_k, const CUtensorMap& map_v,
                                const CUtensorMap& map_do, cudaStream_t stream) {
-  if (!g_configured) {
-    cudaError_t e = cudaFuncSetAttribute(bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemKV);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemQ);
-    if (e != cudaSuccess) return e;
-    g_configured = true;
-  }
+  cudaError_t e0 = ensure_smem_limit(bwd_dkdv_kernel, kSmemKV, g_dkdv_configured);
+  if (e0 == cudaSuccess) e0 = ensure_smem_limit(bwd_dq_kernel, kSmemQ, g_dq_configured);
+  if (e0 != cudaSuccess) return e0;
   if (p.num_items > 0) {
     TraceScope trace_scope(stream, "bwd_dq_kernel");
     bwd_dq_kernel<<<2 * p.num_items, kThreads, kSmemQ, stream>>>(map_q, map_k, map_v, map_do, p);

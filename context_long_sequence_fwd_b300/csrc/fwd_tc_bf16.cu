@@ -497,13 +497,9 @@ cudaError_t launch_fwd_tc_bf16(const FwdParams& p, const CUtensorMap& map_q,
                                const CUtensorMap& map_k, const CUtensorMap& map_v,
                                cudaStream_t stream) {
   if (p.num_items == 0) return cudaSuccess;
-  static bool configured = false;  // per process; the attribute is per function
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_tc_bf16_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static bool configured[64] = {};
+  cudaError_t e = ensure_smem_limit(fwd_tc_bf16_kernel, kSmemBytes, configured);
+  if (e != cudaSuccess) return e;
   // persistent: one CTA per SM (shared memory and TMEM allow no more), each
   // claiming items from the work counter; without one, one item per CTA
   const int grid = p.work_counter ? p.num_ctas : p.num_items;

@@ -7,6 +7,20 @@
 
 namespace ra {
 
+// Raises a kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device (`done` is the kernel's own per-device record).
+template <typename Kernel>
+cudaError_t ensure_smem_limit(Kernel kernel, int bytes, bool (&done)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[dev] = true;
+  return e;
+}
+
 // fp32 forward on CUDA cores (D = 64 or 128).
 cudaError_t launch_fwd_simt_fp32(const FwdParams& p, cudaStream_t stream);
 

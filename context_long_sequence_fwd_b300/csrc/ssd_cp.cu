@@ -254,16 +254,10 @@ __global__ void __launch_bounds__(kThreads) ssd_correction_kernel(const SsdParam
 template <int N>
 cudaError_t launch_n(const SsdParams& p, cudaStream_t stream) {
   const size_t smem = sizeof(Stage<N>);
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(ssd_chunk_scan_kernel<N>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(ssd_correction_kernel<N>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static bool scan_configured[64] = {}, corr_configured[64] = {};
+  cudaError_t e0 = ensure_smem_limit(ssd_chunk_scan_kernel<N>, (int)smem, scan_configured);
+  if (e0 == cudaSuccess) e0 = ensure_smem_limit(ssd_correction_kernel<N>, (int)smem, corr_configured);
+  if (e0 != cudaSuccess) return e0;
   {
     TraceScope trace_scope(stream, "ssd_chunk_scan_kernel");
     ssd_chunk_scan_kernel<N><<<dim3(p.H, p.R), kThreads, smem, stream>>>(p);
