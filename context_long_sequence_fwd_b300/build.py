@@ -1,6 +1,6 @@
 """Builds libringattn.so in-tree with nvcc for sm_103a (B300).
 
-    python -m context_long_sequence_fwd_b300.build [--force] [--debug]
+    python -m context_long_sequence_fwd_b300.build [--force] [-v]
 
 Objects go to ``_build/`` next to this file; the shared library is written
 to ``context_long_sequence_fwd_b300/libringattn.so`` (the binding loads it
@@ -49,10 +49,10 @@ def _mtime(p: str) -> float:
     return os.path.getmtime(p) if os.path.exists(p) else -1.0
 
 
-def build(force: bool = False, debug: bool = False, verbose: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
     newest_header = max((_mtime(h) for h in headers()), default=0.0)
-    flags = list(COMMON) + (["-DRINGATTN_DEBUG=1"] if debug else [])
+    flags = list(COMMON)
     jobs = []
     for src in sources():
         obj = os.path.join(BUILD, os.path.basename(src) + ".o")
@@ -88,7 +88,6 @@ def build(force: bool = False, debug: bool = False, verbose: bool = False) -> st
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
-    ap.add_argument("--debug", action="store_true")
     ap.add_argument("-v", "--verbose", action="store_true")
     a = ap.parse_args()
-    print(build(force=a.force, debug=a.debug, verbose=a.verbose))
+    print(build(force=a.force, verbose=a.verbose))
