@@ -47,8 +47,9 @@
  *   - Errors raised inside kernels (a bounded wait that timed out) are
  *     recorded in a device status word that ringattn_get_status() reads.
  *   - The library allocates no device memory per call.  It caches work lists
- *     (one small device buffer per distinct problem) and one status word per
- *     device, and releases them at unload.
+ *     (one small device buffer per distinct problem, up to 32 problems) and
+ *     keeps one status word and 64 work counters of the persistent forward
+ *     per device in static device arrays.
  */
 #ifndef RINGATTN_H
 #define RINGATTN_H
