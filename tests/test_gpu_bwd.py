@@ -89,6 +89,8 @@ BF16_CASES = [
     (2048, 4, 2, 16, ra.ZIGZAG, True, None),             # 32 chunks of 64: half tiles
     (1024, 1, 1, 4, ra.ZIGZAG, True, None),              # a single head
     (2048, 4, 2, 4, ra.CONTIGUOUS, True, MANY_DOCS),     # 44 documents shorter than a tile
+    (16, 2, 1, 2, ra.ZIGZAG, True, None),                # 4 chunks of 4 tokens
+    (2, 1, 1, 1, ra.CONTIGUOUS, True, None),             # two tokens
 ]
 
 
