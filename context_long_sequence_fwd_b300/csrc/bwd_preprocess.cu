@@ -3,9 +3,10 @@
 // D_i equals sum_j P_ij dP_ij (the row sums of P o dP), which the backward
 // needs in dS_ij = P_ij (dP_ij - D_i); computing it from O and dO costs one
 // read of each instead of a pass over the keys.  Memory-bound: a group of
-// D/8 threads reads one row of O and of dO with 16-byte (bf16) or 2 x 16-byte
-// (fp32) loads and reduces with shuffles; rows are numbered head-major so the
-// D stores of a warp are contiguous.
+// D/32 threads reads one row of O and of dO, four 16-byte (bf16) or 2 x
+// 16-byte (fp32) loads of each per thread, and reduces with shuffles; (row, head) pairs are numbered in
+// memory order of O, so the grid streams O and dO front to back (the 4-byte
+// D stores, strided by T, are merged into full sectors in L2).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -43,20 +44,27 @@ __device__ __forceinline__ float dot8(const void* a, const void* b, size_t idx) 
   return s;
 }
 
+// Four chunks of 8 values per thread, all loads issued before the sums.
+constexpr int kChunks = 4;
+
 template <bool kF32>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const void* out, const void* dout,
                                                              float* Dvec, int T, int hq, int D,
                                                              long long rows) {
-  const int tpr = D / 8;  // threads per row; divides 32
+  const int tpr = D / (8 * kChunks);  // threads per row; divides 32
   const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long r = gt / tpr;
   const int part = (int)(gt % tpr);
   float s = 0.f;
   int h = 0, i = 0;
   if (r < rows) {
-    h = (int)(r / T);
-    i = (int)(r % T);
-    s = dot8<kF32>(out, dout, ((size_t)i * hq + h) * D + (size_t)part * 8);
+    i = (int)(r / hq);
+    h = (int)(r % hq);
+    const size_t idx = ((size_t)i * hq + h) * D + (size_t)part * 8 * kChunks;
+    float t[kChunks];
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) t[c] = dot8<kF32>(out, dout, idx + 8 * c);
+    s = (t[0] + t[1]) + (t[2] + t[3]);
   }
   for (int off = tpr / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
   if (r < rows && part == 0) Dvec[(size_t)h * T + i] = s;
@@ -68,7 +76,7 @@ cudaError_t launch_bwd_preprocess(const void* out, const void* dout, bool fp32, 
                                   int hq, int D, cudaStream_t stream) {
   const long long rows = (long long)T * hq;
   if (rows == 0) return cudaSuccess;
-  const long long threads = rows * (D / 8);
+  const long long threads = rows * (D / (8 * kChunks));
   const long long grid = (threads + 255) / 256;
   TraceScope trace_scope(stream, "bwd_preprocess_kernel");
   if (fp32)

@@ -8,10 +8,12 @@
 // a side with lse = -inf (no visible key) contributes nothing, and two empty
 // sides give o = 0, lse = -inf.
 //
-// Memory-bound: each (row, head) pair is D contiguous values; a group of D/8
-// threads moves them with 16-byte (bf16) or 2 x 16-byte (fp32) accesses.
-// Pairs are numbered head-major so that the lse reads/writes of a warp are
-// contiguous.
+// Memory-bound: each (row, head) pair is D contiguous values, moved in chunks
+// of 8 with 16-byte (bf16) or 2 x 16-byte (fp32) accesses.
+// Pairs are numbered in memory order of o (row-major), so the grid streams
+// o_a, o_b and the output front to back; the 4-byte lse accesses, strided by
+// rows, are merged into full sectors in L2 (the lse arrays are 1/64 of the
+// bytes at D = 128 in bf16).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -63,50 +65,63 @@ __device__ __forceinline__ void store8(void* base, bool fp32, size_t idx, const 
   }
 }
 
+// kC chunks of 8 values per thread (kC = min(4, D / 8)): every load of the
+// thread (both lse values and 2 kC chunks of o) is issued before any is
+// used, so each thread keeps up to 8 16-byte reads in flight.
+template <int kC>
 __global__ void __launch_bounds__(256) lse_merge_kernel(const void* o_a, bool a_fp32,
                                                         const float* lse_a, const void* o_b,
                                                         bool b_fp32, const float* lse_b,
                                                         void* o_out, bool out_fp32,
                                                         float* lse_out, int rows, int heads,
                                                         int D, long long pairs) {
-  const int tpp = D / 8;  // threads per (row, head) pair; divides 32
+  const int tpp = D / (8 * kC);  // threads per (row, head) pair; divides 32
   const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long pair = gt / tpp;
   const int part = (int)(gt % tpp);
   const bool active = pair < pairs;
   float a = -INFINITY, b = -INFINITY;
   int h = 0, row = 0;
+  Vec8 x[kC], y[kC];
+  size_t idx = 0;
   if (active) {
-    h = (int)(pair / rows);
-    row = (int)(pair % rows);
+    row = (int)(pair / heads);
+    h = (int)(pair % heads);
     a = lse_a[(size_t)h * rows + row];
     b = lse_b[(size_t)h * rows + row];
+    idx = ((size_t)row * heads + h) * D + (size_t)part * 8 * kC;
+    // a side with lse = -inf is read too (its values are then not used)
+#pragma unroll
+    for (int c = 0; c < kC; ++c) {
+      x[c] = load8(o_a, a_fp32, idx + 8 * c);
+      y[c] = load8(o_b, b_fp32, idx + 8 * c);
+    }
   }
   // every lane of the pair has read lse_a before any lane overwrites it
   __syncwarp();
   if (!active) return;
-  const size_t idx = ((size_t)row * heads + h) * D + (size_t)part * 8;
-  Vec8 r;
-  float L;
-  if (a == -INFINITY && b == -INFINITY) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) r.x[i] = 0.f;
-    L = -INFINITY;
-  } else if (b == -INFINITY) {
-    r = load8(o_a, a_fp32, idx);
-    L = a;
-  } else if (a == -INFINITY) {
-    r = load8(o_b, b_fp32, idx);
-    L = b;
-  } else {
+  const bool ea = a == -INFINITY, eb = b == -INFINITY;
+  float L = -INFINITY, wa = 0.f, wb = 0.f;
+  if (!ea && !eb) {
     const float mx = fmaxf(a, b);
     L = mx + log1pf(expf(-fabsf(a - b)));
-    const float wa = expf(a - L), wb = expf(b - L);
-    const Vec8 x = load8(o_a, a_fp32, idx), y = load8(o_b, b_fp32, idx);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) r.x[i] = fmaf(wa, x.x[i], wb * y.x[i]);
+    wa = expf(a - L);
+    wb = expf(b - L);
+  } else if (!ea) {
+    L = a;
+  } else if (!eb) {
+    L = b;
   }
-  store8(o_out, out_fp32, idx, r);
+#pragma unroll
+  for (int c = 0; c < kC; ++c) {
+    Vec8 r;
+    // an empty side contributes exactly nothing, whatever its o holds
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      r.x[i] = ea ? (eb ? 0.f : y[c].x[i])
+                  : (eb ? x[c].x[i] : fmaf(wa, x[c].x[i], wb * y[c].x[i]));
+    store8(o_out, out_fp32, idx + 8 * c, r);
+  }
   if (part == 0) lse_out[(size_t)h * rows + row] = L;
 }
 
@@ -117,13 +132,20 @@ cudaError_t launch_lse_merge(const void* o_a, bool a_fp32, const float* lse_a, c
                              float* lse_out, int rows, int heads, int D, cudaStream_t stream) {
   const long long pairs = (long long)rows * heads;
   if (pairs == 0) return cudaSuccess;
-  const long long threads = pairs * (D / 8);
+  const int chunks = D / 8 < 4 ? D / 8 : 4;
+  const long long threads = pairs * (D / 8 / chunks);
   const int block = 256;
-  const long long grid = (threads + block - 1) / block;
+  const unsigned grid = (unsigned)((threads + block - 1) / block);
   TraceScope trace_scope(stream, "lse_merge_kernel");
-  lse_merge_kernel<<<(unsigned)grid, block, 0, stream>>>(o_a, a_fp32, lse_a, o_b, b_fp32, lse_b,
-                                                         o_out, out_fp32, lse_out, rows, heads, D,
-                                                         pairs);
+  if (chunks == 4)
+    lse_merge_kernel<4><<<grid, block, 0, stream>>>(o_a, a_fp32, lse_a, o_b, b_fp32, lse_b, o_out,
+                                                    out_fp32, lse_out, rows, heads, D, pairs);
+  else if (chunks == 2)
+    lse_merge_kernel<2><<<grid, block, 0, stream>>>(o_a, a_fp32, lse_a, o_b, b_fp32, lse_b, o_out,
+                                                    out_fp32, lse_out, rows, heads, D, pairs);
+  else
+    lse_merge_kernel<1><<<grid, block, 0, stream>>>(o_a, a_fp32, lse_a, o_b, b_fp32, lse_b, o_out,
+                                                    out_fp32, lse_out, rows, heads, D, pairs);
   return cudaGetLastError();
 }
 

@@ -20,7 +20,8 @@ def to_np(t):
 def max_err(a, b):
     a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
     both_inf = np.isinf(a) & np.isinf(b) & (np.sign(a) == np.sign(b))
-    d = np.where(both_inf, 0.0, np.abs(a - b))
+    with np.errstate(invalid="ignore"):  # inf - inf where both_inf masks it out
+        d = np.where(both_inf, 0.0, np.abs(a - b))
     return float(np.max(d)) if d.size else 0.0
 
 

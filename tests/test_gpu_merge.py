@@ -31,7 +31,8 @@ def partials(rows, heads, d, seed, dtype):
 
 
 @pytest.mark.parametrize("dtype,tol", [(torch.float32, TOL_FP32), (torch.bfloat16, None)])
-@pytest.mark.parametrize("rows,heads,d", [(1000, 3, 128), (37, 2, 64), (4096, 8, 128)])
+@pytest.mark.parametrize("rows,heads,d", [(1000, 3, 128), (37, 2, 64), (4096, 8, 128), (300, 3, 8),
+                                          (129, 2, 16), (77, 5, 32), (64, 2, 256)])
 def test_merge_matches_oracle(dtype, tol, rows, heads, d):
     oa, la, ob, lb = partials(rows, heads, d, 7, dtype)
     ro, rl = oracle.lse_merge(oa.permute(1, 0, 2), la, ob.permute(1, 0, 2), lb)
@@ -48,6 +49,29 @@ def test_merge_matches_oracle(dtype, tol, rows, heads, d):
         fin = np.isfinite(ro)
         assert np.all(np.abs(go - ro)[fin] <= np.abs(ro[fin]) * 2.0 ** -8 * 1.01 + 1e-5)
     assert np.all(go[0, 2] == 0) and gl[0, 2] == -np.inf
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_merge_empty_side_is_ignored_exactly(dtype):
+    """A side with lse = -inf contributes nothing, whatever its o holds (here
+    NaN and inf): the other side comes through bit for bit."""
+    rows, heads, d = 513, 4, 128
+    oa, la, ob, lb = partials(rows, heads, d, 3, dtype)
+    la[:, :] = torch.randn(heads, rows)
+    lb[:, :] = -float("inf")
+    lb[:, ::3] = torch.randn(heads, (rows + 2) // 3)
+    la[:, ::3] = -float("inf")
+    ob[1::3] = float("nan")
+    ob[2::3] = float("inf")
+    oa[0::3] = float("nan")
+    a_o, a_l = oa.to(DEV), la.to(DEV)
+    ra.attn_lse_merge(a_o, a_l, ob.to(DEV), lb.to(DEV))
+    assert ra.ringattn_get_status() == 0
+    go, gl = a_o.cpu(), a_l.cpu()
+    keep_b = torch.zeros(rows, dtype=torch.bool)
+    keep_b[::3] = True
+    assert torch.equal(go[keep_b], ob[keep_b]) and torch.equal(go[~keep_b], oa[~keep_b])
+    assert torch.equal(gl[:, keep_b], lb[:, keep_b]) and torch.equal(gl[:, ~keep_b], la[:, ~keep_b])
 
 
 def test_merge_of_shard_partials_is_attention():
