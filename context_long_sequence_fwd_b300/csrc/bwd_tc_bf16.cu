@@ -23,11 +23,12 @@
 //     the first 32 columns of their S^T / dP^T block.
 //
 //   bwd_dq_kernel  one CTA per 128-row query tile (the forward plan's tiles),
-//     walking its key ranges in ring order; each key tile is split into two
-//     64-key halves, one per softmax warpgroup:
-//       S  = Q K_h^T,  dP = dO V_h^T   (M = 128 queries, N = 64 keys)
-//       dQ += dS K_h                   (TS: dS from TMEM, K MN-major)
-//     TMEM: S_a 0-63, dP_a 64-127, S_b 128-191, dP_b 192-255, dQ 256-383.
+//     walking its key ranges in ring order, one 128-key tile at a time:
+//       S  = Q K_j^T,  dP = dO V_j^T   (M = 128 queries, N = 128 keys)
+//       dQ += dS K_j                   (TS: dS from TMEM, K MN-major; two
+//                                       64-key halves, one per warpgroup)
+//     TMEM: S in two buffers 0-127 and 128-255 (key tile j in j % 2), dP
+//     256-383, dQ 384-511.
 //
 // Roles in both kernels (384 threads): warp 0 TMA producer, warp 1 TMEM
 // allocation and the single MMA-issuing thread, warps 2-3 (dK/dV only) load
