@@ -185,78 +185,118 @@ __global__ void __launch_bounds__(kThreads) ssd_state_pass_kernel(const SsdParam
   }
 }
 
+// Shared memory of the correction: the received state H (64 x N) and a block
+// of 32 tokens' C, rows padded by 4 floats so that the float4 reads of 16
+// different rows fall on distinct bank groups.
+template <int N>
+struct CorrStage {
+  float H[kP][N + 4];
+  float C[kTok][N + 4];
+  float y[kTok][kP];
+  float decay[kTok];  // exp(A sum dt) from the chunk start through the token
+  int m;              // tokens of the block before the first sample start
+};
+
+// Y[t, :] += exp(A sum_{c0 <= u <= t} dt_u) H C_t for the block's tokens t
+// before the first sample start: a 32 x 64 x N product per block, on CUDA
+// cores in fp32.  Thread (ty, tx) computes tokens ty and ty + 16 for head-dim
+// rows tx + 16 i (i < 4), accumulating even and odd n in the two halves of
+// paired registers.
 template <int N>
 __global__ void __launch_bounds__(kThreads) ssd_correction_kernel(const SsdParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  Stage<N>& st = *reinterpret_cast<Stage<N>*>(smem_raw);
-  constexpr int kCols = N / 8;
+  CorrStage<N>& st = *reinterpret_cast<CorrStage<N>*>(smem_raw);
   const int h = blockIdx.x, r = blockIdx.y + 1;
   const int g = h / (p.H / p.G);
-  const int rp = threadIdx.x >> 3, cs = threadIdx.x & 7;
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = p.T / p.R;
   const int c0 = r * L;
   const float A = p.A[h];
-  // rows 2 rp, 2 rp + 1 of the state rank r receives, in column pairs
-  uint64_t H0[kCols / 2], H1[kCols / 2];
-  const float* src = p.incoming + (((size_t)r * p.H + h) * kP + 2 * rp) * N;
-#pragma unroll
-  for (int i = 0; i < kCols / 2; ++i) {
-    const float2 u = *reinterpret_cast<const float2*>(&src[ssd_col(cs, 2 * i)]);
-    const float2 w = *reinterpret_cast<const float2*>(&src[N + ssd_col(cs, 2 * i)]);
-    H0[i] = f32x2(u.x, u.y);
-    H1[i] = f32x2(w.x, w.y);
+  {
+    const float4* src = reinterpret_cast<const float4*>(p.incoming + ((size_t)r * p.H + h) * kP * N);
+    for (int i = threadIdx.x; i < kP * N / 4; i += kThreads) {
+      const int row = i / (N / 4), c4 = i % (N / 4);
+      *reinterpret_cast<float4*>(&st.H[row][4 * c4]) = src[i];
+    }
   }
-  float lam = 0.f;  // A * sum dt from the chunk start
-  bool done = false;
-  for (int t0 = c0; t0 < c0 + L && !done; t0 += kTok) {
+  float lam = 0.f;  // A sum dt before the block (warp 0)
+  for (int t0 = c0; t0 < c0 + L; t0 += kTok) {
     const int n = min(kTok, c0 + L - t0);
-    __syncthreads();
-    stage_tokens<N, false, false>(st, p, h, g, t0, n);
-    __syncthreads();
-    int m = n;  // tokens of this block before the first sample start
-    for (int k = 0; k < n; ++k) {
-      if (st.pos[k] == 0) {
-        m = k;
-        done = true;
-        break;
-      }
-      lam = fmaf(st.dt[k], A, lam);
-      const float decay = expf(lam);
-      uint64_t acc0 = f32x2(0.f, 0.f), acc1 = f32x2(0.f, 0.f);
+    __syncthreads();  // the previous block's C and y are consumed
+    for (int i = threadIdx.x; i < n * (N / 4); i += kThreads) {
+      const int k = i / (N / 4), c4 = i % (N / 4);
+      *reinterpret_cast<float4*>(&st.C[k][4 * c4]) =
+          *reinterpret_cast<const float4*>(&p.C[((size_t)(t0 + k) * p.G + g) * N + 4 * c4]);
+    }
+    if (warp == 0) {
+      // prefix sum of dt A over the block, and the first sample start
+      const bool in = lane < n;
+      float v = in ? p.dt[(size_t)(t0 + lane) * p.H + h] * A : 0.f;
 #pragma unroll
-      for (int j = 0; j < kCols / 4; ++j) {
-        const float4 c4 = *reinterpret_cast<const float4*>(&st.C[k][ssd_col(cs, 4 * j)]);
-        const uint64_t c01 = f32x2(c4.x, c4.y), c23 = f32x2(c4.z, c4.w);
-        acc0 = ffma2(H0[2 * j], c01, acc0);
-        acc0 = ffma2(H0[2 * j + 1], c23, acc0);
-        acc1 = ffma2(H1[2 * j], c01, acc1);
-        acc1 = ffma2(H1[2 * j + 1], c23, acc1);
+      for (int o = 1; o < 32; o <<= 1) {
+        const float u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
       }
-      float p0, p1, q0, q1;
-      f32x2_split(acc0, &p0, &p1);
-      f32x2_split(acc1, &q0, &q1);
-      float y0 = p0 + p1, y1 = q0 + q1;
+      const float lk = lam + v;
+      st.decay[lane] = expf(lk);
+      lam = __shfl_sync(0xffffffffu, lk, 31);
+      const unsigned starts =
+          __ballot_sync(0xffffffffu, in && p.pos != nullptr && p.pos[t0 + lane] == 0);
+      if (lane == 0) st.m = starts ? __ffs(starts) - 1 : n;
+    }
+    __syncthreads();
+    const int m = st.m;
+    if (m > 0) {
+      uint64_t acc[2][4];
 #pragma unroll
-      for (int mm = 1; mm < 8; mm <<= 1) {
-        y0 += __shfl_xor_sync(0xffffffffu, y0, mm);
-        y1 += __shfl_xor_sync(0xffffffffu, y1, mm);
+      for (int a = 0; a < 2; ++a)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[a][i] = f32x2(0.f, 0.f);
+#pragma unroll 4
+      for (int c = 0; c < N; c += 4) {
+        const float4 ca = *reinterpret_cast<const float4*>(&st.C[ty][c]);
+        const float4 cb = *reinterpret_cast<const float4*>(&st.C[ty + 16][c]);
+        const uint64_t ca01 = f32x2(ca.x, ca.y), ca23 = f32x2(ca.z, ca.w);
+        const uint64_t cb01 = f32x2(cb.x, cb.y), cb23 = f32x2(cb.z, cb.w);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 hv = *reinterpret_cast<const float4*>(&st.H[tx + 16 * i][c]);
+          const uint64_t h01 = f32x2(hv.x, hv.y), h23 = f32x2(hv.z, hv.w);
+          acc[0][i] = ffma2(ca01, h01, acc[0][i]);
+          acc[0][i] = ffma2(ca23, h23, acc[0][i]);
+          acc[1][i] = ffma2(cb01, h01, acc[1][i]);
+          acc[1][i] = ffma2(cb23, h23, acc[1][i]);
+        }
       }
-      if (cs == 0) *reinterpret_cast<float2*>(&st.y[k][2 * rp]) = make_float2(decay * y0, decay * y1);
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        const int k = ty + 16 * a;
+        const float dk = st.decay[k];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float lo, hi;
+          f32x2_split(acc[a][i], &lo, &hi);
+          st.y[k][tx + 16 * i] = dk * (lo + hi);
+        }
+      }
     }
     __syncthreads();
     for (int i = threadIdx.x; i < m * kP; i += kThreads) {
       const int k = i / kP, c = i % kP;
       p.y[((size_t)(t0 + k) * p.H + h) * kP + c] += st.y[k][c];
     }
+    if (m < n) break;  // a sample starts here: the received state is gone
   }
 }
 
 template <int N>
 cudaError_t launch_n(const SsdParams& p, cudaStream_t stream) {
-  const size_t smem = sizeof(Stage<N>);
+  const size_t smem = sizeof(Stage<N>), smem_corr = sizeof(CorrStage<N>);
   static bool scan_configured[64] = {}, corr_configured[64] = {};
   cudaError_t e0 = ensure_smem_limit(ssd_chunk_scan_kernel<N>, (int)smem, scan_configured);
-  if (e0 == cudaSuccess) e0 = ensure_smem_limit(ssd_correction_kernel<N>, (int)smem, corr_configured);
+  if (e0 == cudaSuccess)
+    e0 = ensure_smem_limit(ssd_correction_kernel<N>, (int)smem_corr, corr_configured);
   if (e0 != cudaSuccess) return e0;
   {
     TraceScope trace_scope(stream, "ssd_chunk_scan_kernel");
@@ -272,7 +312,7 @@ cudaError_t launch_n(const SsdParams& p, cudaStream_t stream) {
   if (e != cudaSuccess || p.R < 2) return e;
   {
     TraceScope trace_scope(stream, "ssd_correction_kernel");
-    ssd_correction_kernel<N><<<dim3(p.H, p.R - 1), kThreads, smem, stream>>>(p);
+    ssd_correction_kernel<N><<<dim3(p.H, p.R - 1), kThreads, smem_corr, stream>>>(p);
   }
   return cudaGetLastError();
 }
