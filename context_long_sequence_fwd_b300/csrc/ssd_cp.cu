@@ -42,47 +42,141 @@ constexpr int kP = 64;       // head dimension
 constexpr int kThreads = 256;
 constexpr int kTok = 32;     // tokens staged per block
 
+// The scan keeps the state of each 32-token block scaled: with rho_k the
+// product of the decays exp(dt A) from the block start through token k,
+// S~_k = S_k / rho_k obeys S~_k = S~_{k-1} + (dt_k / rho_k) x_k B_k^T (one
+// FMA per entry instead of a multiply and an FMA), y_k = rho_k S~_k C_k, and
+// S = rho S~ again at the block end.  If rho would fall below kTinyRho, the
+// block rebases: S~ is first rescaled to the true state of the previous
+// token (pre = that token's rho) and rho restarts from the current decay, or,
+// when that decay itself is below kTinyRho, the previous state is dropped
+// (pre = 0: it would contribute less than 1e-20 of itself).
+constexpr float kTinyRho = 1e-20f;
+
 template <int N>
 struct Stage {
   float x[kTok][kP];
   float B[kTok][N];
   float C[kTok][N];
   float dt[kTok];
-  float decay[kTok];  // exp(dt A)
+  float rho[kTok];   // decay product since the block start (or the last rebase)
+  float irho[kTok];  // 1 / rho
+  float pre[kTok];   // factor applied to S~ before token k (1 = none)
   int pos[kTok];
   float y[kTok][kP];
 };
+
+// 16-byte global -> shared copy that does not pass through registers
+// (cp.async); with valid == false it writes zeros and reads nothing.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+// Waits for this thread's cp.async copies (a barrier then publishes them).
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
 
 // Column of the state a thread's i-th entry (of each of its rows) holds.
 __device__ __forceinline__ int ssd_col(int cs, int i) {
   return 32 * (i >> 2) + 4 * cs + (i & 3);
 }
 
-// Loads tokens [t0, t0 + n) of head h (group g) into shared memory.
-template <int N, bool kWantX, bool kWantB>
+// Loads tokens [t0, t0 + n) of head h (group g) into shared memory; warp 0
+// also forms the block's decay products (a multiplicative warp scan, so each
+// rho carries at most a few roundings).
+template <int N>
 __device__ __forceinline__ void stage_tokens(Stage<N>& st, const SsdParams& p, int h, int g, int t0,
                                              int n) {
-  for (int i = threadIdx.x; i < n * kP; i += kThreads) {
-    const int k = i / kP, c = i % kP;
-    if (kWantX) st.x[k][c] = p.x[((size_t)(t0 + k) * p.H + h) * kP + c];
+  // every 16-byte copy of the block is in flight at once
+  constexpr int kX4 = kTok * kP / 4 / kThreads, kB4 = kTok * N / 4 / kThreads;
+#pragma unroll
+  for (int u = 0; u < kX4; ++u) {
+    const int i = threadIdx.x + u * kThreads, k = i / (kP / 4), c4 = i % (kP / 4);
+    cp_async16(&st.x[k][4 * c4], &p.x[((size_t)(t0 + min(k, n - 1)) * p.H + h) * kP + 4 * c4], k < n);
   }
-  for (int i = threadIdx.x; i < n * N; i += kThreads) {
-    const int k = i / N, c = i % N;
-    const size_t o = ((size_t)(t0 + k) * p.G + g) * N + c;
-    if (kWantB) st.B[k][c] = p.B[o];
-    st.C[k][c] = p.C[o];
+#pragma unroll
+  for (int u = 0; u < kB4; ++u) {
+    const int i = threadIdx.x + u * kThreads, k = i / (N / 4), c4 = i % (N / 4);
+    const size_t o = ((size_t)(t0 + min(k, n - 1)) * p.G + g) * N + 4 * c4;
+    cp_async16(&st.B[k][4 * c4], &p.B[o], k < n);
+    cp_async16(&st.C[k][4 * c4], &p.C[o], k < n);
   }
-  const float A = p.A[h];
-  for (int k = threadIdx.x; k < n; k += kThreads) {
-    const float d = p.dt[(size_t)(t0 + k) * p.H + h];
-    st.dt[k] = d;
-    st.decay[k] = expf(d * A);
-    st.pos[k] = p.pos ? p.pos[t0 + k] : 1;
+  if (threadIdx.x < 32) {
+    const int k = threadIdx.x;
+    const bool in = k < n;
+    const float d = in ? p.dt[(size_t)(t0 + k) * p.H + h] : 0.f;
+    const float a = in ? expf(d * p.A[h]) : 1.f;
+    float rho = a;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float u = __shfl_up_sync(0xffffffffu, rho, o);
+      if (k >= o) rho *= u;
+    }
+    if (in) {
+      st.dt[k] = d;
+      st.pos[k] = p.pos ? p.pos[t0 + k] : 1;
+    }
+    if (__ballot_sync(0xffffffffu, in && rho < kTinyRho) == 0) {
+      if (in) {
+        st.rho[k] = rho;
+        st.irho[k] = 1.f / rho;
+        st.pre[k] = 1.f;
+      }
+    } else {
+      // rare: the block decays past kTinyRho; rebase token by token
+      const float ak = a;
+      float r = 1.f;
+      for (int j = 0; j < n; ++j) {
+        const float aj = __shfl_sync(0xffffffffu, ak, j);
+        float pre = 1.f;
+        const float rn = r * aj;
+        if (rn >= kTinyRho) {
+          r = rn;
+        } else if (aj >= kTinyRho) {
+          pre = r;  // S~ becomes the true state of token j - 1
+          r = aj;
+        } else {
+          pre = 0.f;  // the previous state is dropped
+          r = 1.f;
+        }
+        if (k == 0) {
+          st.rho[j] = r;
+          st.irho[j] = 1.f / r;
+          st.pre[j] = pre;
+        }
+      }
+    }
   }
+  cp_async_wait_all();
+}
+
+// Sums v[t] (t < 8: eight tokens' partial row values of this thread) over the
+// eight lanes of a row pair and leaves token cs's total in the result:
+// three halving exchanges (xor 4, 2, 1) instead of a full reduction per token.
+__device__ __forceinline__ float reduce_scatter8(const float (&v)[8], int cs) {
+  float w[4];
+  const bool b2 = (cs & 4) != 0;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float send = b2 ? v[t] : v[t + 4];
+    w[t] = (b2 ? v[t + 4] : v[t]) + __shfl_xor_sync(0xffffffffu, send, 4);
+  }
+  const bool b1 = (cs & 2) != 0;
+  float u[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const float send = b1 ? w[t] : w[t + 2];
+    u[t] = (b1 ? w[t + 2] : w[t]) + __shfl_xor_sync(0xffffffffu, send, 2);
+  }
+  const bool b0 = (cs & 1) != 0;
+  const float send = b0 ? u[0] : u[1];
+  return (b0 ? u[1] : u[0]) + __shfl_xor_sync(0xffffffffu, send, 1);
 }
 
 template <int N>
-__global__ void __launch_bounds__(kThreads) ssd_chunk_scan_kernel(const SsdParams p) {
+__global__ void __launch_bounds__(kThreads, 4) ssd_chunk_scan_kernel(const SsdParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Stage<N>& st = *reinterpret_cast<Stage<N>*>(smem_raw);
   constexpr int kCols = N / 8;  // columns per thread, for each of its two rows
@@ -93,8 +187,8 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_scan_kernel(const SsdParam
   const int c0 = r * L;
   const float A = p.A[h];
   const float Dh = p.D ? p.D[h] : 0.f;
-  // rows 2 rp and 2 rp + 1, two adjacent columns per 64-bit register pair:
-  // the update and the read-out run on paired fp32 instructions
+  // rows 2 rp and 2 rp + 1 of S~, two adjacent columns per 64-bit register
+  // pair: the update and the read-out run on paired fp32 instructions
   uint64_t S0[kCols / 2], S1[kCols / 2];
 #pragma unroll
   for (int i = 0; i < kCols / 2; ++i) S0[i] = S1[i] = f32x2(0.f, 0.f);
@@ -103,54 +197,80 @@ __global__ void __launch_bounds__(kThreads) ssd_chunk_scan_kernel(const SsdParam
   for (int t0 = c0; t0 < c0 + L; t0 += kTok) {
     const int n = min(kTok, c0 + L - t0);
     __syncthreads();  // the previous block's y has been written out
-    stage_tokens<N, true, true>(st, p, h, g, t0, n);
+    stage_tokens<N>(st, p, h, g, t0, n);
     __syncthreads();
-    for (int k = 0; k < n; ++k) {
-      if (st.pos[k] == 0) {
+    for (int k8 = 0; k8 < n; k8 += 8) {
+      float v0[8], v1[8];  // this thread's partial y of rows 2 rp, 2 rp + 1
 #pragma unroll
-        for (int i = 0; i < kCols / 2; ++i) S0[i] = S1[i] = f32x2(0.f, 0.f);
-        reset = true;
-        logcarry = 0.f;
-      }
-      const float d = st.dt[k];
-      const float a = st.decay[k];
-      logcarry += d * A;
-      const float2 x2 = *reinterpret_cast<const float2*>(&st.x[k][2 * rp]);
-      const uint64_t aa = f32x2(a, a);
-      const uint64_t dx0 = f32x2(d * x2.x, d * x2.x), dx1 = f32x2(d * x2.y, d * x2.y);
-      uint64_t acc0 = f32x2(0.f, 0.f), acc1 = f32x2(0.f, 0.f);
+      for (int kk = 0; kk < 8; ++kk) {
+        const int k = k8 + kk;
+        v0[kk] = v1[kk] = 0.f;
+        if (k < n) {
+          if (st.pos[k] == 0) {
 #pragma unroll
-      for (int j = 0; j < kCols / 4; ++j) {
-        const float4 b4 = *reinterpret_cast<const float4*>(&st.B[k][ssd_col(cs, 4 * j)]);
-        const float4 c4 = *reinterpret_cast<const float4*>(&st.C[k][ssd_col(cs, 4 * j)]);
-        const uint64_t b01 = f32x2(b4.x, b4.y), b23 = f32x2(b4.z, b4.w);
-        const uint64_t c01 = f32x2(c4.x, c4.y), c23 = f32x2(c4.z, c4.w);
-        S0[2 * j] = ffma2(aa, S0[2 * j], fmul2(dx0, b01));
-        S0[2 * j + 1] = ffma2(aa, S0[2 * j + 1], fmul2(dx0, b23));
-        S1[2 * j] = ffma2(aa, S1[2 * j], fmul2(dx1, b01));
-        S1[2 * j + 1] = ffma2(aa, S1[2 * j + 1], fmul2(dx1, b23));
-        acc0 = ffma2(S0[2 * j], c01, acc0);
-        acc0 = ffma2(S0[2 * j + 1], c23, acc0);
-        acc1 = ffma2(S1[2 * j], c01, acc1);
-        acc1 = ffma2(S1[2 * j + 1], c23, acc1);
-      }
-      float p0, p1, q0, q1;
-      f32x2_split(acc0, &p0, &p1);
-      f32x2_split(acc1, &q0, &q1);
-      float y0 = p0 + p1, y1 = q0 + q1;
+            for (int i = 0; i < kCols / 2; ++i) S0[i] = S1[i] = f32x2(0.f, 0.f);
+            reset = true;
+            logcarry = 0.f;
+          }
+          const float pre = st.pre[k];
+          if (pre != 1.f) {
+            const uint64_t pp = f32x2(pre, pre);
 #pragma unroll
-      for (int m = 1; m < 8; m <<= 1) {
-        y0 += __shfl_xor_sync(0xffffffffu, y0, m);
-        y1 += __shfl_xor_sync(0xffffffffu, y1, m);
+            for (int i = 0; i < kCols / 2; ++i) {
+              S0[i] = fmul2(pp, S0[i]);
+              S1[i] = fmul2(pp, S1[i]);
+            }
+          }
+          const float d = st.dt[k];
+          logcarry = fmaf(d, A, logcarry);
+          const float2 x2 = *reinterpret_cast<const float2*>(&st.x[k][2 * rp]);
+          const float di = d * st.irho[k];
+          const uint64_t dx0 = f32x2(di * x2.x, di * x2.x), dx1 = f32x2(di * x2.y, di * x2.y);
+          uint64_t acc0 = f32x2(0.f, 0.f), acc1 = f32x2(0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < kCols / 4; ++j) {
+            const float4 b4 = *reinterpret_cast<const float4*>(&st.B[k][ssd_col(cs, 4 * j)]);
+            const float4 c4 = *reinterpret_cast<const float4*>(&st.C[k][ssd_col(cs, 4 * j)]);
+            const uint64_t b01 = f32x2(b4.x, b4.y), b23 = f32x2(b4.z, b4.w);
+            const uint64_t c01 = f32x2(c4.x, c4.y), c23 = f32x2(c4.z, c4.w);
+            S0[2 * j] = ffma2(dx0, b01, S0[2 * j]);
+            S0[2 * j + 1] = ffma2(dx0, b23, S0[2 * j + 1]);
+            S1[2 * j] = ffma2(dx1, b01, S1[2 * j]);
+            S1[2 * j + 1] = ffma2(dx1, b23, S1[2 * j + 1]);
+            acc0 = ffma2(S0[2 * j], c01, acc0);
+            acc0 = ffma2(S0[2 * j + 1], c23, acc0);
+            acc1 = ffma2(S1[2 * j], c01, acc1);
+            acc1 = ffma2(S1[2 * j + 1], c23, acc1);
+          }
+          float p0, p1, q0, q1;
+          f32x2_split(acc0, &p0, &p1);
+          f32x2_split(acc1, &q0, &q1);
+          v0[kk] = p0 + p1;
+          v1[kk] = q0 + q1;
+        }
       }
-      if (cs == 0)
+      // lane cs of the row pair finishes token k8 + cs of both rows
+      const float y0 = reduce_scatter8(v0, cs), y1 = reduce_scatter8(v1, cs);
+      const int k = k8 + cs;
+      if (k < n) {
+        const float2 x2 = *reinterpret_cast<const float2*>(&st.x[k][2 * rp]);
+        const float rk = st.rho[k];
         *reinterpret_cast<float2*>(&st.y[k][2 * rp]) =
-            make_float2(fmaf(Dh, x2.x, y0), fmaf(Dh, x2.y, y1));
+            make_float2(fmaf(Dh, x2.x, rk * y0), fmaf(Dh, x2.y, rk * y1));
+      }
+    }
+    // back to the true state for the next block
+    const uint64_t rr = f32x2(st.rho[n - 1], st.rho[n - 1]);
+#pragma unroll
+    for (int i = 0; i < kCols / 2; ++i) {
+      S0[i] = fmul2(rr, S0[i]);
+      S1[i] = fmul2(rr, S1[i]);
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < n * kP; i += kThreads) {
-      const int k = i / kP, c = i % kP;
-      p.y[((size_t)(t0 + k) * p.H + h) * kP + c] = st.y[k][c];
+    for (int i = threadIdx.x; i < n * (kP / 4); i += kThreads) {
+      const int k = i / (kP / 4), c4 = i % (kP / 4);
+      *reinterpret_cast<float4*>(&p.y[((size_t)(t0 + k) * p.H + h) * kP + 4 * c4]) =
+          *reinterpret_cast<const float4*>(&st.y[k][4 * c4]);
     }
   }
   // the chunk's final state and the factor an incoming state survives with
@@ -224,10 +344,14 @@ __global__ void __launch_bounds__(kThreads) ssd_correction_kernel(const SsdParam
   for (int t0 = c0; t0 < c0 + L; t0 += kTok) {
     const int n = min(kTok, c0 + L - t0);
     __syncthreads();  // the previous block's C and y are consumed
-    for (int i = threadIdx.x; i < n * (N / 4); i += kThreads) {
-      const int k = i / (N / 4), c4 = i % (N / 4);
-      *reinterpret_cast<float4*>(&st.C[k][4 * c4]) =
-          *reinterpret_cast<const float4*>(&p.C[((size_t)(t0 + k) * p.G + g) * N + 4 * c4]);
+    {
+      constexpr int kC4 = kTok * N / 4 / kThreads;
+#pragma unroll
+      for (int u = 0; u < kC4; ++u) {
+        const int i = threadIdx.x + u * kThreads, k = i / (N / 4), c4 = i % (N / 4);
+        cp_async16(&st.C[k][4 * c4], &p.C[((size_t)(t0 + min(k, n - 1)) * p.G + g) * N + 4 * c4],
+                   k < n);
+      }
     }
     if (warp == 0) {
       // prefix sum of dt A over the block, and the first sample start
@@ -245,6 +369,7 @@ __global__ void __launch_bounds__(kThreads) ssd_correction_kernel(const SsdParam
           __ballot_sync(0xffffffffu, in && p.pos != nullptr && p.pos[t0 + lane] == 0);
       if (lane == 0) st.m = starts ? __ffs(starts) - 1 : n;
     }
+    cp_async_wait_all();
     __syncthreads();
     const int m = st.m;
     if (m > 0) {
@@ -282,9 +407,24 @@ __global__ void __launch_bounds__(kThreads) ssd_correction_kernel(const SsdParam
       }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < m * kP; i += kThreads) {
-      const int k = i / kP, c = i % kP;
-      p.y[((size_t)(t0 + k) * p.H + h) * kP + c] += st.y[k][c];
+    {
+      // y += the block's correction: both 16-byte reads in flight before the adds
+      constexpr int kY4 = kTok * kP / 4 / kThreads;
+      float4 ry[kY4];
+#pragma unroll
+      for (int u = 0; u < kY4; ++u) {
+        const int i = threadIdx.x + u * kThreads, k = i / (kP / 4), c4 = i % (kP / 4);
+        if (k < m) ry[u] = *reinterpret_cast<const float4*>(&p.y[((size_t)(t0 + k) * p.H + h) * kP + 4 * c4]);
+      }
+#pragma unroll
+      for (int u = 0; u < kY4; ++u) {
+        const int i = threadIdx.x + u * kThreads, k = i / (kP / 4), c4 = i % (kP / 4);
+        if (k < m) {
+          const float4 c = *reinterpret_cast<const float4*>(&st.y[k][4 * c4]);
+          *reinterpret_cast<float4*>(&p.y[((size_t)(t0 + k) * p.H + h) * kP + 4 * c4]) =
+              make_float4(ry[u].x + c.x, ry[u].y + c.y, ry[u].z + c.z, ry[u].w + c.w);
+        }
+      }
     }
     if (m < n) break;  // a sample starts here: the received state is gone
   }

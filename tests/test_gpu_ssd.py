@@ -79,6 +79,20 @@ def test_without_skip_term():
     check(inp, 4)
 
 
+@pytest.mark.parametrize("lo,hi", [(0.3, 1.0), (0.01, 10.0)])
+def test_strong_decay(lo, hi):
+    """Decays strong enough that a 32-token block's running decay product
+    falls below 1e-20: the scan rebases its scaled state (dt A about -5 per
+    token), or drops the previous state outright where one token's decay is
+    itself below 1e-20 (dt A down to -160)."""
+    T, H = 1024, 4
+    inp = make_ssd_inputs(T, H, 64, 128, 2, seed=9, packed=False)
+    g = torch.Generator("cpu").manual_seed(19)
+    inp["dt"] = torch.exp(torch.empty(T, H).uniform_(np.log(lo), np.log(hi), generator=g))
+    inp["A"] = -torch.empty(H).uniform_(5.0, 16.0, generator=g)
+    check(inp, 4)
+
+
 def test_shards_do_not_change_the_result():
     inp = make_ssd_inputs(4096, 4, 64, 128, 2, seed=7)
     y1, h1 = run(inp, 1)
