@@ -53,9 +53,13 @@ constexpr int kTok = 32;     // tokens staged per block
 // (pre = 0: it would contribute less than 1e-20 of itself).
 constexpr float kTinyRho = 1e-20f;
 
+// x and y rows are padded to kPX floats: the output step reads x and writes y
+// of eight different tokens at once, which 64-float rows put on one bank.
+constexpr int kPX = kP + 4;
+
 template <int N>
 struct Stage {
-  float x[kTok][kP];
+  float x[kTok][kPX];
   float B[kTok][N];
   float C[kTok][N];
   float dt[kTok];
@@ -63,7 +67,7 @@ struct Stage {
   float irho[kTok];  // 1 / rho
   float pre[kTok];   // factor applied to S~ before token k (1 = none)
   int pos[kTok];
-  float y[kTok][kP];
+  float y[kTok][kPX];
 };
 
 // 16-byte global -> shared copy that does not pass through registers
@@ -312,7 +316,7 @@ template <int N>
 struct CorrStage {
   float H[kP][N + 4];
   float C[kTok][N + 4];
-  float y[kTok][kP];
+  float y[kTok][kP + 16];  // rows 16 banks apart: two tokens' rows per warp store
   float decay[kTok];  // exp(A sum dt) from the chunk start through the token
   int m;              // tokens of the block before the first sample start
 };
