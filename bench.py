@@ -73,7 +73,8 @@ def load_peaks():
 
 
 KERNEL_SOURCES = {"fwd_tc_bf16_kernel": "fwd_tc_bf16.cu", "bwd_dkdv_kernel": "bwd_tc_bf16.cu",
-                  "bwd_dq_kernel": "bwd_tc_bf16.cu"}
+                  "bwd_dq_kernel": "bwd_tc_bf16.cu", "ssd_chunk_scan_kernel": "ssd_cp.cu",
+                  "ssd_correction_kernel": "ssd_cp.cu"}
 
 
 def kernel_traffic(kernel: str, workload: str):
@@ -625,7 +626,8 @@ def run_ssd(args):
                      "achieved": round(achieved, 3), "peak": round(peak, 1),
                      "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "peak_source": "148 SMs x 128 fp32 lanes x 2 flops x 2.032 GHz",
-                     "traffic": None, "flops_per_launch": f},
+                     "traffic": kernel_traffic("ssd_chunk_scan_kernel", w.name),
+                     "flops_per_launch": f},
         "kernels": ktab,
         "cpu_baseline": cpu,
         "e2e": {"value": round(world * f / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
