@@ -60,6 +60,16 @@ def visible_pairs(w, cu) -> int:
     return int(sum(L * (L + 1) // 2 for L in ls) if w.causal else sum(L * L for L in ls))
 
 
+def power_capped(clk: dict) -> bool:
+    """Whether the power cap held the SM clock down while the step was timed
+    (flag seen, median clock under load below 90 % of its maximum).  The top
+    kernel is timed inside the step loop, so it is then measured against the
+    sustained (seconds-long, power-capped) GEMM figure, else the burst one."""
+    mhz, top = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    return bool("sw_power_cap" in clk.get("reasons", []) and mhz is not None and top
+                and mhz < 0.9 * top)
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -453,12 +463,7 @@ def run_ours(args):
         ktab[name] = ent
     top = max((n for n in ktab if n in KERNEL_FWD_UNITS), key=lambda n: ktab[n]["share"])
     achieved = ktab[top]["tflops"]
-    # The top kernel is timed inside the step loop: when the power cap held
-    # the SM clock down during the timed region (flag seen, median clock under
-    # load below 90 % of its maximum), the sustained (seconds-long, power-
-    # capped) GEMM figure is its denominator, else the burst figure.
-    capped = ("sw_power_cap" in clk.get("reasons", []) and clk.get("sm_mhz") is not None
-              and clk.get("sm_max_mhz") and clk["sm_mhz"] < 0.9 * clk["sm_max_mhz"])
+    capped = power_capped(clk)
     peak_top = peak_s if capped else peak
     roof = {"bound": "tensor", "kernel": top, "achieved": achieved, "peak": peak_top,
             "unit": "TFLOP/s", "frac": round(achieved / peak_top, 4),

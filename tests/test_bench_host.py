@@ -85,3 +85,26 @@ def test_ours_refuses_without_gpu():
     r = subprocess.run([sys.executable, "bench.py", "--steps", "1", "--warmup", "3"], cwd=ROOT,
                        capture_output=True, text=True, timeout=300)
     assert r.returncode != 0 and "needs a CUDA device" in (r.stdout + r.stderr)
+
+
+def test_power_capped_rule():
+    """The sustained peak applies only when the cap actually held the clock
+    down; a flag seen at full clock (a short forward) keeps the burst peak."""
+    cap = ["sw_power_cap"]
+    assert bench.power_capped({"sm_mhz": 1530.0, "sm_max_mhz": 2032.0, "reasons": cap})
+    assert not bench.power_capped({"sm_mhz": 2028.5, "sm_max_mhz": 2032.0, "reasons": cap})
+    assert not bench.power_capped({"sm_mhz": 1530.0, "sm_max_mhz": 2032.0, "reasons": []})
+    assert not bench.power_capped({"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]})
+
+
+def test_committed_profiles_parse():
+    """Every committed kernel summary the bench reads carries a source digest
+    and a DRAM byte count (the digest decides whether the count is used)."""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    for kernel in bench.KERNEL_SOURCES:
+        for name in os.listdir(os.path.join(root, "profiles")):
+            if not name.startswith(kernel + "_"):
+                continue
+            text = open(os.path.join(root, "profiles", name)).read()
+            assert "- kernel_source_sha256_16: `" in text, name
+            assert "- dram_bytes_per_launch: `" in text, name
