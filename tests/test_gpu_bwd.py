@@ -91,6 +91,8 @@ BF16_CASES = [
     (2048, 4, 2, 4, ra.CONTIGUOUS, True, MANY_DOCS),     # 44 documents shorter than a tile
     (16, 2, 1, 2, ra.ZIGZAG, True, None),                # 4 chunks of 4 tokens
     (2, 1, 1, 1, ra.CONTIGUOUS, True, None),             # two tokens
+    (1024, 16, 2, 4, ra.ZIGZAG, True, None),             # GQA group of 8
+    (896, 8, 1, 2, ra.CONTIGUOUS, True, [0, 333, 896]),  # one KV head for 8 query heads
 ]
 
 
