@@ -99,6 +99,7 @@ def library():
         lib.attn_lse_merge.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, _vp]
         lib.ringattn_get_status.argtypes = [_vp]
+        lib.ringattn_selftest_wait_timeout.argtypes = [_vp]
         lib.ringattn_status_string.argtypes = [ctypes.c_int]
         lib.ringattn_status_string.restype = ctypes.c_char_p
         lib.ringattn_version.restype = ctypes.c_int
@@ -114,7 +115,8 @@ def library():
         lib.ringattn_trace_enable.argtypes = [ctypes.c_int]
         lib.ringattn_trace_collect.argtypes = [ctypes.POINTER(ra_trace_entry), ctypes.c_int, _ip]
         for fn in ("ringattn_fwd", "ringattn_fwd_stepwise", "ringattn_bwd", "attn_lse_merge",
-                   "ringattn_get_status", "ringattn_plan_fwd", "ringattn_plan_bwd",
+                   "ringattn_get_status", "ringattn_selftest_wait_timeout",
+                   "ringattn_plan_fwd", "ringattn_plan_bwd",
                    "ringattn_trace_enable", "ringattn_trace_collect"):
             getattr(lib, fn).restype = ctypes.c_int
         _lib = lib
@@ -279,6 +281,14 @@ def attn_lse_merge(o_a, lse_a, o_b, lse_b, stream=None):
 def ringattn_get_status(stream=None) -> int:
     """Synchronises the stream; returns and clears the kernel-side error word."""
     return int(library().ringattn_get_status(_stream(stream)))
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Launches the failure-path self-test: one kernel wait that runs out
+    after its time limit and records RA_ERR_TIMEOUT (read it with
+    ringattn_get_status)."""
+    _check("ringattn_selftest_wait_timeout",
+           library().ringattn_selftest_wait_timeout(_stream(stream)))
 
 
 def _plan(fn_name, item_fields, total_tokens, hq, hkv, num_shards, shard_layout, causal,

@@ -699,6 +699,19 @@ ra_status ringattn_get_status(void* stream) {
   return static_cast<ra_status>(word);
 }
 
+ra_status ringattn_selftest_wait_timeout(void* stream) {
+  int dev;
+  DeviceState* ds;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    ra_status st = current_device(&dev, &ds);
+    if (st != RA_OK) return st;
+  }
+  return launch_wait_timeout_selftest(ds->status, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RA_OK
+             : RA_ERR_CUDA;
+}
+
 const char* ringattn_status_string(int status) {
   switch (status) {
     case RA_OK: return "ok";

@@ -48,6 +48,10 @@ cudaError_t launch_bwd_tc_bf16(const BwdParams& p, const CUtensorMap& map_q,
                                const CUtensorMap& map_k, const CUtensorMap& map_v,
                                const CUtensorMap& map_do, cudaStream_t stream);
 
+// One CTA whose single bounded wait is never satisfied: after the wait
+// limit it records RA_ERR_TIMEOUT in *status and exits (failure-path test).
+cudaError_t launch_wait_timeout_selftest(int* status, cudaStream_t stream);
+
 // fp32 backward on CUDA cores (D = 64 or 128).
 cudaError_t launch_bwd_simt_fp32(const BwdParams& p, cudaStream_t stream);
 

@@ -228,6 +228,16 @@ ra_status ssd_cp_fwd(const float* x, const float* dt, const float* A, const floa
  * the last call (RA_OK if none) and clears it. */
 ra_status ringattn_get_status(void* stream);
 
+/*
+ * Self-test of the failure path of every kernel wait.  Launches one CTA that
+ * waits on a barrier nothing ever arrives at; the wait gives up after its
+ * time limit (1 s), records RA_ERR_TIMEOUT in the status word and the kernel
+ * exits normally, so the context stays usable.  Asynchronous on `stream`;
+ * ringattn_get_status(stream) afterwards returns RA_ERR_TIMEOUT (and clears
+ * it).  Returns RA_OK if the launch succeeded.
+ */
+ra_status ringattn_selftest_wait_timeout(void* stream);
+
 /* Static text for a status code. */
 const char* ringattn_status_string(int status);
 

@@ -256,3 +256,20 @@ def test_ulysses_head_partition_equals_ring():
     uly_o, uly_l = run_fwd(q, k, v, None, P, ra.CONTIGUOUS, True, hks=hkv // P,
                            exchange=ra.ALLGATHER)
     assert max_err(uly_o, ring_o) <= 2e-2 and max_err(uly_l, ring_l) <= 1e-4
+
+
+def test_bounded_wait_runs_out_and_is_reported():
+    """The kernels' failure path, without a fault: a wait on a barrier that
+    nothing arrives at gives up after its limit (about 1 s), the status word
+    reports RA_ERR_TIMEOUT once, and the context still computes correctly."""
+    import time
+    assert ra.ringattn_get_status() == 0
+    t0 = time.perf_counter()
+    ra.selftest_wait_timeout()
+    status = ra.ringattn_get_status()
+    elapsed = time.perf_counter() - t0
+    assert status == -5, status  # RA_ERR_TIMEOUT
+    assert 0.5 < elapsed < 30.0, elapsed
+    assert ra.ringattn_get_status() == 0  # read once, then cleared
+    q, k, v = make_qkv(512, 2, 1, 128, "bf16", seed=21)
+    check_full(q, k, v, None, 2, ra.ZIGZAG, True, TOL_BF16_O, TOL_BF16_LSE, False)
