@@ -145,6 +145,9 @@ ra_status ringattn_fwd_stepwise(const void* q, const void* k, const void* v,
  *     RA_ERR_WORKSPACE and launch nothing.
  *   - All calls share the array: calls that overlap on the GPU (different
  *     streams or threads) race; calls on one stream are ordered.
+ *   - Every call builds its work list on the host and copies it into the
+ *     array with cudaMemcpyAsync on `stream` (from host memory that the call
+ *     frees when it returns) before it launches the kernels.
  *   - The first call on a device looks up the array's device address; make
  *     that first call before any stream capture.
  */
@@ -234,7 +237,10 @@ ra_status ringattn_get_status(void* stream);
  * time limit (1 s), records RA_ERR_TIMEOUT in the status word and the kernel
  * exits normally, so the context stays usable.  Asynchronous on `stream`;
  * ringattn_get_status(stream) afterwards returns RA_ERR_TIMEOUT (and clears
- * it).  Returns RA_OK if the launch succeeded.
+ * it).  Returns RA_OK if the launch succeeded.  The status word is shared by
+ * every stream of the device, so run the self-test while no other call of
+ * this library is in flight on the device: a concurrent caller's
+ * ringattn_get_status would otherwise report (and clear) this timeout.
  */
 ra_status ringattn_selftest_wait_timeout(void* stream);
 
