@@ -7,7 +7,10 @@ product package.
 
 The arithmetic lives in ``attention_fp64.c`` and ``ssd_fp64.c`` (plain C,
 OpenMP over rows / heads); this module compiles them with gcc on first use and
-marshals numpy/torch arrays to them.
+marshals numpy/torch arrays to them.  ``oracle.blas`` (``attention_blas.py``)
+computes the same attention definition with fp64 library matrix products, fast
+enough to check every row of the full-size workloads; it is pinned by the same
+checks as the C oracle.
 Every function computes the plain definition of attention over the whole,
 unsharded sequence (the ring schedule is an exact re-ordering of that sum,
 axolotl "Sequence Parallelism" page, introduction and "Implementation
@@ -273,3 +276,6 @@ def ssd_scan(x, dt, A, B, C, D=None, position_ids=None, h0=None):
         None if Dd is None else _ptr(Dd, _dp), None if pos is None else _ptr(pos, _ip),
         T, H, P, N, G, None if h0d is None else _ptr(h0d, _dp), _ptr(y, _dp), _ptr(hT, _dp)))
     return y, hT
+
+
+from . import attention_blas as blas  # noqa: E402  (fp64 matrix-product oracle)

@@ -13,6 +13,10 @@
   sum_j dV_j = sum over the group's queries of dO;
 * finite differences of L = sum(dO * O) against the analytic gradients.
 
+The pins that speak only of the definition take the implementation as an
+argument, so the same checks also pin the matrix-product oracle
+(``oracle.blas``, see test_oracle_blas.py).
+
 These follow the definition of attention the ring schedule must reproduce
 (every query sees every key of its document, axolotl "Sequence Parallelism"
 page, introduction; aicassindra "tm_sp_math", "Context parallelism is the axis
@@ -82,25 +86,25 @@ CASES = [
 # ------------------------------------------------------------ pin checks
 # Written as functions so the mutation tests can run them on a broken oracle.
 
-def check_bruteforce(seed=0):
+def check_bruteforce(seed=0, impl=oracle):
     for (T, hq, hkv, d, cu, causal) in CASES:
         q, k, v = rand_qkv(T, hq, hkv, d, seed, with_do=False)
-        o, lse = oracle.attention_fwd(q, k, v, causal=causal, cu_seqlens=cu)
+        o, lse = impl.attention_fwd(q, k, v, causal=causal, cu_seqlens=cu)
         ob, lb = brute_force(q, k, v, cu, causal)
         assert np.max(np.abs(o - ob)) < 1e-12
         assert np.max(np.abs(lse - lb)) < 1e-12
 
 
-def check_fd_gradients():
+def check_fd_gradients(impl=oracle):
     T, hq, hkv, d = 12, 4, 2, 3
     cu = [0, 5, 12]
     q, k, v, do = rand_qkv(T, hq, hkv, d, 7)
 
     def loss(q_, k_, v_):
-        o, _ = oracle.attention_fwd(q_, k_, v_, causal=True, cu_seqlens=cu)
+        o, _ = impl.attention_fwd(q_, k_, v_, causal=True, cu_seqlens=cu)
         return float(np.sum(do * o))
 
-    dq, dk, dv, _, _ = oracle.attention_bwd(q, k, v, do, causal=True, cu_seqlens=cu)
+    dq, dk, dv, _, _ = impl.attention_bwd(q, k, v, do, causal=True, cu_seqlens=cu)
     h = 1e-5
     r = np.random.default_rng(3)
     for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
@@ -117,11 +121,11 @@ def check_fd_gradients():
             assert abs(fd - g[idx]) <= 1e-6 * max(1.0, abs(fd)), (name, idx, fd, g[idx])
 
 
-def check_partition_merge():
+def check_partition_merge(impl=oracle):
     T, hq, hkv, d = 64, 4, 2, 8
     cu = [0, 9, 41, 64]
     q, k, v = rand_qkv(T, hq, hkv, d, 11, with_do=False)
-    o_full, l_full = oracle.attention_fwd(q, k, v, causal=True, cu_seqlens=cu)
+    o_full, l_full = impl.attention_fwd(q, k, v, causal=True, cu_seqlens=cu)
     r = np.random.default_rng(5)
     partitions = []
     labels = r.integers(0, 3, T)                       # random 3-way partition
@@ -136,8 +140,8 @@ def check_partition_merge():
         order = r.permutation(len(parts))
         acc_o, acc_l = None, None
         for p in order:
-            o_p, l_p = oracle.attention_fwd(q, k, v, causal=True, cu_seqlens=cu,
-                                            key_allowed=parts[p])
+            o_p, l_p = impl.attention_fwd(q, k, v, causal=True, cu_seqlens=cu,
+                                          key_allowed=parts[p])
             o_p = o_p.transpose(1, 0, 2)               # [Hq, T, D] rows match lse
             if acc_o is None:
                 acc_o, acc_l = o_p, l_p
@@ -169,12 +173,12 @@ def check_merge_rule():
     assert np.all(om[5] == 0.0) and lm[5] == -np.inf
 
 
-def check_backward_identities():
+def check_backward_identities(impl=oracle):
     T, hq, hkv, d = 40, 6, 2, 8
     cu = [0, 13, 40]
     q, k, v, do = rand_qkv(T, hq, hkv, d, 21)
-    o, lse = oracle.attention_fwd(q, k, v, causal=True, cu_seqlens=cu)
-    dq, dk, dv, D, l2 = oracle.attention_bwd(q, k, v, do, causal=True, cu_seqlens=cu)
+    o, lse = impl.attention_fwd(q, k, v, causal=True, cu_seqlens=cu)
+    dq, dk, dv, D, l2 = impl.attention_bwd(q, k, v, do, causal=True, cu_seqlens=cu)
     assert np.max(np.abs(l2 - lse)) < 1e-12
     # D_i = sum_j P_ij dP_ij equals dO_i . O_i
     assert np.max(np.abs(D - np.einsum("thd,thd->ht", do, o))) < 1e-12
@@ -187,13 +191,13 @@ def check_backward_identities():
         assert np.max(np.abs(dv[:, g, :].sum(0) - ref)) < 1e-11
 
 
-def check_closed_forms():
+def check_closed_forms(impl=oracle):
     T, hq, hkv, d = 30, 2, 1, 4
     cu = [0, 12, 30]
     _, k, v = rand_qkv(T, hq, hkv, d, 2, with_do=False)
     q = np.zeros((T, hq, d))
     M = mask_matrix(T, cu, True)
-    o, lse = oracle.attention_fwd(q, k, v, causal=True, cu_seqlens=cu)
+    o, lse = impl.attention_fwd(q, k, v, causal=True, cu_seqlens=cu)
     for i in range(T):
         vis = np.nonzero(M[i])[0]
         for h in range(hq):
@@ -201,18 +205,18 @@ def check_closed_forms():
             assert np.max(np.abs(o[i, h] - v[vis, 0].mean(0))) < 1e-13
     # the first row of each document sees only itself
     q2, k2, v2 = rand_qkv(T, hq, hkv, d, 3, with_do=False)
-    o2, l2 = oracle.attention_fwd(q2, k2, v2, causal=True, cu_seqlens=cu)
+    o2, l2 = impl.attention_fwd(q2, k2, v2, causal=True, cu_seqlens=cu)
     for i in cu[:-1]:
         for h in range(hq):
             assert np.max(np.abs(o2[i, h] - v2[i, 0])) < 1e-13
             s = float(q2[i, h] @ k2[i, 0]) / math.sqrt(d)
             assert abs(l2[h, i] - s) < 1e-13
     # v = 1 everywhere: every row's weights sum to one, so O = 1
-    o3, _ = oracle.attention_fwd(q2, k2, np.ones_like(v2), causal=False)
+    o3, _ = impl.attention_fwd(q2, k2, np.ones_like(v2), causal=False)
     assert np.max(np.abs(o3 - 1.0)) < 1e-13
 
 
-def check_dominant_key():
+def check_dominant_key(impl=oracle):
     T, d = 16, 4
     r = np.random.default_rng(9)
     q = r.standard_normal((T, 1, d)) * 0.01
@@ -220,16 +224,16 @@ def check_dominant_key():
     v = r.standard_normal((T, 1, d))
     q[:, 0, :] += np.array([1.0, 0, 0, 0]) * 60.0
     k[5, 0, :] = np.array([1.0, 0, 0, 0]) * 60.0   # score 1800 for key 5
-    o, _ = oracle.attention_fwd(q, k, v, causal=False)
+    o, _ = impl.attention_fwd(q, k, v, causal=False)
     assert np.max(np.abs(o[:, 0, :] - v[5, 0])) < 1e-12
 
 
-def check_hand_case():
+def check_hand_case(impl=oracle):
     # D = 1, T = 2, non-causal, scale 1: q = (1, 2), k = (0.5, -1), v = (3, 5)
     q = np.array([[[1.0]], [[2.0]]])
     k = np.array([[[0.5]], [[-1.0]]])
     v = np.array([[[3.0]], [[5.0]]])
-    o, lse = oracle.attention_fwd(q, k, v, causal=False, scale=1.0)
+    o, lse = impl.attention_fwd(q, k, v, causal=False, scale=1.0)
     # row 0: scores 0.5, -1; row 1: scores 1, -2
     e = math.exp
     assert abs(o[0, 0, 0] - (3 * e(0.5) + 5 * e(-1)) / (e(0.5) + e(-1))) < 1e-14
@@ -237,7 +241,7 @@ def check_hand_case():
     assert abs(lse[0, 0] - math.log(e(0.5) + e(-1))) < 1e-14
     assert abs(lse[0, 1] - math.log(e(1) + e(-2))) < 1e-14
     # causal: row 0 sees only key 0
-    o, lse = oracle.attention_fwd(q, k, v, causal=True, scale=1.0)
+    o, lse = impl.attention_fwd(q, k, v, causal=True, scale=1.0)
     assert o[0, 0, 0] == 3.0 and lse[0, 0] == 0.5
 
 
