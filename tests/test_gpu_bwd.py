@@ -106,6 +106,17 @@ def test_bf16_backward(case, grad_fp32):
     check_full(q, k, v, do, cu, P, layout, causal, TOL_BF16_GRAD, grad_fp32=grad_fp32)
 
 
+D64_CASES = [BF16_CASES[i] for i in (0, 1, 2, 4, 5, 7, 9, 12, 13, 14, 15, 16)]
+
+
+@pytest.mark.parametrize("grad_fp32", [True, False], ids=["fp32grad", "bf16grad"])
+@pytest.mark.parametrize("case", D64_CASES, ids=[str(i) for i in range(len(D64_CASES))])
+def test_bf16_backward_head_dim_64(case, grad_fp32):
+    T, hq, hkv, P, layout, causal, cu = case
+    q, k, v, do = make_qkv(T, hq, hkv, 64, "bf16", seed=15, with_dout=True)
+    check_full(q, k, v, do, cu, P, layout, causal, TOL_BF16_GRAD, grad_fp32=grad_fp32)
+
+
 def test_bwd_layout_and_stride_invariance():
     T, hq, hkv = 2048, 8, 4
     q, k, v, do = make_qkv(T, hq, hkv, 128, "bf16", seed=6, with_dout=True)
@@ -138,7 +149,7 @@ def test_causal_gqa_fwdbwd_t65536_p8_zigzag():
 
 
 def test_bwd_unsupported_is_loud():
-    q = torch.zeros(256, 2, 64, dtype=torch.bfloat16, device=DEV)
+    q = torch.zeros(256, 2, 96, dtype=torch.bfloat16, device=DEV)
     lse = torch.zeros(2, 256, device=DEV)
     with pytest.raises(ra.RingAttnError) as e:
         ra.ringattn_bwd(q, q, q, q, lse, q, None, 2, ra.CONTIGUOUS, True)
@@ -152,3 +163,16 @@ def test_allgather_backward(case):
     q, k, v, do = make_qkv(T, hq, hkv, 128, "bf16", seed=22, with_dout=True)
     check_full(q, k, v, do, cu, P, layout, causal, TOL_BF16_GRAD, grad_fp32=True,
                exchange=ra.ALLGATHER)
+
+
+@pytest.mark.parametrize("case", [(2048, 8, 4, 2, None), (2048, 8, 4, 4, None),
+                                  (1024, 16, 8, 8, None), (2048, 4, 2, 2, [0, 300, 301, 1500, 2048])],
+                         ids=str)
+def test_ulysses_backward(case):
+    """Ulysses head sharding (all-gather exchange, heads_k_stride = Hkv / P:
+    Hkv / P key/value heads per rank, a single one in the second and third
+    case): the backward against the oracle."""
+    T, hq, hkv, P, cu = case
+    q, k, v, do = make_qkv(T, hq, hkv, 128, "bf16", seed=32, with_dout=True)
+    check_full(q, k, v, do, cu, P, ra.CONTIGUOUS, True, TOL_BF16_GRAD, hks=hkv // P,
+               grad_fp32=True, exchange=ra.ALLGATHER)
