@@ -141,8 +141,7 @@ ra_status check_problem(const int32_t* cu_seqlens, const ra_dims& d, int P, int 
   const long long parts = layout == RA_ZIGZAG ? 2LL * P : P;
   if (d.total_tokens % parts) return RA_ERR_NOT_DIVISIBLE;
   if (d.dtype != RA_BF16 && d.dtype != RA_FP32) return RA_ERR_UNSUPPORTED;
-  if (d.dtype == RA_BF16 && d.head_dim != 128) return RA_ERR_UNSUPPORTED;
-  if (d.dtype == RA_FP32 && d.head_dim != 64 && d.head_dim != 128) return RA_ERR_UNSUPPORTED;
+  if (d.head_dim != 64 && d.head_dim != 128) return RA_ERR_UNSUPPORTED;
   if ((long long)d.total_tokens * d.hq * d.head_dim >= (1LL << 40)) return RA_ERR_UNSUPPORTED;
   *in = make_input(cu_seqlens, d, P, layout, causal);
   if (!plan_check(*in).empty()) return RA_ERR_INVALID_ARG;

@@ -49,19 +49,26 @@ namespace ra {
 
 namespace {
 
-constexpr int kD = 128;
 constexpr int kTile = 128;
-constexpr int kTileBytes = kTile * kD * 2;   // 32 KB
-constexpr int kHalfBytes = kTileBytes / 2;   // 128 rows x 64 columns
-constexpr int kRowsHalf = 64 * 128;          // byte offset of row 64 in a 64-column half
+constexpr int kHalfBytes = 128 * 64 * 2;     // one box: 128 rows x 64 columns (a swizzle span)
+constexpr int kRowsHalf = 64 * 128;          // byte offset of row 64 in a 64-column box
 constexpr int kThreads = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr uint32_t kIdescN64 = make_idesc_bf16(128, 64, false, false);    // S-type, K-major B
-constexpr uint32_t kIdescMN = make_idesc_bf16(128, 128, false, true);     // X += A_tmem * B(MN)
+constexpr uint32_t kIdescN128 = make_idesc_bf16(128, 128, false, false);  // S-type, 128 keys
+
+// Per head dimension D (64 or 128): a 128 x D bf16 tile is D / 64 boxes.
+template <int kD>
+struct BwdCfg {
+  static_assert(kD == 64 || kD == 128, "head dimension");
+  static constexpr int kTileBytes = kTile * kD * 2;
+  static constexpr uint32_t kIdescMN = make_idesc_bf16(128, kD, false, true);  // X += A_tmem * B(MN)
+};
 
 // X[128 x 64] = A[128 x D] * B[64 x D]^T, both K-major; b_smem points at the
 // first of B's 64 rows inside a 128-row, 128-byte-swizzled tile.
+template <int kD>
 __device__ __forceinline__ void mma_rows_x_half(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
 #pragma unroll
   for (int kk = 0; kk < kD / 16; ++kk) {
@@ -73,19 +80,22 @@ __device__ __forceinline__ void mma_rows_x_half(uint32_t d_tmem, uint32_t a_smem
 
 // X[128 x D] (+)= A_tmem[128 x 64] * B[64 x D]; B is 64 rows (the K
 // dimension) of a 128-row tile whose D values are contiguous (MN-major).
+template <int kD>
 __device__ __forceinline__ void mma_tmem_x_rows(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
                                                 bool accumulate) {
 #pragma unroll
   for (int kk = 0; kk < 64 / 16; ++kk) {
     mma_bf16_ts(d_tmem, a_tmem + kk * 8, make_sdesc_sw128(b_smem + kk * 2048, kHalfBytes, 1024),
-                kIdescMN, (accumulate || kk > 0) ? 1u : 0u);
+                BwdCfg<kD>::kIdescMN, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
+// A 128-row tile of head `head` from row `row`: D / 64 boxes of 64 columns.
+template <int kD>
 __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
                                           int head, int row) {
-  tma_load_3d(dst, map, bar, 0, head, row);
-  tma_load_3d(dst + kHalfBytes, map, bar, 64, head, row);
+#pragma unroll
+  for (int hf = 0; hf < kD / 64; ++hf) tma_load_3d(dst + hf * kHalfBytes, map, bar, hf * 64, head, row);
 }
 
 // Stores 32 fp32 values (times `mul`) as fp32 at dst (16-byte aligned).
@@ -161,23 +171,32 @@ __device__ __forceinline__ void bwd_elementwise32(const uint32_t (&us)[32], cons
 
 // ============================================================== dK / dV
 
-constexpr int kKvStages = 2;
-constexpr int kOffK = 0;
-constexpr int kOffV = kTileBytes;
-constexpr int kOffStage = 2 * kTileBytes;                      // per stage: Q, dO
-constexpr int kStageBytes = 2 * kTileBytes;
-constexpr int kOffInfo = kOffStage + kKvStages * kStageBytes;  // per stage: row values + flags
+constexpr int kMaxKvStages = 4;
 // per stage: (-lse log2 e, -D) of the 128 query rows, interleaved by column
 // pair | their visible key ranges | 2 flags
 constexpr int kInfoBytes = 128 * sizeof(float2) + 128 * sizeof(int2) + 16;
-constexpr int kOffCtlKV = kOffInfo + kKvStages * ((kInfoBytes + 127) / 128 * 128);
-constexpr int kSmemKV = kOffCtlKV + 256 + 1024;
+constexpr int kInfoStride = (kInfoBytes + 127) / 128 * 128;
+
+template <int kD>
+struct KvCfg {
+  static constexpr int kTileBytes = BwdCfg<kD>::kTileBytes;
+  static constexpr int kKvStages = kD == 128 ? 2 : 4;         // Q/dO stages
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTileBytes;
+  static constexpr int kOffStage = 2 * kTileBytes;             // per stage: Q, dO
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kOffInfo = kOffStage + kKvStages * kStageBytes;  // per stage: row values
+  static constexpr int kOffCtlKV = kOffInfo + kKvStages * kInfoStride;
+  static constexpr int kSmemKV = kOffCtlKV + 256 + 1024;
+  static_assert(kKvStages <= kMaxKvStages, "stages");
+  static_assert(kSmemKV <= 232448, "dynamic shared memory of one CTA");
+};
 
 struct CtlKV {
   uint64_t kv_full;
-  uint64_t q_full[kKvStages];
-  uint64_t info_full[kKvStages];
-  uint64_t stage_empty[kKvStages];
+  uint64_t q_full[kMaxKvStages];
+  uint64_t info_full[kMaxKvStages];
+  uint64_t stage_empty[kMaxKvStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t acc_full;
@@ -187,10 +206,17 @@ struct CtlKV {
 };
 static_assert(sizeof(CtlKV) <= 256, "control block");
 
+template <int kD>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                     const BwdParams p) {
+  using Cfg = KvCfg<kD>;
+  constexpr int kTileBytes = Cfg::kTileBytes;
+  constexpr int kKvStages = Cfg::kKvStages;
+  constexpr int kOffK = Cfg::kOffK, kOffV = Cfg::kOffV, kOffStage = Cfg::kOffStage;
+  constexpr int kStageBytes = Cfg::kStageBytes, kOffInfo = Cfg::kOffInfo;
+  constexpr int kOffCtlKV = Cfg::kOffCtlKV;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -239,8 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&map_q);
       tma_prefetch_map(&map_do);
       mbar_arrive_expect_tx(&ctl->kv_full, 2 * kTileBytes);
-      load_tile(smem + kOffK, &map_k, &ctl->kv_full, g, it.k0);
-      load_tile(smem + kOffV, &map_v, &ctl->kv_full, g, it.k0);
+      load_tile<kD>(smem + kOffK, &map_k, &ctl->kv_full, g, it.k0);
+      load_tile<kD>(smem + kOffV, &map_v, &ctl->kv_full, g, it.k0);
       int li = 0;
       bool ok = true;
       for (int si = 0; si < it.seg_count && ok; ++si) {
@@ -255,8 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             uint8_t* st = smem + kOffStage + slot * kStageBytes;
             mbar_arrive_expect_tx(&ctl->q_full[slot], 2 * kTileBytes);
-            load_tile(st, &map_q, &ctl->q_full[slot], h, i0);
-            load_tile(st + kTileBytes, &map_do, &ctl->q_full[slot], h, i0);
+            load_tile<kD>(st, &map_q, &ctl->q_full[slot], h, i0);
+            load_tile<kD>(st + kTileBytes, &map_do, &ctl->q_full[slot], h, i0);
           }
         }
       }
@@ -287,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                    p.status, abort));
             if (!ok) break;
           }
-          uint8_t* info = smem + kOffInfo + slot * ((kInfoBytes + 127) / 128 * 128);
+          uint8_t* info = smem + kOffInfo + slot * kInfoStride;
           float* stat = reinterpret_cast<float*>(info);  // [64 pairs][nl2 a, nl2 b, nd a, nd b]
           int2* range = reinterpret_cast<int2*>(info + 128 * sizeof(float2));
           float lv[2], dv[2];
@@ -342,14 +368,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S^T and dP^T of half x of pair li
       auto issue_s = [&](int li, int x) {
         const uint32_t q = sQ(li) + x * kRowsHalf, dO = sQ(li) + kTileBytes + x * kRowsHalf;
-        mma_rows_x_half(tS[x], sK, q);
-        mma_rows_x_half(tdP[x], sV, dO);
+        mma_rows_x_half<kD>(tS[x], sK, q);
+        mma_rows_x_half<kD>(tdP[x], sV, dO);
         mma_commit(&ctl->s_full[x]);
       };
       auto issue_acc = [&](int li, int x, bool accumulate) {
         const uint32_t q = sQ(li) + x * kRowsHalf, dO = sQ(li) + kTileBytes + x * kRowsHalf;
-        mma_tmem_x_rows(tdV, tS[x], dO, accumulate);
-        mma_tmem_x_rows(tdK, tdP[x], q, accumulate);
+        mma_tmem_x_rows<kD>(tdV, tS[x], dO, accumulate);
+        mma_tmem_x_rows<kD>(tdK, tdP[x], q, accumulate);
       };
       bool ok = mbar_wait(&ctl->kv_full, 0, p.status, abort) && q_ready(0);
       if (ok) {
@@ -395,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->s_full[x], jj & 1, p.status, abort));
       if (!ok) break;
       tc_fence_after_sync();
-      const uint8_t* info = smem + kOffInfo + slot * ((kInfoBytes + 127) / 128 * 128);
+      const uint8_t* info = smem + kOffInfo + slot * kInfoStride;
       const int* flags = reinterpret_cast<const int*>(info + 128 * (sizeof(float2) + sizeof(int2)));
       const bool full = flags[0] != 0 && flags[1] != 0;
       const float4* hstat = reinterpret_cast<const float4*>(info) + x * 32;
@@ -471,24 +497,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 // tile j+1 before that wait: dS(j) therefore signals on one of two barriers
 // per warpgroup (by j % 2), so no barrier runs two phases ahead of its waiter.
 
-constexpr int kKSlots = 3;
-constexpr int kVSlots = 2;
-constexpr int kOffQ = 0;
-constexpr int kOffDO = kTileBytes;
-constexpr int kOffKq = 2 * kTileBytes;
-constexpr int kOffVq = kOffKq + kKSlots * kTileBytes;
-constexpr int kOffCtlQ = kOffVq + kVSlots * kTileBytes;
-constexpr int kSmemQ = kOffCtlQ + 256 + 1024;
-static_assert(kSmemQ <= 232448, "dynamic shared memory of one CTA");
+constexpr int kMaxKSlots = 4, kMaxVSlots = 3;
 
-constexpr uint32_t kIdescN128 = make_idesc_bf16(128, 128, false, false);
+template <int kD>
+struct QCfg {
+  static constexpr int kTileBytes = BwdCfg<kD>::kTileBytes;
+  static constexpr int kKSlots = kD == 128 ? 3 : 4;
+  static constexpr int kVSlots = kD == 128 ? 2 : 3;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDO = kTileBytes;
+  static constexpr int kOffKq = 2 * kTileBytes;
+  static constexpr int kOffVq = kOffKq + kKSlots * kTileBytes;
+  static constexpr int kOffCtlQ = kOffVq + kVSlots * kTileBytes;
+  static constexpr int kSmemQ = kOffCtlQ + 256 + 1024;
+  static_assert(kKSlots <= kMaxKSlots && kVSlots <= kMaxVSlots, "slots");
+  static_assert(kSmemQ <= 232448, "dynamic shared memory of one CTA");
+};
 
 struct CtlQ {
   uint64_t qd_full;
-  uint64_t k_full[kKSlots];
-  uint64_t k_empty[kKSlots];
-  uint64_t v_full[kVSlots];
-  uint64_t v_empty[kVSlots];
+  uint64_t k_full[kMaxKSlots];
+  uint64_t k_empty[kMaxKSlots];
+  uint64_t v_full[kMaxVSlots];
+  uint64_t v_empty[kMaxVSlots];
   uint64_t s_full[2];   // S(j) in buffer j % 2
   uint64_t dp_full;     // dP(j)
   uint64_t dp_free;     // every softmax thread has read dP(j)
@@ -501,6 +532,7 @@ struct CtlQ {
 static_assert(sizeof(CtlQ) <= 256, "control block");
 
 // X[128 x 128] = A[128 x D] * B[128 x D]^T, both K-major, 128-row tiles.
+template <int kD>
 __device__ __forceinline__ void mma_rows_x_rows(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
 #pragma unroll
   for (int kk = 0; kk < kD / 16; ++kk) {
@@ -510,10 +542,16 @@ __device__ __forceinline__ void mma_rows_x_rows(uint32_t d_tmem, uint32_t a_smem
   }
 }
 
+template <int kD>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_do,
                   const BwdParams p) {
+  using Cfg = QCfg<kD>;
+  constexpr int kTileBytes = Cfg::kTileBytes;
+  constexpr int kKSlots = Cfg::kKSlots, kVSlots = Cfg::kVSlots;
+  constexpr int kOffQ = Cfg::kOffQ, kOffDO = Cfg::kOffDO, kOffKq = Cfg::kOffKq;
+  constexpr int kOffVq = Cfg::kOffVq, kOffCtlQ = Cfg::kOffCtlQ;
   const PlanItem it = p.items[blockIdx.x >> 1];
   const bool second = (blockIdx.x & 1) != 0;  // which of the item's two query tiles
   const int qlen = second ? it.qlen[1] : it.qlen[0];
@@ -571,8 +609,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&map_k);
       tma_prefetch_map(&map_v);
       mbar_arrive_expect_tx(&ctl->qd_full, 2 * kTileBytes);
-      load_tile(smem + kOffQ, &map_q, &ctl->qd_full, head, q0);
-      load_tile(smem + kOffDO, &map_do, &ctl->qd_full, head, q0);
+      load_tile<kD>(smem + kOffQ, &map_q, &ctl->qd_full, head, q0);
+      load_tile<kD>(smem + kOffDO, &map_do, &ctl->qd_full, head, q0);
       int j = 0, nk = 0, nv = 0;  // tiles visited, K and V loads issued
       bool ok = true;
       for (int si = 0; si < it.seg_count && ok; ++si) {
@@ -585,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&ctl->k_full[ks], kTileBytes);
-          load_tile(smem + kOffKq + ks * kTileBytes, &map_k, &ctl->k_full[ks], g, kt);
+          load_tile<kD>(smem + kOffKq + ks * kTileBytes, &map_k, &ctl->k_full[ks], g, kt);
           ++nk;
           if (j >= kVSlots &&
               !mbar_wait(&ctl->v_empty[vs], ((j / kVSlots) - 1) & 1, p.status, abort)) {
@@ -593,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&ctl->v_full[vs], kTileBytes);
-          load_tile(smem + kOffVq + vs * kTileBytes, &map_v, &ctl->v_full[vs], g, kt);
+          load_tile<kD>(smem + kOffVq + vs * kTileBytes, &map_v, &ctl->v_full[vs], g, kt);
           ++nv;
         }
       }
@@ -624,11 +662,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         return mbar_wait(&ctl->v_full[j % kVSlots], (j / kVSlots) & 1, p.status, abort);
       };
       auto issue_s = [&](int j) {  // S(j) into buffer j % 2
-        mma_rows_x_rows(tS(j), sQ, sK(j));
+        mma_rows_x_rows<kD>(tS(j), sQ, sK(j));
         mma_commit(&ctl->s_full[j & 1]);
       };
       auto issue_dp = [&](int j) {  // dP(j); V(j) is then no longer needed
-        mma_rows_x_rows(tdP, sdO, sV(j));
+        mma_rows_x_rows<kD>(tdP, sdO, sV(j));
         mma_commit(&ctl->dp_full);
         mma_commit(&ctl->v_empty[j % kVSlots]);
       };
@@ -656,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait(&ctl->ds_full[w][j & 1], (j >> 1) & 1, p.status, abort))) break;
           tc_fence_after_sync();
           // dQ += dS(j)[:, 64 w : 64 w + 64] K_j[64 w : 64 w + 64, :]
-          mma_tmem_x_rows(tdQ, tS(j) + 64 * w, sK(j) + w * kRowsHalf, j > 0 || w > 0);
+          mma_tmem_x_rows<kD>(tdQ, tS(j) + 64 * w, sK(j) + w * kRowsHalf, j > 0 || w > 0);
         }
         if (!ok) break;
         mma_commit(&ctl->k_empty[j % kKSlots]);
@@ -736,13 +774,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!ok) *abort = 1;
     if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->acc_full, 0, p.status, abort));
     tc_fence_after_sync();
-    // epilogue: warpgroup w writes columns [64 w, 64 w + 64) of its row of dQ
-    const size_t off = ((size_t)row * p.hq + head) * kD + w * 64;
+    // epilogue: warpgroup w writes columns [w D / 2, (w + 1) D / 2) of its row of dQ
+    const size_t off = ((size_t)row * p.hq + head) * kD + w * (kD / 2);
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
+    for (int c = 0; c < kD / 64; ++c) {
       uint32_t u[32];
       if (ok && n > 0) {
-        tmem_load_32(tmem + lane_off + 384 + w * 64 + c * 32, u);
+        tmem_load_32(tmem + lane_off + 384 + w * (kD / 2) + c * 32, u);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) u[i] = 0u;
@@ -764,28 +802,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-bool g_dkdv_configured[64] = {};
-bool g_dq_configured[64] = {};
+template <int kD>
+cudaError_t launch_bwd_tc_bf16_d(const BwdParams& p, const CUtensorMap& map_q,
+                                 const CUtensorMap& map_k, const CUtensorMap& map_v,
+                                 const CUtensorMap& map_do, cudaStream_t stream) {
+  static bool dkdv_configured[64] = {};
+  static bool dq_configured[64] = {};
+  constexpr int smem_kv = KvCfg<kD>::kSmemKV, smem_q = QCfg<kD>::kSmemQ;
+  cudaError_t e0 = ensure_smem_limit(bwd_dkdv_kernel<kD>, smem_kv, dkdv_configured);
+  if (e0 == cudaSuccess) e0 = ensure_smem_limit(bwd_dq_kernel<kD>, smem_q, dq_configured);
+  if (e0 != cudaSuccess) return e0;
+  if (p.num_items > 0) {
+    TraceScope trace_scope(stream, "bwd_dq_kernel");
+    bwd_dq_kernel<kD><<<2 * p.num_items, kThreads, smem_q, stream>>>(map_q, map_k, map_v, map_do, p);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (p.num_bitems > 0) {
+    TraceScope trace_scope(stream, "bwd_dkdv_kernel");
+    bwd_dkdv_kernel<kD><<<p.num_bitems, kThreads, smem_kv, stream>>>(map_q, map_k, map_v, map_do, p);
+  }
+  return cudaGetLastError();
+}
 
 }  // namespace
 
 cudaError_t launch_bwd_tc_bf16(const BwdParams& p, const CUtensorMap& map_q,
                                const CUtensorMap& map_k, const CUtensorMap& map_v,
                                const CUtensorMap& map_do, cudaStream_t stream) {
-  cudaError_t e0 = ensure_smem_limit(bwd_dkdv_kernel, kSmemKV, g_dkdv_configured);
-  if (e0 == cudaSuccess) e0 = ensure_smem_limit(bwd_dq_kernel, kSmemQ, g_dq_configured);
-  if (e0 != cudaSuccess) return e0;
-  if (p.num_items > 0) {
-    TraceScope trace_scope(stream, "bwd_dq_kernel");
-    bwd_dq_kernel<<<2 * p.num_items, kThreads, kSmemQ, stream>>>(map_q, map_k, map_v, map_do, p);
-  }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (p.num_bitems > 0) {
-    TraceScope trace_scope(stream, "bwd_dkdv_kernel");
-    bwd_dkdv_kernel<<<p.num_bitems, kThreads, kSmemKV, stream>>>(map_q, map_k, map_v, map_do, p);
-  }
-  return cudaGetLastError();
+  if (p.D == 128) return launch_bwd_tc_bf16_d<128>(p, map_q, map_k, map_v, map_do, stream);
+  if (p.D == 64) return launch_bwd_tc_bf16_d<64>(p, map_q, map_k, map_v, map_do, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace ra

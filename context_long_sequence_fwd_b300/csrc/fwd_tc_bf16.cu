@@ -13,8 +13,9 @@
 // Roles (384 threads), each looping over the CTA's items:
 //   warp 0      TMA producer: Q_A, Q_B once per item (as soon as the previous
 //               item's last S MMAs have read the Q buffer), then K_j, V_j into
-//               a ring of five 32 KB shared-memory slots (128 B swizzle) that
-//               runs on across items.
+//               a ring of shared-memory slots (128 B swizzle; five 32 KB slots
+//               at head dimension 128, eight 16 KB slots at 64) that runs on
+//               across items.
 //   warp 1      allocates TMEM; one thread issues every tcgen05.mma:
 //                 S_X = Q_X K_j^T      (SS, both operands K-major)
 //                 O_X += P_X V_j       (TS: P from TMEM, V MN-major)
@@ -22,7 +23,8 @@
 //               softmax overlaps the other tile's MMAs.
 //   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: one query
 //               row per thread, read from TMEM lane (warp % 4) * 32 + lane.
-// TMEM columns: S_A 0-127, S_B 128-255, O_A 256-383, O_B 384-511.  P (bf16,
+// TMEM columns: S_A 0-127, S_B 128-255, O_A from 256, O_B from 384 (D
+// columns each, D = 64 or 128).  P (bf16,
 // two per column) overwrites the first 64 columns of its S block; tcgen05
 // MMAs of one thread execute in issue order, so S_X(j+1) cannot overwrite
 // P_X(j) before PV_X(j) has read it.  At an item boundary the next item's
@@ -51,27 +53,35 @@ namespace ra {
 
 namespace {
 
-constexpr int kD = 128;
+// Per head dimension (64 or 128): a 128 x D bf16 tile is D / 64 boxes of
+// 128 rows x 64 columns, each one 128-byte swizzle span wide.
+template <int kD>
+struct FwdCfg {
+  static constexpr int kBN = 128;                   // keys per K/V tile
+  static constexpr int kStages = kD == 128 ? 5 : 8; // K/V slots
+  static constexpr int kTileBytes = kBN * kD * 2;   // one 128 x D bf16 tile
+  static constexpr int kOffQ = 0;                   // Q_A, Q_B
+  static constexpr int kOffKV = 2 * kTileBytes;     // K/V ring
+  static constexpr int kOffCtl = kOffKV + kStages * kTileBytes;
+  static constexpr int kSmemBytes = kOffCtl + 512 + 1024;  // control block + alignment slack
+  static constexpr uint32_t kIdescQK = make_idesc_bf16(128, 128, false, false);
+  static constexpr uint32_t kIdescPV = make_idesc_bf16(128, kD, false, true);
+  static_assert(kD == 64 || kD == 128, "head dimension");
+  static_assert(kSmemBytes <= 232448, "dynamic shared memory of one CTA");
+};
+
 constexpr int kBN = 128;                     // keys per K/V tile
-constexpr int kStages = 5;                   // K/V slots
-constexpr int kTileBytes = kBN * kD * 2;     // 32 KB: one 128 x 128 bf16 tile
-constexpr int kHalfBytes = kTileBytes / 2;   // 128 rows x 64 columns (one swizzle span)
+constexpr int kHalfBytes = 128 * 64 * 2;     // 128 rows x 64 columns (one swizzle span)
+constexpr int kMaxStages = 8;
 constexpr int kThreads = 384;
-constexpr int kOffQ = 0;                     // Q_A, Q_B
-constexpr int kOffKV = 2 * kTileBytes;       // K/V ring
-constexpr int kOffCtl = kOffKV + kStages * kTileBytes;
-constexpr int kSmemBytes = kOffCtl + 256 + 1024;  // control block + alignment slack
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
 constexpr int kSchedSlots = 4;               // item indices in flight inside a CTA
-
-constexpr uint32_t kIdescQK = make_idesc_bf16(128, 128, false, false);
-constexpr uint32_t kIdescPV = make_idesc_bf16(128, 128, false, true);
 
 struct Ctl {
   uint64_t q_full;
   uint64_t q_empty;  // the item's last S MMAs have read Q
-  uint64_t kv_full[kStages];
-  uint64_t kv_empty[kStages];
+  uint64_t kv_full[kMaxStages];
+  uint64_t kv_empty[kMaxStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_full[2];
@@ -82,23 +92,25 @@ struct Ctl {
   uint32_t tmem_base;
   int abort;
 };
-static_assert(sizeof(Ctl) <= 256, "control block");
+static_assert(sizeof(Ctl) <= 512, "control block");
 
+template <int kD>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
 #pragma unroll
   for (int kk = 0; kk < kD / 16; ++kk) {
     const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
     mma_bf16_ss(d_tmem, make_sdesc_sw128(q_smem + off, 16, 1024),
-                make_sdesc_sw128(k_smem + off, 16, 1024), kIdescQK, kk > 0);
+                make_sdesc_sw128(k_smem + off, 16, 1024), FwdCfg<kD>::kIdescQK, kk > 0);
   }
 }
 
+template <int kD>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
                                          bool accumulate) {
 #pragma unroll
   for (int kk = 0; kk < kBN / 16; ++kk) {
     mma_bf16_ts(d_tmem, p_tmem + kk * 8, make_sdesc_sw128(v_smem + kk * 2048, kHalfBytes, 1024),
-                kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+                FwdCfg<kD>::kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -112,10 +124,17 @@ __device__ __forceinline__ int item_tiles(const PlanItem& it, const FwdParams& p
   return n;
 }
 
+template <int kD>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_bf16_kernel(const __grid_constant__ CUtensorMap map_q,
                        const __grid_constant__ CUtensorMap map_k,
                        const __grid_constant__ CUtensorMap map_v, const FwdParams p) {
+  using Cfg = FwdCfg<kD>;
+  constexpr int kStages = Cfg::kStages;
+  constexpr int kTileBytes = Cfg::kTileBytes;
+  constexpr int kOffQ = Cfg::kOffQ;
+  constexpr int kOffKV = Cfg::kOffKV;
+  constexpr int kOffCtl = Cfg::kOffCtl;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -209,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         mbar_arrive_expect_tx(&ctl->q_full, (has_b ? 2 : 1) * kTileBytes);
-        for (int hf = 0; hf < 2; ++hf) {
+        for (int hf = 0; hf < kD / 64; ++hf) {
           tma_load_3d(smem + kOffQ + hf * kHalfBytes, &map_q, &ctl->q_full, hf * 64, it.head[0],
                       it.q0[0]);
           if (has_b)
@@ -230,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               mbar_arrive_expect_tx(&ctl->kv_full[slot], kTileBytes);
               const CUtensorMap* map = kv == 0 ? &map_k : &map_v;
-              for (int hf = 0; hf < 2; ++hf)
+              for (int hf = 0; hf < kD / 64; ++hf)
                 tma_load_3d(smem + kOffKV + slot * kTileBytes + hf * kHalfBytes, map,
                             &ctl->kv_full[slot], hf * 64, g, kt);
             }
@@ -269,10 +288,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool has_b = it.qlen[1] > 0;
         if (!(ok = mbar_wait(&ctl->q_full, items & 1, p.status, abort) && kv_ready(li))) break;
         tc_fence_after_sync();
-        issue_qk(tS[0], sQx[0], slot_addr(li));
+        issue_qk<kD>(tS[0], sQx[0], slot_addr(li));
         mma_commit(&ctl->s_full[0]);
         if (has_b) {
-          issue_qk(tS[1], sQx[1], slot_addr(li));
+          issue_qk<kD>(tS[1], sQx[1], slot_addr(li));
           mma_commit(&ctl->s_full[1]);
         }
         mma_commit(&ctl->kv_empty[li % kStages]);
@@ -283,26 +302,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait(&ctl->p_full[0], done[0] & 1, p.status, abort))) break;
           ++done[0];
           tc_fence_after_sync();
-          issue_pv(tO[0], tS[0], slot_addr(liV), j > 0);
+          issue_pv<kD>(tO[0], tS[0], slot_addr(liV), j > 0);
           if (j == n - 1) mma_commit(&ctl->o_full[0]);
           const bool more = j + 1 < n;
           if (more) {
             if (!(ok = kv_ready(liK))) break;
             tc_fence_after_sync();
-            issue_qk(tS[0], sQx[0], slot_addr(liK));
+            issue_qk<kD>(tS[0], sQx[0], slot_addr(liK));
             mma_commit(&ctl->s_full[0]);
           }
           if (has_b) {
             if (!(ok = mbar_wait(&ctl->p_full[1], done[1] & 1, p.status, abort))) break;
             ++done[1];
             tc_fence_after_sync();
-            issue_pv(tO[1], tS[1], slot_addr(liV), j > 0);
+            issue_pv<kD>(tO[1], tS[1], slot_addr(liV), j > 0);
             if (j == n - 1) mma_commit(&ctl->o_full[1]);
           }
           mma_commit(&ctl->kv_empty[liV % kStages]);
           if (more) {
             if (has_b) {
-              issue_qk(tS[1], sQx[1], slot_addr(liK));
+              issue_qk<kD>(tS[1], sQx[1], slot_addr(liK));
               mma_commit(&ctl->s_full[1]);
             }
             mma_commit(&ctl->kv_empty[liK % kStages]);
@@ -493,20 +512,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_fwd_tc_bf16(const FwdParams& p, const CUtensorMap& map_q,
-                               const CUtensorMap& map_k, const CUtensorMap& map_v,
-                               cudaStream_t stream) {
-  if (p.num_items == 0) return cudaSuccess;
+namespace {
+
+template <int kD>
+cudaError_t launch_fwd_tc_bf16_d(const FwdParams& p, const CUtensorMap& map_q,
+                                 const CUtensorMap& map_k, const CUtensorMap& map_v,
+                                 cudaStream_t stream) {
   static bool configured[64] = {};
-  cudaError_t e = ensure_smem_limit(fwd_tc_bf16_kernel, kSmemBytes, configured);
+  constexpr int smem = FwdCfg<kD>::kSmemBytes;
+  cudaError_t e = ensure_smem_limit(fwd_tc_bf16_kernel<kD>, smem, configured);
   if (e != cudaSuccess) return e;
   // persistent: one CTA per SM (shared memory and TMEM allow no more), each
   // claiming items from the work counter; without one, one item per CTA
   const int grid = p.work_counter ? p.num_ctas : p.num_items;
   if (grid == 0) return cudaSuccess;
   TraceScope trace_scope(stream, "fwd_tc_bf16_kernel");
-  fwd_tc_bf16_kernel<<<grid, kThreads, kSmemBytes, stream>>>(map_q, map_k, map_v, p);
+  fwd_tc_bf16_kernel<kD><<<grid, kThreads, smem, stream>>>(map_q, map_k, map_v, p);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc_bf16(const FwdParams& p, const CUtensorMap& map_q,
+                               const CUtensorMap& map_k, const CUtensorMap& map_v,
+                               cudaStream_t stream) {
+  if (p.num_items == 0) return cudaSuccess;
+  if (p.D == 128) return launch_fwd_tc_bf16_d<128>(p, map_q, map_k, map_v, stream);
+  if (p.D == 64) return launch_fwd_tc_bf16_d<64>(p, map_q, map_k, map_v, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace ra

@@ -24,7 +24,7 @@ cudaError_t ensure_smem_limit(Kernel kernel, int bytes, bool (&done)[64]) {
 // fp32 forward on CUDA cores (D = 64 or 128).
 cudaError_t launch_fwd_simt_fp32(const FwdParams& p, cudaStream_t stream);
 
-// bf16 forward on tcgen05 tensor cores (D = 128).  The tensor maps describe
+// bf16 forward on tcgen05 tensor cores (D = 64 or 128).  The tensor maps describe
 // q [T, Hq, D] and k, v [T, Hkv, D] with 64 x 1 x 128 boxes, 128 B swizzle.
 cudaError_t launch_fwd_tc_bf16(const FwdParams& p, const CUtensorMap& map_q,
                                const CUtensorMap& map_k, const CUtensorMap& map_v,
@@ -41,7 +41,7 @@ cudaError_t launch_lse_merge(const void* o_a, bool a_fp32, const float* lse_a, c
 cudaError_t launch_bwd_preprocess(const void* out, const void* dout, bool fp32, float* Dvec, int T,
                                   int hq, int D, cudaStream_t stream);
 
-// bf16 backward on tcgen05 (D = 128): dQ (query-tile-major, over the forward
+// bf16 backward on tcgen05 (D = 64 or 128): dQ (query-tile-major, over the forward
 // plan) and dK, dV (key-tile-major, over the backward plan).  Tensor maps as
 // for the forward, plus dout [T, Hq, D].
 cudaError_t launch_bwd_tc_bf16(const BwdParams& p, const CUtensorMap& map_q,

@@ -92,7 +92,7 @@ typedef struct {
   int num_seqs;       /* packed documents; ignored when cu_seqlens is NULL */
   int hq;             /* query heads */
   int hkv;            /* key/value heads, divides hq */
-  int head_dim;       /* D: 64 or 128 (bf16 path: 128) */
+  int head_dim;       /* D: 64 or 128 */
   int dtype;          /* ra_dtype of q, k, v, out (and dout, dq, dk, dv) */
   int heads_k_stride; /* key/value heads per ring pass; 0 = 1 */
   int grad_fp32;      /* backward only: 1 = dq, dk, dv are fp32 whatever dtype

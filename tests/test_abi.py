@@ -62,7 +62,10 @@ def test_argument_errors_without_gpu(lib):
     assert f(None, None, None, None, dims(T=256), 3, ra.ZIGZAG, 1, None, None, None) == -2
     # heads, dtype, head_dim
     assert f(None, None, None, None, dims(hq=3, hkv=2), 1, 0, 1, None, None, None) == -1
-    assert f(None, None, None, None, dims(d=64), 1, 0, 1, None, None, None) == -3
+    assert f(None, None, None, None, dims(d=96), 1, 0, 1, None, None, None) == -3
+    assert f(None, None, None, None, dims(d=256), 1, 0, 1, None, None, None) == -3
+    # bf16 at head_dim 64 is supported: with null tensors it fails as a null argument
+    assert f(None, None, None, None, dims(d=64), 1, 0, 1, None, None, None) == -1
     assert f(None, None, None, None, dims(dtype=7), 1, 0, 1, None, None, None) == -3
     assert f(None, None, None, None, dims(hks=3, hkv=2), 1, 0, 1, None, None, None) == -1
     # null tensors with a non-empty problem
