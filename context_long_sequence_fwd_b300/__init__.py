@@ -8,6 +8,8 @@ compute function raises: there is no CPU fallback.
 
 Entry points (same names as the C ABI):
     ringattn_fwd, ringattn_fwd_stepwise, ringattn_bwd, attn_lse_merge,
+    ringattn_fwd_rank_step / ringattn_bwd_rank_step (one ring step of one rank
+    of a multi-GPU ring, on shard-local buffers; ``ring.py`` drives them),
     ringattn_get_status, plan_fwd / plan_bwd (host-only work-list
     introspection), trace_enable / trace_collect (per-kernel device time),
     ssd_cp_fwd (context-parallel Mamba2 selective scan).
@@ -107,6 +109,18 @@ def library():
                                           ctypes.c_int, _i32p, ctypes.c_int, _i32p, ctypes.c_int,
                                           _ip, _ip]
         lib.ringattn_plan_bwd.argtypes = lib.ringattn_plan_fwd.argtypes
+        lib.ringattn_fwd_rank_workspace_size.argtypes = [ra_dims, ctypes.c_int]
+        lib.ringattn_fwd_rank_workspace_size.restype = ctypes.c_size_t
+        lib.ringattn_fwd_rank_step.argtypes = [_vp, _vp, _vp, _i32p, ra_dims, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, _vp, _vp, _vp, _vp, _vp,
+                                               ctypes.c_size_t, _vp]
+        lib.ringattn_bwd_rank_workspace_size.argtypes = [ra_dims, ctypes.c_int]
+        lib.ringattn_bwd_rank_workspace_size.restype = ctypes.c_size_t
+        lib.ringattn_bwd_rank_step.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32p, ra_dims,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp,
+                                               ctypes.c_size_t, _vp]
         lib.ssd_cp_workspace_size.argtypes = [ssd_dims, ctypes.c_int]
         lib.ssd_cp_workspace_size.restype = ctypes.c_size_t
         lib.ssd_cp_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ssd_dims, ctypes.c_int,
@@ -115,6 +129,7 @@ def library():
         lib.ringattn_trace_enable.argtypes = [ctypes.c_int]
         lib.ringattn_trace_collect.argtypes = [ctypes.POINTER(ra_trace_entry), ctypes.c_int, _ip]
         for fn in ("ringattn_fwd", "ringattn_fwd_stepwise", "ringattn_bwd", "attn_lse_merge",
+                   "ringattn_fwd_rank_step", "ringattn_bwd_rank_step",
                    "ringattn_get_status", "ringattn_selftest_wait_timeout",
                    "ringattn_plan_fwd", "ringattn_plan_bwd",
                    "ringattn_trace_enable", "ringattn_trace_collect"):
@@ -262,6 +277,63 @@ def ringattn_bwd(q, k, v, out, lse, dout, cu_seqlens=None, num_shards=1,
         dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream(stream)))
     return dq, dk, dv
+
+
+def _rank_dims(q, k, total_tokens, num_seqs):
+    """Whole-problem dims from one rank's local buffers ([T / P, H, D])."""
+    _, hq, d = q.shape
+    return ra_dims(int(total_tokens), num_seqs, hq, k.shape[1], d, _dtype_code(q), 1, 1, RING)
+
+
+def fwd_rank_workspace_size(q, k, total_tokens, num_shards) -> int:
+    return int(library().ringattn_fwd_rank_workspace_size(_rank_dims(q, k, total_tokens, 0),
+                                                          int(num_shards)))
+
+
+def bwd_rank_workspace_size(q, k, total_tokens, num_shards) -> int:
+    return int(library().ringattn_bwd_rank_workspace_size(_rank_dims(q, k, total_tokens, 0),
+                                                          int(num_shards)))
+
+
+def ringattn_fwd_rank_step(q, k, v, cu_seqlens, total_tokens, num_shards, shard_layout, causal,
+                           rank, step, o_acc, lse_acc, out, lse, workspace, stream=None):
+    """One ring step of one rank on shard-local buffers (see ringattn.h)."""
+    import torch
+    _check_qkv(q, k, v)
+    Tr, hq, d = q.shape
+    ptr = lambda t: None if t is None else t.data_ptr()
+    for t, n, shp, dt in ((o_acc, "o_acc", (Tr, hq, d), torch.float32),
+                          (lse_acc, "lse_acc", (hq, Tr), torch.float32),
+                          (out, "out", (Tr, hq, d), q.dtype), (lse, "lse", (hq, Tr), torch.float32)):
+        if t is not None:
+            _need(t, n, shp, dt)
+    cu_p, nseq, _keep = _cu_host(cu_seqlens)
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("ringattn_fwd_rank_step", library().ringattn_fwd_rank_step(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), cu_p, _rank_dims(q, k, total_tokens, nseq),
+        int(num_shards), int(shard_layout), int(bool(causal)), int(rank), int(step), ptr(o_acc),
+        ptr(lse_acc), ptr(out), ptr(lse), ptr(workspace), ws, _stream(stream)))
+
+
+def ringattn_bwd_rank_step(q, k, v, out, lse, dout, cu_seqlens, total_tokens, num_shards,
+                           shard_layout, causal, rank, step, dq, dk, dv, workspace, stream=None):
+    """Backward of one ring step of one rank; fp32 dq, dk, dv (see ringattn.h)."""
+    import torch
+    _check_qkv(q, k, v)
+    Tr, hq, d = q.shape
+    _need(out, "out", q.shape, q.dtype)
+    _need(dout, "dout", q.shape, q.dtype)
+    _need(lse, "lse", (hq, Tr), torch.float32)
+    _need(dq, "dq", q.shape, torch.float32)
+    _need(dk, "dk", k.shape, torch.float32)
+    _need(dv, "dv", v.shape, torch.float32)
+    cu_p, nseq, _keep = _cu_host(cu_seqlens)
+    _check("ringattn_bwd_rank_step", library().ringattn_bwd_rank_step(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+        dout.data_ptr(), cu_p, _rank_dims(q, k, total_tokens, nseq), int(num_shards),
+        int(shard_layout), int(bool(causal)), int(rank), int(step), dq.data_ptr(),
+        dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def attn_lse_merge(o_a, lse_a, o_b, lse_b, stream=None):

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <climits>
 #include <cmath>
 #include <cstring>
 #include <list>
@@ -24,7 +25,7 @@ __device__ int g_status_word;
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr size_t kMaxCachedPlans = 32;
+constexpr size_t kMaxCachedPlans = 128;
 
 struct DeviceState {
   bool ready = false;
@@ -58,7 +59,8 @@ std::list<CachedPlan> g_plans;  // most recently used first
 bool same_key(const PlanInput& a, const PlanInput& b) {
   return a.T == b.T && a.hq == b.hq && a.hkv == b.hkv && a.num_shards == b.num_shards &&
          a.layout == b.layout && a.causal == b.causal && a.heads_k_stride == b.heads_k_stride &&
-         a.exchange == b.exchange && a.cu == b.cu;
+         a.exchange == b.exchange && a.q_rank == b.q_rank && a.k_rank == b.k_rank &&
+         a.cu == b.cu;
 }
 
 // Checks the current device once: it must be an sm_103 part.
@@ -255,7 +257,17 @@ FwdParams make_params(const void* q, const void* k, const void* v, void* out, fl
   p.step_filter = -1;
   p.out_fp32 = d.dtype == RA_FP32 ? 1 : 0;
   p.status = status;
+  p.qmap = RowMap{0, INT_MAX, 0};  // whole-sequence buffers
+  p.kmap = RowMap{0, INT_MAX, 0};
+  p.lse_stride = d.total_tokens;
   return p;
+}
+
+// Rows of rank r's shard-local buffer: its chunk(s) back to back.
+RowMap rank_rows(int T, int P, int layout, int r) {
+  int ch[2][2], n;
+  rank_chunks(T, P, layout, r, ch, &n);
+  return RowMap{ch[0][0], ch[0][1], n > 1 ? ch[1][0] : ch[0][1]};
 }
 
 struct Maps {
@@ -324,6 +336,20 @@ ra_status prepare_maps(const void* q, const void* k, const void* v, const ra_dim
       !encode_thd(&maps->k, k, d.total_tokens, d.hkv, d.head_dim) ||
       !encode_thd(&maps->v, v, d.total_tokens, d.hkv, d.head_dim))
     return RA_ERR_CUDA;
+  return RA_OK;
+}
+
+// Checks shared by the rank-step calls; fills `in` (with the step's rank
+// filters) and the shard's row count.
+ra_status check_rank_step(const int32_t* cu_seqlens, const ra_dims& dims, int P, int layout,
+                          int causal, int rank, int step, PlanInput* in, int* Tr) {
+  ra_status st = check_problem(cu_seqlens, dims, P, layout, causal, in);
+  if (st != RA_OK) return st;
+  if (dims.dtype != RA_BF16 || dims.kv_exchange != RA_RING) return RA_ERR_UNSUPPORTED;
+  if (rank < 0 || rank >= P || step < 0 || step >= P) return RA_ERR_INVALID_ARG;
+  in->q_rank = rank;
+  in->k_rank = ((rank - step) % P + P) % P;
+  *Tr = dims.total_tokens / P;
   return RA_OK;
 }
 
@@ -599,9 +625,167 @@ ra_status ringattn_bwd(const void* q, const void* k, const void* v, const void* 
   p.scale_log2 = p.scale * 1.4426950408889634f;
   p.grad_fp32 = (f32 || dims.grad_fp32) ? 1 : 0;
   p.status = ds->status;
+  p.qmap = RowMap{0, INT_MAX, 0};
+  p.kmap = RowMap{0, INT_MAX, 0};
+  p.lse_stride = dims.total_tokens;
+  p.accumulate = 0;
   cudaError_t e = f32 ? launch_bwd_simt_fp32(p, s)
                       : launch_bwd_tc_bf16(p, maps.q, maps.k, maps.v, map_do, s);
   if (e != cudaSuccess) return RA_ERR_CUDA;
+  if (cudaEventRecord(cp->last_use, s) != cudaSuccess) return RA_ERR_CUDA;
+  return RA_OK;
+}
+
+// ---------------------------------------------------------------------------
+// One ring step of one rank, on shard-local buffers (the multi-GPU ring: each
+// GPU holds its own query rows and receives the K/V shard of rank
+// (rank - step) mod P into its own memory before the step).
+// ---------------------------------------------------------------------------
+
+size_t ringattn_fwd_rank_workspace_size(ra_dims dims, int num_shards) {
+  if (dims.total_tokens < 0 || dims.hq < 1 || dims.head_dim < 1 || num_shards < 1) return 0;
+  ra_dims r = dims;
+  r.total_tokens = dims.total_tokens / num_shards;
+  return fp32_o_bytes(r) + lse_bytes(r);
+}
+
+ra_status ringattn_fwd_rank_step(const void* q, const void* k, const void* v,
+                                 const int32_t* cu_seqlens, ra_dims dims, int num_shards,
+                                 int shard_layout, int causal, int rank, int step, float* o_acc,
+                                 float* lse_acc, void* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  PlanInput in;
+  int Tr = 0;
+  ra_status st = check_rank_step(cu_seqlens, dims, num_shards, shard_layout, causal, rank, step,
+                                 &in, &Tr);
+  if (st != RA_OK) return st;
+  if (dims.total_tokens == 0) return RA_OK;
+  const bool first = step == 0, last = step == num_shards - 1;
+  if (!q || !k || !v || !aligned16(q) || !aligned16(k) || !aligned16(v)) return RA_ERR_INVALID_ARG;
+  if (!(first && last) && (!o_acc || !lse_acc || !aligned16(o_acc))) return RA_ERR_INVALID_ARG;
+  if (last && (!out || !lse || !aligned16(out))) return RA_ERR_INVALID_ARG;
+  if (!first && (!workspace || !aligned16(workspace) ||
+                 workspace_bytes < ringattn_fwd_rank_workspace_size(dims, num_shards)))
+    return RA_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev;
+  DeviceState* ds;
+  if ((st = current_device(&dev, &ds)) != RA_OK) return st;
+  Maps maps;
+  if (!encode_thd(&maps.q, q, Tr, dims.hq, dims.head_dim) ||
+      !encode_thd(&maps.k, k, Tr, dims.hkv, dims.head_dim) ||
+      !encode_thd(&maps.v, v, Tr, dims.hkv, dims.head_dim))
+    return RA_ERR_CUDA;
+  CachedPlan* cp;
+  if ((st = get_plan(dev, in, static_cast<cudaStream_t>(stream), &cp)) != RA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ra_dims rd = dims;
+  rd.total_tokens = Tr;
+  float* stp_o = static_cast<float*>(workspace);
+  float* stp_l = reinterpret_cast<float*>(static_cast<char*>(workspace) + fp32_o_bytes(rd));
+  // the step's partial result: straight to the output when it is the only
+  // step, to the running result when it starts it, else to the workspace
+  void* o_dst = first ? (last ? out : static_cast<void*>(o_acc)) : stp_o;
+  float* l_dst = first ? (last ? lse : lse_acc) : stp_l;
+  FwdParams p = make_params(q, k, v, o_dst, l_dst, dims, causal, *cp, ds->status);
+  p.qmap = rank_rows(dims.total_tokens, num_shards, shard_layout, rank);
+  p.kmap = rank_rows(dims.total_tokens, num_shards, shard_layout, in.k_rank);
+  p.lse_stride = Tr;
+  p.out_fp32 = (first && last) ? 0 : 1;
+  // every query tile of the rank is an item (one CTA each); a tile that sees
+  // no key of this shard writes O = 0, lse = -inf
+  if ((st = launch_fwd(p, dims, &maps, s)) != RA_OK) return st;
+  if (!first) {
+    if (launch_lse_merge(o_acc, true, lse_acc, stp_o, true, stp_l,
+                         last ? out : static_cast<void*>(o_acc), last ? false : true,
+                         last ? lse : lse_acc, Tr, dims.hq, dims.head_dim, s) != cudaSuccess)
+      return RA_ERR_CUDA;
+  }
+  if (cudaEventRecord(cp->last_use, s) != cudaSuccess) return RA_ERR_CUDA;
+  return RA_OK;
+}
+
+size_t ringattn_bwd_rank_workspace_size(ra_dims dims, int num_shards) {
+  if (dims.total_tokens < 0 || dims.hq < 1 || dims.head_dim < 1 || num_shards < 1) return 0;
+  ra_dims r = dims;
+  r.total_tokens = dims.total_tokens / num_shards;
+  return lse_bytes(r);  // D_i = dO_i . O_i of the rank's rows, fp32 [Hq, Tr]
+}
+
+ra_status ringattn_bwd_rank_step(const void* q, const void* k, const void* v, const void* out,
+                                 const float* lse, const void* dout, const int32_t* cu_seqlens,
+                                 ra_dims dims, int num_shards, int shard_layout, int causal,
+                                 int rank, int step, float* dq, float* dk, float* dv,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+  PlanInput in;
+  int Tr = 0;
+  ra_status st = check_rank_step(cu_seqlens, dims, num_shards, shard_layout, causal, rank, step,
+                                 &in, &Tr);
+  if (st != RA_OK) return st;
+  if (dims.total_tokens == 0) return RA_OK;
+  for (const void* t : {q, k, v, out, dout, static_cast<const void*>(dq),
+                        static_cast<const void*>(dk), static_cast<const void*>(dv)})
+    if (!t || !aligned16(t)) return RA_ERR_INVALID_ARG;
+  if (!lse) return RA_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) ||
+      workspace_bytes < ringattn_bwd_rank_workspace_size(dims, num_shards))
+    return RA_ERR_WORKSPACE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  int dev;
+  DeviceState* ds;
+  if ((st = current_device(&dev, &ds)) != RA_OK) return st;
+  Maps maps;
+  CUtensorMap map_do;
+  if (!encode_thd(&maps.q, q, Tr, dims.hq, dims.head_dim) ||
+      !encode_thd(&maps.k, k, Tr, dims.hkv, dims.head_dim) ||
+      !encode_thd(&maps.v, v, Tr, dims.hkv, dims.head_dim) ||
+      !encode_thd(&map_do, dout, Tr, dims.hq, dims.head_dim))
+    return RA_ERR_CUDA;
+  CachedPlan* cp;
+  if ((st = get_plan(dev, in, static_cast<cudaStream_t>(stream), &cp)) != RA_OK) return st;
+  if ((st = get_bwd_plan(cp)) != RA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* Dvec = static_cast<float*>(workspace);
+  // step 0 computes the rank's D_i once; the caller keeps the workspace
+  // for the later steps
+  if (step == 0 &&
+      launch_bwd_preprocess(out, dout, false, Dvec, Tr, dims.hq, dims.head_dim, s) != cudaSuccess)
+    return RA_ERR_CUDA;
+  BwdParams p{};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.dout = dout;
+  p.lse = lse;
+  p.Dvec = Dvec;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.items = cp->items;
+  p.segs = cp->segs;
+  p.bitems = cp->bitems;
+  p.bsegs = cp->bsegs;
+  p.cu = cp->cu;
+  p.num_docs = static_cast<int>(cp->plan.cu.size()) - 1;
+  p.num_items = static_cast<int>(cp->plan.items.size());
+  p.num_bitems = static_cast<int>(cp->bwd.items.size());
+  p.T = dims.total_tokens;
+  p.hq = dims.hq;
+  p.hkv = dims.hkv;
+  p.D = dims.head_dim;
+  p.group = dims.hq / dims.hkv;
+  p.causal = causal ? 1 : 0;
+  p.scale = 1.0f / std::sqrt(static_cast<float>(dims.head_dim));
+  p.scale_log2 = p.scale * 1.4426950408889634f;
+  p.grad_fp32 = 1;
+  p.status = ds->status;
+  p.qmap = rank_rows(dims.total_tokens, num_shards, shard_layout, rank);
+  p.kmap = rank_rows(dims.total_tokens, num_shards, shard_layout, in.k_rank);
+  p.lse_stride = Tr;
+  // step 0 starts dq (this rank's rows) and dk, dv (its own keys, which
+  // then travel the ring); later steps add to them
+  p.accumulate = step == 0 ? 0 : 1;
+  if (launch_bwd_tc_bf16(p, maps.q, maps.k, maps.v, map_do, s) != cudaSuccess) return RA_ERR_CUDA;
   if (cudaEventRecord(cp->last_use, s) != cudaSuccess) return RA_ERR_CUDA;
   return RA_OK;
 }

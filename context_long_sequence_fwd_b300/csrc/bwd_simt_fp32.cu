@@ -44,8 +44,8 @@ __global__ void __launch_bounds__(256) bwd_dq_simt_kernel(BwdParams p) {
     doc_bounds(p.cu, p.num_docs, row, &ds, &de);
     lo = ds;
     hi = p.causal ? row + 1 : de;
-    lse = p.lse[(size_t)h * p.T + row];
-    Dv = p.Dvec[(size_t)h * p.T + row];
+    lse = p.lse[(size_t)h * p.lse_stride + row];
+    Dv = p.Dvec[(size_t)h * p.lse_stride + row];
   }
 #pragma unroll
   for (int d = 0; d < D; ++d) {
@@ -132,8 +132,8 @@ __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(BwdParams p) {
             doc_bounds(p.cu, p.num_docs, i, &ds, &de);
             lo = ds;
             hi = p.causal ? i + 1 : de;
-            l = p.lse[(size_t)h * p.T + i];
-            dd = p.Dvec[(size_t)h * p.T + i];
+            l = p.lse[(size_t)h * p.lse_stride + i];
+            dd = p.Dvec[(size_t)h * p.lse_stride + i];
           }
           Lo[threadIdx.x] = lo;
           Hi[threadIdx.x] = hi;

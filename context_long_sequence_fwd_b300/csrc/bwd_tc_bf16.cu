@@ -107,6 +107,21 @@ __device__ __forceinline__ void store_f32x32(float* dst, const uint32_t (&u)[32]
                        __uint_as_float(u[4 * i + 2]) * mul, __uint_as_float(u[4 * i + 3]) * mul);
 }
 
+// Adds 32 fp32 values (times `mul`) into fp32 dst (16-byte aligned); each
+// element has one writer per launch, so no atomics are needed.
+__device__ __forceinline__ void add_f32x32(float* dst, const uint32_t (&u)[32], float mul) {
+  float4* d = reinterpret_cast<float4*>(dst);
+  float4 old[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) old[i] = d[i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    d[i] = make_float4(old[i].x + __uint_as_float(u[4 * i]) * mul,
+                       old[i].y + __uint_as_float(u[4 * i + 1]) * mul,
+                       old[i].z + __uint_as_float(u[4 * i + 2]) * mul,
+                       old[i].w + __uint_as_float(u[4 * i + 3]) * mul);
+}
+
 // Stores 32 fp32 values (times `mul`) as bf16 at dst (16-byte aligned).
 __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t (&u)[32], float mul) {
   uint4* d = reinterpret_cast<uint4*>(dst);
@@ -265,8 +280,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&map_q);
       tma_prefetch_map(&map_do);
       mbar_arrive_expect_tx(&ctl->kv_full, 2 * kTileBytes);
-      load_tile<kD>(smem + kOffK, &map_k, &ctl->kv_full, g, it.k0);
-      load_tile<kD>(smem + kOffV, &map_v, &ctl->kv_full, g, it.k0);
+      const int k0l = local_row(p.kmap, it.k0);
+      load_tile<kD>(smem + kOffK, &map_k, &ctl->kv_full, g, k0l);
+      load_tile<kD>(smem + kOffV, &map_v, &ctl->kv_full, g, k0l);
       int li = 0;
       bool ok = true;
       for (int si = 0; si < it.seg_count && ok; ++si) {
@@ -281,8 +297,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             uint8_t* st = smem + kOffStage + slot * kStageBytes;
             mbar_arrive_expect_tx(&ctl->q_full[slot], 2 * kTileBytes);
-            load_tile<kD>(st, &map_q, &ctl->q_full[slot], h, i0);
-            load_tile<kD>(st + kTileBytes, &map_do, &ctl->q_full[slot], h, i0);
+            const int i0l = local_row(p.qmap, i0);
+            load_tile<kD>(st, &map_q, &ctl->q_full[slot], h, i0l);
+            load_tile<kD>(st + kTileBytes, &map_do, &ctl->q_full[slot], h, i0l);
           }
         }
       }
@@ -321,8 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 2; ++k) {
             const int i = i0 + rbase + lane + 32 * k;
             const bool valid = i < sg.q1;
-            lv[k] = valid ? p.lse[(size_t)h * p.T + i] : 0.f;
-            dv[k] = valid ? p.Dvec[(size_t)h * p.T + i] : 0.f;
+            const size_t at = (size_t)h * p.lse_stride + (valid ? local_row(p.qmap, i) : 0);
+            lv[k] = valid ? p.lse[at] : 0.f;
+            dv[k] = valid ? p.Dvec[at] : 0.f;
           }
           bool full = true;
 #pragma unroll
@@ -449,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     // epilogue: half 0 writes dV, half 1 writes dK (times the softmax scale)
     const uint32_t tAcc = tmem + lane_off + (x == 0 ? 256 : 384);
-    const size_t off = ((size_t)j * p.hkv + g) * kD;
+    const size_t off = ((size_t)local_row(p.kmap, j) * p.hkv + g) * kD;
     void* dst = x == 0 ? p.dv : p.dk;
     const float mul = x == 0 ? 1.f : p.scale;
 #pragma unroll
@@ -462,7 +480,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 32; ++i) u[i] = 0u;
       }
       if (ok && kr < it.klen) {
-        if (p.grad_fp32)
+        if (p.accumulate)
+          add_f32x32(static_cast<float*>(dst) + off + c * 32, u, mul);
+        else if (p.grad_fp32)
           store_f32x32(static_cast<float*>(dst) + off + c * 32, u, mul);
         else
           store_bf16x32(static_cast<__nv_bfloat16*>(dst) + off + c * 32, u, mul);
@@ -609,8 +629,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&map_k);
       tma_prefetch_map(&map_v);
       mbar_arrive_expect_tx(&ctl->qd_full, 2 * kTileBytes);
-      load_tile<kD>(smem + kOffQ, &map_q, &ctl->qd_full, head, q0);
-      load_tile<kD>(smem + kOffDO, &map_do, &ctl->qd_full, head, q0);
+      const int q0l = local_row(p.qmap, q0);
+      load_tile<kD>(smem + kOffQ, &map_q, &ctl->qd_full, head, q0l);
+      load_tile<kD>(smem + kOffDO, &map_do, &ctl->qd_full, head, q0l);
       int j = 0, nk = 0, nv = 0;  // tiles visited, K and V loads issued
       bool ok = true;
       for (int si = 0; si < it.seg_count && ok; ++si) {
@@ -623,7 +644,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&ctl->k_full[ks], kTileBytes);
-          load_tile<kD>(smem + kOffKq + ks * kTileBytes, &map_k, &ctl->k_full[ks], g, kt);
+          load_tile<kD>(smem + kOffKq + ks * kTileBytes, &map_k, &ctl->k_full[ks], g,
+                        local_row(p.kmap, kt));
           ++nk;
           if (j >= kVSlots &&
               !mbar_wait(&ctl->v_empty[vs], ((j / kVSlots) - 1) & 1, p.status, abort)) {
@@ -631,7 +653,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&ctl->v_full[vs], kTileBytes);
-          load_tile<kD>(smem + kOffVq + vs * kTileBytes, &map_v, &ctl->v_full[vs], g, kt);
+          load_tile<kD>(smem + kOffVq + vs * kTileBytes, &map_v, &ctl->v_full[vs], g,
+                        local_row(p.kmap, kt));
           ++nv;
         }
       }
@@ -724,8 +747,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       doc_bounds(p.cu, p.num_docs, row, &ds, &de);
       lo = ds;
       hi = p.causal ? row + 1 : de;
-      lse2 = p.lse[(size_t)head * p.T + row] * kLog2e;
-      Dv = p.Dvec[(size_t)head * p.T + row];
+      const size_t at = (size_t)head * p.lse_stride + local_row(p.qmap, row);
+      lse2 = p.lse[at] * kLog2e;
+      Dv = p.Dvec[at];
     }
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tdP = tmem + lane_off + 256 + 64 * w;
@@ -775,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->acc_full, 0, p.status, abort));
     tc_fence_after_sync();
     // epilogue: warpgroup w writes columns [w D / 2, (w + 1) D / 2) of its row of dQ
-    const size_t off = ((size_t)row * p.hq + head) * kD + w * (kD / 2);
+    const size_t off = ((size_t)(valid ? local_row(p.qmap, row) : 0) * p.hq + head) * kD + w * (kD / 2);
 #pragma unroll
     for (int c = 0; c < kD / 64; ++c) {
       uint32_t u[32];
@@ -786,7 +810,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 32; ++i) u[i] = 0u;
       }
       if (ok && valid) {
-        if (p.grad_fp32)
+        if (p.accumulate)
+          add_f32x32(static_cast<float*>(p.dq) + off + c * 32, u, p.scale);
+        else if (p.grad_fp32)
           store_f32x32(static_cast<float*>(p.dq) + off + c * 32, u, p.scale);
         else
           store_bf16x32(static_cast<__nv_bfloat16*>(p.dq) + off + c * 32, u, p.scale);

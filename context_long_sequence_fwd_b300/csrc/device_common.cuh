@@ -7,6 +7,19 @@
 
 namespace ra {
 
+// Where global token t lives in a buffer: chunk [a0, b0) holds rows
+// [0, b0 - a0) and chunk [a1, ...) the rows after them.  Whole-sequence
+// buffers use the identity (a0 = 0, b0 = INT_MAX); one rank's shard-local
+// buffer of a multi-GPU ring holds its chunk(s) back to back (ZIGZAG: chunk r,
+// then chunk 2P-1-r).  Masks always use global positions; loads, stores and
+// lse rows use the buffer's rows.
+struct RowMap {
+  int a0, b0, a1;
+};
+__device__ __forceinline__ int local_row(const RowMap& m, int t) {
+  return t < m.b0 ? t - m.a0 : t - m.a1 + (m.b0 - m.a0);
+}
+
 struct FwdParams {
   const void* q;          // [T, Hq, D]
   const void* k;          // [T, Hkv, D]
@@ -29,6 +42,9 @@ struct FwdParams {
   int step_filter;        // -1: every ring step; s >= 0: only segments of step s
   int out_fp32;           // 1: out is fp32, 0: out is bf16
   int* status;            // device status word (first error wins)
+  RowMap qmap;            // rows of q, out and lse (identity: whole sequence)
+  RowMap kmap;            // rows of k and v
+  int lse_stride;         // rows per head of lse: [Hq, lse_stride]
 };
 
 struct BwdParams {
@@ -55,6 +71,10 @@ struct BwdParams {
   float scale_log2;         // scale * log2(e)
   int grad_fp32;            // 1: dq, dk, dv are fp32, else bf16
   int* status;
+  RowMap qmap;              // rows of q, dout, dq, lse and Dvec (identity: whole sequence)
+  RowMap kmap;              // rows of k, v, dk and dv
+  int lse_stride;           // rows per head of lse and Dvec
+  int accumulate;           // 1: add into fp32 dq, dk, dv instead of writing them
 };
 
 // Context-parallel selective scan (Mamba2 SSD), fp32.

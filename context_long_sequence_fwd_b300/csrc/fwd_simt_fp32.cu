@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(256) fwd_simt_fp32_kernel(FwdParams p) {
 #pragma unroll
     for (int d = 0; d < D; ++d) out[ob + d] = __float2bfloat16_rn(empty ? 0.f : o[d] / l);
   }
-  p.lse[(size_t)h * p.T + row] = empty ? -INFINITY : m + logf(l);
+  p.lse[(size_t)h * p.lse_stride + row] = empty ? -INFINITY : m + logf(l);
 }
 
 }  // namespace

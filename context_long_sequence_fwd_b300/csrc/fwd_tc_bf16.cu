@@ -228,12 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         mbar_arrive_expect_tx(&ctl->q_full, (has_b ? 2 : 1) * kTileBytes);
+        const int qa = local_row(p.qmap, it.q0[0]), qb = local_row(p.qmap, it.q0[1]);
         for (int hf = 0; hf < kD / 64; ++hf) {
           tma_load_3d(smem + kOffQ + hf * kHalfBytes, &map_q, &ctl->q_full, hf * 64, it.head[0],
-                      it.q0[0]);
+                      qa);
           if (has_b)
             tma_load_3d(smem + kOffQ + kTileBytes + hf * kHalfBytes, &map_q, &ctl->q_full,
-                        hf * 64, it.head[1], it.q0[1]);
+                        hf * 64, it.head[1], qb);
         }
         ++items;
         for (int si = 0; si < it.seg_count && ok; ++si) {
@@ -251,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const CUtensorMap* map = kv == 0 ? &map_k : &map_v;
               for (int hf = 0; hf < kD / 64; ++hf)
                 tma_load_3d(smem + kOffKV + slot * kTileBytes + hf * kHalfBytes, map,
-                            &ctl->kv_full[slot], hf * 64, g, kt);
+                            &ctl->kv_full[slot], hf * 64, g, local_row(p.kmap, kt));
             }
           }
         }
@@ -458,7 +459,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------------------------------- epilogue
       const bool empty = !(l > 0.f);
       const float inv_l = empty ? 0.f : 1.f / l;
-      const size_t ob = ((size_t)row * p.hq + head) * kD;
+      const int lrow = local_row(p.qmap, row);
+      const size_t ob = ((size_t)lrow * p.hq + head) * kD;
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t u[32];
@@ -493,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (valid)
-        p.lse[(size_t)head * p.T + row] =
+        p.lse[(size_t)head * p.lse_stride + lrow] =
             empty ? -INFINITY : (m2 + log2f(l)) * 0.69314718055994530942f;
       // the epilogue's TMEM reads precede the next item's first P (and with
       // it the PV MMA that overwrites O)

@@ -38,6 +38,11 @@ std::string plan_check(const PlanInput& in) {
   if (in.layout != 0 && in.layout != 1) return "unknown shard layout";
   if (in.heads_k_stride < 1 || in.hkv % in.heads_k_stride) return "heads_k_stride must divide hkv";
   if (in.exchange != 0 && in.exchange != 1) return "unknown K/V exchange";
+  if (in.q_rank < -1 || in.q_rank >= in.num_shards || in.k_rank < -1 ||
+      in.k_rank >= in.num_shards)
+    return "rank out of range";
+  if ((in.q_rank >= 0 || in.k_rank >= 0) && in.exchange != 0)
+    return "a single ring step needs the ring exchange";
   if (in.cu.size() < 2) return "cu_seqlens needs at least two entries";
   if (in.cu.front() != 0 || in.cu.back() != in.T) return "cu_seqlens must run from 0 to T";
   for (size_t i = 1; i < in.cu.size(); ++i)
@@ -73,6 +78,7 @@ Plan build_fwd_plan(const PlanInput& in) {
     const size_t first_item = plan.items.size();
     for (int g = pass * in.heads_k_stride; g < (pass + 1) * in.heads_k_stride; ++g) {
       for (int r = 0; r < P; ++r) {
+        if (in.q_rank >= 0 && r != in.q_rank) continue;
         int qch[2][2], nq;
         rank_chunks(in.T, P, in.layout, r, qch, &nq);
         for (int c = 0; c < nq; ++c) {
@@ -117,6 +123,7 @@ Plan build_fwd_plan(const PlanInput& in) {
               } else {
                 for (int s = 0; s < P; ++s) {
                   const int src = ((r - s) % P + P) % P;
+                  if (in.k_rank >= 0 && src != in.k_rank) continue;
                   int kch[2][2], nk;
                   rank_chunks(in.T, P, in.layout, src, kch, &nk);
                   for (int kc = 0; kc < nk; ++kc) {
@@ -154,6 +161,7 @@ BwdPlan build_bwd_plan(const PlanInput& in) {
     const size_t first_item = plan.items.size();
     for (int g = pass * in.heads_k_stride; g < (pass + 1) * in.heads_k_stride; ++g) {
       for (int src = 0; src < P; ++src) {
+        if (in.k_rank >= 0 && src != in.k_rank) continue;
         int kch[2][2], nk;
         rank_chunks(in.T, P, in.layout, src, kch, &nk);
         for (int c = 0; c < nk; ++c) {
@@ -180,6 +188,7 @@ BwdPlan build_bwd_plan(const PlanInput& in) {
             } else {
               for (int s = 0; s < P; ++s) {
                 const int r = (src + s) % P;
+                if (in.q_rank >= 0 && r != in.q_rank) continue;
                 int qch[2][2], nq;
                 rank_chunks(in.T, P, in.layout, r, qch, &nq);
                 for (int qc = 0; qc < nq; ++qc) {

@@ -42,6 +42,9 @@ struct PlanInput {
   int num_shards = 1, layout = 0, causal = 0, heads_k_stride = 1;
   int exchange = 0;  // 0: ring order of K/V shards; 1: all-gathered, token order
   std::vector<int32_t> cu;  // num_docs + 1 offsets (always filled: one doc if none given)
+  // One ring step of one rank (multi-GPU form): only the queries of rank
+  // q_rank and only the keys of rank k_rank (-1: every rank).  Ring exchange only.
+  int q_rank = -1, k_rank = -1;
 };
 
 struct Plan {

@@ -178,6 +178,61 @@ ra_status ringattn_bwd(const void* q, const void* k, const void* v, const void* 
                        void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * One ring step of one rank of a MULTI-GPU ring, on shard-local buffers.
+ * The pages' deployment of ring attention puts one rank on each GPU: the rank
+ * keeps its own query rows, and the K/V blocks rotate around the ring so that
+ * no device ever holds the whole sequence (aicassindra "tm_sp_math", "Context
+ * parallelism is the axis that is independent"; axolotl "Sequence
+ * Parallelism" page, introduction and "Implementation Details": results are
+ * aggregated through a ring communication pattern).  The caller moves the
+ * K/V shards between GPUs (into this GPU's own memory) and calls one step per
+ * shard; these calls do the step's attention and fold it into the rank's
+ * running result.  bf16 only, RA_RING exchange only (else RA_ERR_UNSUPPORTED).
+ *   - dims describe the WHOLE problem (total_tokens = T, cu_seqlens of the
+ *     whole sequence, host array); Tr = T / num_shards rows per rank.
+ *   - rank r's buffers hold its rows back to back: CONTIGUOUS tokens
+ *     [r Tr, (r+1) Tr); ZIGZAG chunk r then chunk 2P-1-r (each Tr / 2 tokens).
+ *   - step s (0 .. P-1) is the step at which rank r holds the K/V shard of
+ *     rank src = (r - s) mod P; k, v are that shard's rows [Tr, Hkv, D], laid
+ *     out as src's own buffers.  Steps must be called in order s = 0 .. P-1
+ *     on one stream.  Masks use global positions, so causal and document
+ *     masks are exact; a shard the rank cannot see (causal, src > r with
+ *     CONTIGUOUS) gives an all-masked partial that the merge ignores.
+ *
+ * Forward: q [Tr, Hq, D]; o_acc fp32 [Tr, Hq, D] and lse_acc fp32 [Hq, Tr]
+ * hold the running result between steps (unused when P = 1); the last step
+ * (s = P-1) writes out [Tr, Hq, D] bf16 and lse [Hq, Tr] (natural log).
+ * Steps after the first need a device workspace of
+ * ringattn_fwd_rank_workspace_size(dims, num_shards) bytes (one step's fp32
+ * partial result).
+ */
+size_t ringattn_fwd_rank_workspace_size(ra_dims dims, int num_shards);
+ra_status ringattn_fwd_rank_step(const void* q, const void* k, const void* v,
+                                 const int32_t* cu_seqlens, ra_dims dims, int num_shards,
+                                 int shard_layout, int causal, int rank, int step, float* o_acc,
+                                 float* lse_acc, void* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
+ * Backward of one ring step of one rank (same conventions as
+ * ringattn_fwd_rank_step).  q, out, lse, dout are the rank's own rows (out
+ * and lse from its forward); k, v the K/V shard it holds at step s.  The
+ * gradients are fp32: dq [Tr, Hq, D] of the rank's rows; dk, dv [Tr, Hkv, D]
+ * of the keys of rank src, which travel around the ring with k and v.  Step 0
+ * (src = rank) writes dq and the rank's own dk, dv; every later step adds to
+ * them, so after step P-1 dq is complete and the dk, dv the rank holds (those
+ * of rank (rank + 1) mod P) are complete and go back to their owner.  The
+ * workspace (ringattn_bwd_rank_workspace_size bytes: D_i = dout_i . out_i of
+ * the rank's rows) is filled by step 0 and must be kept for the later steps.
+ */
+size_t ringattn_bwd_rank_workspace_size(ra_dims dims, int num_shards);
+ra_status ringattn_bwd_rank_step(const void* q, const void* k, const void* v, const void* out,
+                                 const float* lse, const void* dout, const int32_t* cu_seqlens,
+                                 ra_dims dims, int num_shards, int shard_layout, int causal,
+                                 int rank, int step, float* dq, float* dk, float* dv,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Log-sum-exp merge of two partial attention results over disjoint key sets,
  * in place into (o_a, lse_a) -- how the pages' ring steps are aggregated
  * (axolotl page, introduction).  Per row:

@@ -96,3 +96,25 @@ def test_trace_without_launches(lib):
     ra.trace_enable(False)
     n = ctypes.c_int(-1)
     assert lib.ringattn_trace_collect(None, -1, ctypes.byref(n)) == -1
+
+
+def test_rank_step_argument_errors_without_gpu(lib):
+    """One ring step of one rank (multi-GPU form): bf16 and the ring exchange
+    only, rank and step inside the ring, a workspace for the steps that merge."""
+    f = lib.ringattn_fwd_rank_step
+    ws = lib.ringattn_fwd_rank_workspace_size(dims(T=256), 2)
+    assert ws >= 128 * 2 * 128 * 4 + 2 * 128 * 4
+    assert lib.ringattn_bwd_rank_workspace_size(dims(T=256), 2) >= 2 * 128 * 4
+    assert f(16, 16, 16, None, dims(dtype=ra.RA_FP32), 2, 0, 1, 0, 0, 16, 16, 16, 16, 16, ws,
+             None) == -3
+    assert f(16, 16, 16, None, dims(), 2, 0, 1, 2, 0, 16, 16, 16, 16, 16, ws, None) == -1
+    assert f(16, 16, 16, None, dims(), 2, 0, 1, 0, 2, 16, 16, 16, 16, 16, ws, None) == -1
+    assert f(16, 16, 16, None, dims(T=250), 4, 0, 1, 0, 0, 16, 16, 16, 16, 16, ws, None) == -2
+    # a step after the first merges through the workspace
+    assert f(16, 16, 16, None, dims(), 2, 0, 1, 0, 1, 16, 16, 16, 16, None, 0, None) == -6
+    d = dims()
+    d.kv_exchange = 1
+    assert f(16, 16, 16, None, d, 2, 0, 1, 0, 0, 16, 16, 16, 16, 16, ws, None) == -3
+    b = lib.ringattn_bwd_rank_step
+    assert b(16, 16, 16, 16, 16, 16, None, dims(), 2, 0, 1, 0, 0, 16, 16, 16, None, 0,
+             None) == -6
