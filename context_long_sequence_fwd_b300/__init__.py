@@ -37,7 +37,7 @@ PLAN_ITEM_FIELDS = 16
 PLAN_SEG_FIELDS = 4
 ITEM_COLUMNS = ("q0_a", "q0_b", "qlen_a", "qlen_b", "head_a", "head_b", "seg_begin",
                 "seg_count", "rank", "cost", "mask_lo_a", "mask_lo_b", "mask_hi_a",
-                "mask_hi_b", "pass", "pad")
+                "mask_hi_b", "pass", "part")
 SEG_COLUMNS = ("k0", "k1", "step", "src")
 PLAN_BWD_ITEM_FIELDS = 8
 BWD_ITEM_COLUMNS = ("k0", "klen", "kv_head", "src", "seg_begin", "seg_count", "cost", "pad")
@@ -109,6 +109,9 @@ def library():
                                           ctypes.c_int, _i32p, ctypes.c_int, _i32p, ctypes.c_int,
                                           _ip, _ip]
         lib.ringattn_plan_bwd.argtypes = lib.ringattn_plan_fwd.argtypes
+        lib.ringattn_plan_fwd_fused.argtypes = [_i32p, ra_dims, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_int, _i32p, ctypes.c_int,
+                                                _i32p, ctypes.c_int, _ip, _ip]
         lib.ringattn_fwd_rank_workspace_size.argtypes = [ra_dims, ctypes.c_int]
         lib.ringattn_fwd_rank_workspace_size.restype = ctypes.c_size_t
         lib.ringattn_fwd_rank_step.argtypes = [_vp, _vp, _vp, _i32p, ra_dims, ctypes.c_int,
@@ -131,7 +134,7 @@ def library():
         for fn in ("ringattn_fwd", "ringattn_fwd_stepwise", "ringattn_bwd", "attn_lse_merge",
                    "ringattn_fwd_rank_step", "ringattn_bwd_rank_step",
                    "ringattn_get_status", "ringattn_selftest_wait_timeout",
-                   "ringattn_plan_fwd", "ringattn_plan_bwd",
+                   "ringattn_plan_fwd", "ringattn_plan_bwd", "ringattn_plan_fwd_fused",
                    "ringattn_trace_enable", "ringattn_trace_collect"):
             getattr(lib, fn).restype = ctypes.c_int
         _lib = lib
@@ -364,20 +367,20 @@ def selftest_wait_timeout(stream=None) -> None:
 
 
 def _plan(fn_name, item_fields, total_tokens, hq, hkv, num_shards, shard_layout, causal,
-          cu_seqlens, heads_k_stride, kv_exchange=RING):
+          cu_seqlens, heads_k_stride, kv_exchange=RING, extra=()):
     cu_p, nseq, _keep = _cu_host(cu_seqlens)
     dims = ra_dims(total_tokens, nseq, hq, hkv, 64, RA_FP32, heads_k_stride, 0, kv_exchange)
     ni, ns = ctypes.c_int(0), ctypes.c_int(0)
     fn = getattr(library(), fn_name)
-    code = fn(cu_p, dims, num_shards, shard_layout, int(bool(causal)), None, 0, None, 0,
-              ctypes.byref(ni), ctypes.byref(ns))
+    head = (cu_p, dims, num_shards, shard_layout, int(bool(causal))) + tuple(extra)
+    code = fn(*head, None, 0, None, 0, ctypes.byref(ni), ctypes.byref(ns))
     if code not in (0, -6):
         raise RingAttnError(fn_name, code)
     items = np.zeros((max(ni.value, 1), item_fields), np.int32)
     segs = np.zeros((max(ns.value, 1), PLAN_SEG_FIELDS), np.int32)
-    _check(fn_name, fn(cu_p, dims, num_shards, shard_layout, int(bool(causal)),
-                       items.ctypes.data_as(_i32p), items.shape[0], segs.ctypes.data_as(_i32p),
-                       segs.shape[0], ctypes.byref(ni), ctypes.byref(ns)))
+    _check(fn_name, fn(*head, items.ctypes.data_as(_i32p), items.shape[0],
+                       segs.ctypes.data_as(_i32p), segs.shape[0], ctypes.byref(ni),
+                       ctypes.byref(ns)))
     return items[:ni.value], segs[:ns.value]
 
 
@@ -386,6 +389,15 @@ def plan_fwd(total_tokens, hq, hkv, num_shards, shard_layout, causal, cu_seqlens
     """Host-only: the forward work list as (items [n,16], segments [m,4]) int32 arrays."""
     return _plan("ringattn_plan_fwd", PLAN_ITEM_FIELDS, total_tokens, hq, hkv, num_shards,
                  shard_layout, causal, cu_seqlens, heads_k_stride, kv_exchange)
+
+
+def plan_fwd_fused(total_tokens, hq, hkv, num_shards, shard_layout, causal, num_sms,
+                   cu_seqlens=None, heads_k_stride=1, kv_exchange=RING):
+    """Host-only: the fused forward's work list on a GPU of num_sms SMs, in claim
+    order, with long items split (items [n,16], segments [m,4])."""
+    return _plan("ringattn_plan_fwd_fused", PLAN_ITEM_FIELDS, total_tokens, hq, hkv, num_shards,
+                 shard_layout, causal, cu_seqlens, heads_k_stride, kv_exchange,
+                 extra=(int(num_sms),))
 
 
 def plan_bwd(total_tokens, hq, hkv, num_shards, shard_layout, causal, cu_seqlens=None,

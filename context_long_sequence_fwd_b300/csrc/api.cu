@@ -26,6 +26,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr size_t kMaxCachedPlans = 128;
+constexpr int kMaxHeadDim = 128;
 
 struct DeviceState {
   bool ready = false;
@@ -47,6 +48,16 @@ struct CachedPlan {
   int32_t* cu = nullptr;
   int num_ctas = 0;  // grid of the persistent forward: min(items, SMs)
   cudaEvent_t last_use = nullptr;
+  // the persistent fused forward's claim order and split items, and the fp32
+  // slots of the split halves' partial results
+  FusedPlan fused;
+  void* fused_buf = nullptr;
+  PlanItem* fitems = nullptr;
+  PlanSegment* fsegs = nullptr;
+  SplitPair* fpairs = nullptr;
+  float* part_o = nullptr;
+  float* part_lse = nullptr;
+  int fused_ctas = 0;
   // key-side backward schedule, built on the first backward call
   BwdPlan bwd;
   void* bwd_buf = nullptr;
@@ -170,6 +181,7 @@ ra_status get_plan(int dev, const PlanInput& in, cudaStream_t stream, CachedPlan
     }
     cudaFree(old.buf);
     if (old.bwd_buf) cudaFree(old.bwd_buf);
+    if (old.fused_buf) cudaFree(old.fused_buf);
     cudaSetDevice(cur);
     g_plans.pop_back();
   }
@@ -203,6 +215,45 @@ ra_status get_plan(int dev, const PlanInput& in, cudaStream_t stream, CachedPlan
   if (cudaEventCreateWithFlags(&cp.last_use, cudaEventDisableTiming) != cudaSuccess) {
     cudaFree(cp.buf);
     return RA_ERR_CUDA;
+  }
+  // the fused forward's list (a single ring step's plan runs one item per CTA
+  // and never uses it)
+  if (in.q_rank < 0 && in.k_rank < 0 && !cp.plan.items.empty()) {
+    cp.fused = build_fused_plan(cp.plan, sms);
+    cp.fused_ctas = static_cast<int>(cp.fused.items.size()) < sms
+                        ? static_cast<int>(cp.fused.items.size()) : sms;
+    const size_t fb_items = cp.fused.items.size() * sizeof(PlanItem);
+    const size_t fb_segs = cp.fused.segs.size() * sizeof(PlanSegment);
+    const size_t fb_pairs = cp.fused.pairs.size() * sizeof(SplitPair);
+    const size_t nparts = 2 * cp.fused.pairs.size();  // slots of 2 query tiles x 128 rows
+    const size_t fb_po = nparts * 2 * 128 * (size_t)kMaxHeadDim * sizeof(float);
+    const size_t fb_pl = nparts * 2 * 128 * sizeof(float);
+    size_t off = 0;
+    auto take = [&](size_t n) { const size_t o = off; off += (n + 255) & ~size_t(255); return o; };
+    const size_t o_items = take(fb_items), o_segs = take(fb_segs), o_pairs = take(fb_pairs);
+    const size_t o_po = take(fb_po), o_pl = take(fb_pl);
+    if (cudaMalloc(&cp.fused_buf, off + 256) != cudaSuccess) {
+      cudaFree(cp.buf);
+      cudaEventDestroy(cp.last_use);
+      return RA_ERR_CUDA;
+    }
+    char* fb = static_cast<char*>(cp.fused_buf);
+    cp.fitems = reinterpret_cast<PlanItem*>(fb + o_items);
+    cp.fsegs = reinterpret_cast<PlanSegment*>(fb + o_segs);
+    cp.fpairs = reinterpret_cast<SplitPair*>(fb + o_pairs);
+    cp.part_o = reinterpret_cast<float*>(fb + o_po);
+    cp.part_lse = reinterpret_cast<float*>(fb + o_pl);
+    if ((fb_items && cudaMemcpy(cp.fitems, cp.fused.items.data(), fb_items,
+                                cudaMemcpyHostToDevice) != cudaSuccess) ||
+        (fb_segs && cudaMemcpy(cp.fsegs, cp.fused.segs.data(), fb_segs,
+                               cudaMemcpyHostToDevice) != cudaSuccess) ||
+        (fb_pairs && cudaMemcpy(cp.fpairs, cp.fused.pairs.data(), fb_pairs,
+                                cudaMemcpyHostToDevice) != cudaSuccess)) {
+      cudaFree(cp.buf);
+      cudaFree(cp.fused_buf);
+      cudaEventDestroy(cp.last_use);
+      return RA_ERR_CUDA;
+    }
   }
   (void)stream;
   g_plans.push_front(std::move(cp));
@@ -384,11 +435,28 @@ ra_status ringattn_fwd(const void* q, const void* k, const void* v, const int32_
   if ((st = get_plan(dev, in, static_cast<cudaStream_t>(stream), &cp)) != RA_OK) return st;
   FwdParams p = make_params(q, k, v, out, lse, dims, causal, *cp, ds->status);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool tc = dims.dtype == RA_BF16 && cp->fitems != nullptr;
+  if (tc) {  // the persistent launch's claim order, with long items split
+    p.items = cp->fitems;
+    p.segs = cp->fsegs;
+    p.num_items = static_cast<int>(cp->fused.items.size());
+    p.num_ctas = cp->fused_ctas;
+    p.part_o = cp->part_o;
+    p.part_lse = cp->part_lse;
+  }
+  const int npairs = tc ? static_cast<int>(cp->fused.pairs.size()) : 0;
+  // the plan's partial slots are free once its previous launch is done
+  // (launches of one problem on other streams are ordered behind it)
+  if (npairs > 0 && cudaStreamWaitEvent(s, cp->last_use, 0) != cudaSuccess) return RA_ERR_CUDA;
   cudaEvent_t counter_ev = nullptr;
   if (dims.dtype == RA_BF16 && p.num_items > 0 &&
       (st = claim_counter(dev, s, &p.work_counter, &counter_ev)) != RA_OK)
     return st;
   if ((st = launch_fwd(p, dims, &maps, s)) != RA_OK) return st;
+  if (npairs > 0 &&
+      launch_split_merge(cp->fpairs, npairs, cp->part_o, cp->part_lse, out, false, lse, dims.hq,
+                         dims.total_tokens, dims.head_dim, s) != cudaSuccess)
+    return RA_ERR_CUDA;
   if (counter_ev && cudaEventRecord(counter_ev, s) != cudaSuccess) return RA_ERR_CUDA;
   if (cudaEventRecord(cp->last_use, s) != cudaSuccess) return RA_ERR_CUDA;
   return RA_OK;
@@ -923,6 +991,27 @@ ra_status ringattn_plan_fwd(const int32_t* cu_seqlens, ra_dims dims, int num_sha
   if (st != RA_OK) return st;
   if (!num_items || !num_segments) return RA_ERR_INVALID_ARG;
   const Plan plan = build_fwd_plan(in);
+  *num_items = static_cast<int>(plan.items.size());
+  *num_segments = static_cast<int>(plan.segs.size());
+  if (*num_items > max_items || *num_segments > max_segments) return RA_ERR_WORKSPACE;
+  if (*num_items && items) std::memcpy(items, plan.items.data(), plan.items.size() * sizeof(PlanItem));
+  if (*num_segments && segments)
+    std::memcpy(segments, plan.segs.data(), plan.segs.size() * sizeof(PlanSegment));
+  return RA_OK;
+}
+
+ra_status ringattn_plan_fwd_fused(const int32_t* cu_seqlens, ra_dims dims, int num_shards,
+                                  int shard_layout, int causal, int num_sms, int32_t* items,
+                                  int max_items, int32_t* segments, int max_segments,
+                                  int* num_items, int* num_segments) {
+  PlanInput in;
+  ra_dims d = dims;
+  d.dtype = RA_FP32;
+  d.head_dim = 64;
+  ra_status st = check_problem(cu_seqlens, d, num_shards, shard_layout, causal, &in);
+  if (st != RA_OK) return st;
+  if (!num_items || !num_segments || num_sms < 1) return RA_ERR_INVALID_ARG;
+  const FusedPlan plan = build_fused_plan(build_fwd_plan(in), num_sms);
   *num_items = static_cast<int>(plan.items.size());
   *num_segments = static_cast<int>(plan.segs.size());
   if (*num_items > max_items || *num_segments > max_segments) return RA_ERR_WORKSPACE;

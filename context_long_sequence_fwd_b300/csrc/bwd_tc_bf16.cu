@@ -90,12 +90,15 @@ __device__ __forceinline__ void mma_tmem_x_rows(uint32_t d_tmem, uint32_t a_tmem
   }
 }
 
-// A 128-row tile of head `head` from row `row`: D / 64 boxes of 64 columns.
+// A 128-row tile of head `head` from row `row`: D / 64 boxes of 64 columns,
+// with an L2 eviction policy (l2_evict_last_policy for tiles other CTAs read
+// again, l2_evict_first_policy for tiles read once).
 template <int kD>
 __device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar,
-                                          int head, int row) {
+                                          int head, int row, uint64_t policy) {
 #pragma unroll
-  for (int hf = 0; hf < kD / 64; ++hf) tma_load_3d(dst + hf * kHalfBytes, map, bar, hf * 64, head, row);
+  for (int hf = 0; hf < kD / 64; ++hf)
+    tma_load_3d_hint(dst + hf * kHalfBytes, map, bar, hf * 64, head, row, policy);
 }
 
 // Stores 32 fp32 values (times `mul`) as fp32 at dst (16-byte aligned).
@@ -281,8 +284,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&map_do);
       mbar_arrive_expect_tx(&ctl->kv_full, 2 * kTileBytes);
       const int k0l = local_row(p.kmap, it.k0);
-      load_tile<kD>(smem + kOffK, &map_k, &ctl->kv_full, g, k0l);
-      load_tile<kD>(smem + kOffV, &map_v, &ctl->kv_full, g, k0l);
+      const uint64_t once = l2_evict_first_policy(), again = l2_evict_last_policy();
+      load_tile<kD>(smem + kOffK, &map_k, &ctl->kv_full, g, k0l, once);
+      load_tile<kD>(smem + kOffV, &map_v, &ctl->kv_full, g, k0l, once);
       int li = 0;
       bool ok = true;
       for (int si = 0; si < it.seg_count && ok; ++si) {
@@ -298,8 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* st = smem + kOffStage + slot * kStageBytes;
             mbar_arrive_expect_tx(&ctl->q_full[slot], 2 * kTileBytes);
             const int i0l = local_row(p.qmap, i0);
-            load_tile<kD>(st, &map_q, &ctl->q_full[slot], h, i0l);
-            load_tile<kD>(st + kTileBytes, &map_do, &ctl->q_full[slot], h, i0l);
+            load_tile<kD>(st, &map_q, &ctl->q_full[slot], h, i0l, again);
+            load_tile<kD>(st + kTileBytes, &map_do, &ctl->q_full[slot], h, i0l, again);
           }
         }
       }
@@ -630,8 +634,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&map_v);
       mbar_arrive_expect_tx(&ctl->qd_full, 2 * kTileBytes);
       const int q0l = local_row(p.qmap, q0);
-      load_tile<kD>(smem + kOffQ, &map_q, &ctl->qd_full, head, q0l);
-      load_tile<kD>(smem + kOffDO, &map_do, &ctl->qd_full, head, q0l);
+      const uint64_t once = l2_evict_first_policy(), again = l2_evict_last_policy();
+      load_tile<kD>(smem + kOffQ, &map_q, &ctl->qd_full, head, q0l, once);
+      load_tile<kD>(smem + kOffDO, &map_do, &ctl->qd_full, head, q0l, once);
       int j = 0, nk = 0, nv = 0;  // tiles visited, K and V loads issued
       bool ok = true;
       for (int si = 0; si < it.seg_count && ok; ++si) {
@@ -645,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(&ctl->k_full[ks], kTileBytes);
           load_tile<kD>(smem + kOffKq + ks * kTileBytes, &map_k, &ctl->k_full[ks], g,
-                        local_row(p.kmap, kt));
+                        local_row(p.kmap, kt), again);
           ++nk;
           if (j >= kVSlots &&
               !mbar_wait(&ctl->v_empty[vs], ((j / kVSlots) - 1) & 1, p.status, abort)) {
@@ -654,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mbar_arrive_expect_tx(&ctl->v_full[vs], kTileBytes);
           load_tile<kD>(smem + kOffVq + vs * kTileBytes, &map_v, &ctl->v_full[vs], g,
-                        local_row(p.kmap, kt));
+                        local_row(p.kmap, kt), again);
           ++nv;
         }
       }

@@ -45,6 +45,11 @@ struct FwdParams {
   RowMap qmap;            // rows of q, out and lse (identity: whole sequence)
   RowMap kmap;            // rows of k and v
   int lse_stride;         // rows per head of lse: [Hq, lse_stride]
+  // partial results of split items (PlanItem.part >= 0): slot s holds the two
+  // query tiles' O / l, fp32 [2][128][D], at part_o + s * 2 * 128 * D, and
+  // their lse at part_lse + s * 2 * 128
+  float* part_o;
+  float* part_lse;
 };
 
 struct BwdParams {

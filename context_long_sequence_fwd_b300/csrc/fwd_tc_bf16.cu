@@ -461,6 +461,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv_l = empty ? 0.f : 1.f / l;
       const int lrow = local_row(p.qmap, row);
       const size_t ob = ((size_t)lrow * p.hq + head) * kD;
+      // half of a split item: its partial (O / l, lse) goes to its fp32 slot
+      const bool to_part = it.part >= 0;
+      const size_t pslot = ((size_t)it.part * 2 + x) * 128 + r;
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t u[32];
@@ -471,8 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) u[i] = 0u;
         }
         if (valid) {
-          if (p.out_fp32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + ob + c * 32);
+          if (to_part || p.out_fp32) {
+            float* base = to_part ? p.part_o + pslot * kD : static_cast<float*>(p.out) + ob;
+            float4* dst = reinterpret_cast<float4*>(base + c * 32);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               dst[i] = make_float4(__uint_as_float(u[4 * i]) * inv_l,
@@ -494,9 +498,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (valid)
-        p.lse[(size_t)head * p.lse_stride + lrow] =
-            empty ? -INFINITY : (m2 + log2f(l)) * 0.69314718055994530942f;
+      if (valid) {
+        const float L = empty ? -INFINITY : (m2 + log2f(l)) * 0.69314718055994530942f;
+        if (to_part)
+          p.part_lse[pslot] = L;
+        else
+          p.lse[(size_t)head * p.lse_stride + lrow] = L;
+      }
       // the epilogue's TMEM reads precede the next item's first P (and with
       // it the PV MMA that overwrites O)
       tc_fence_before_sync();

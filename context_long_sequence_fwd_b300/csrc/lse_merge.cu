@@ -127,7 +127,93 @@ __global__ void __launch_bounds__(256, 3) lse_merge_kernel(const void* o_a, bool
   if (part == 0) lse_out[(size_t)h * rows + row] = L;
 }
 
+// The two halves of each split item of the fused forward.  One warp per row
+// of a split query tile (CTA c covers rows 4 (c % 32) .. + 3 of tile
+// (c / 32) % 2 of pair c / 64), so every row's loads are in flight at once;
+// the lanes hold D / 32 consecutive values of the row, read and written with
+// vector accesses.  Same merge rule as above, from the halves' fp32 slots
+// into out (bf16 or fp32) and lse at the tile's rows.
+template <int kD>
+__global__ void __launch_bounds__(128) split_merge_kernel(const SplitPair* pairs,
+                                                          const float* part_o,
+                                                          const float* part_lse, void* out,
+                                                          bool out_fp32, float* lse, int hq,
+                                                          int lse_stride) {
+  constexpr int kV = kD / 32;  // values per lane: 4 (D = 128) or 2 (D = 64)
+  const int pair = blockIdx.x >> 6;
+  const int x = (blockIdx.x >> 5) & 1;
+  const int r = (blockIdx.x & 31) * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const SplitPair sp = pairs[pair];
+  if (r >= sp.qlen[x]) return;
+  const size_t sa = ((size_t)sp.part[0] * 2 + x) * 128 + r;
+  const size_t sb = ((size_t)sp.part[1] * 2 + x) * 128 + r;
+  const float a = part_lse[sa], b = part_lse[sb];
+  float oa[kV], ob[kV];
+  if constexpr (kV == 4) {
+    const float4 va = reinterpret_cast<const float4*>(part_o + sa * kD)[lane];
+    const float4 vb = reinterpret_cast<const float4*>(part_o + sb * kD)[lane];
+    oa[0] = va.x; oa[1] = va.y; oa[2] = va.z; oa[3] = va.w;
+    ob[0] = vb.x; ob[1] = vb.y; ob[2] = vb.z; ob[3] = vb.w;
+  } else {
+    const float2 va = reinterpret_cast<const float2*>(part_o + sa * kD)[lane];
+    const float2 vb = reinterpret_cast<const float2*>(part_o + sb * kD)[lane];
+    oa[0] = va.x; oa[1] = va.y;
+    ob[0] = vb.x; ob[1] = vb.y;
+  }
+  const bool ea = a == -INFINITY, eb = b == -INFINITY;
+  float L = -INFINITY, wa = 0.f, wb = 0.f;
+  if (!ea && !eb) {
+    const float mx = fmaxf(a, b);
+    L = mx + log1pf(expf(-fabsf(a - b)));
+    wa = expf(a - L);
+    wb = expf(b - L);
+  } else if (!ea) {
+    L = a;
+    wa = 1.f;
+  } else if (!eb) {
+    L = b;
+    wb = 1.f;
+  }
+  float o[kV];
+#pragma unroll
+  for (int i = 0; i < kV; ++i) o[i] = (ea ? 0.f : wa * oa[i]) + (eb ? 0.f : wb * ob[i]);
+  const int row = sp.q0[x] + r;
+  const size_t at = ((size_t)row * hq + sp.head[x]) * kD + lane * kV;
+  if (out_fp32) {
+#pragma unroll
+    for (int i = 0; i < kV; ++i) static_cast<float*>(out)[at + i] = o[i];
+  } else if constexpr (kV == 4) {
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(o[0], o[1]);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(o[2], o[3]);
+    uint2 w;
+    w.x = *reinterpret_cast<const uint32_t*>(&lo);
+    w.y = *reinterpret_cast<const uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + at) = w;
+  } else {
+    *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(out) + at) =
+        __floats2bfloat162_rn(o[0], o[1]);
+  }
+  if (lane == 0) lse[(size_t)sp.head[x] * lse_stride + row] = L;
+}
+
 }  // namespace
+
+cudaError_t launch_split_merge(const SplitPair* pairs, int num_pairs, const float* part_o,
+                               const float* part_lse, void* out, bool out_fp32, float* lse,
+                               int hq, int lse_stride, int D, cudaStream_t stream) {
+  if (num_pairs == 0) return cudaSuccess;
+  TraceScope trace_scope(stream, "split_merge_kernel");
+  if (D == 128)
+    split_merge_kernel<128><<<64 * num_pairs, 128, 0, stream>>>(pairs, part_o, part_lse, out,
+                                                                out_fp32, lse, hq, lse_stride);
+  else if (D == 64)
+    split_merge_kernel<64><<<64 * num_pairs, 128, 0, stream>>>(pairs, part_o, part_lse, out,
+                                                               out_fp32, lse, hq, lse_stride);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_lse_merge(const void* o_a, bool a_fp32, const float* lse_a, const void* o_b,
                              bool b_fp32, const float* lse_b, void* o_out, bool out_fp32,

@@ -88,6 +88,7 @@ Plan build_fwd_plan(const PlanInput& in) {
             const int hstep = head_pairs ? 2 : 1;
             for (int h = g * G; h < (g + 1) * G; h += hstep) {
               PlanItem it{};
+              it.part = -1;
               for (int x = 0; x < 2; ++x) {
                 int q0 = head_pairs ? t0 : t0 + x * kTileRows;
                 int len = std::max(0, std::min(kTileRows, b - q0));
@@ -148,6 +149,93 @@ Plan build_fwd_plan(const PlanInput& in) {
                      [](const PlanItem& x, const PlanItem& y) { return x.cost > y.cost; });
   }
   return plan;
+}
+
+FusedPlan build_fused_plan(const Plan& plan, int num_ctas) {
+  FusedPlan f;
+  if (plan.items.empty() || num_ctas < 1) return f;
+  long long total = 0;
+  for (const PlanItem& it : plan.items) total += it.cost;
+  const double mean = static_cast<double>(total) / num_ctas;
+  for (const PlanItem& it : plan.items) {
+    const PlanSegment* sg = plan.segs.data() + it.seg_begin;
+    if (it.cost < 2 || it.cost <= mean) {
+      PlanItem c = it;
+      c.seg_begin = static_cast<int32_t>(f.segs.size());
+      f.segs.insert(f.segs.end(), sg, sg + it.seg_count);
+      f.items.push_back(c);
+      continue;
+    }
+    // first half: the first ceil(cost / 2) key tiles in ring order
+    const int first = (it.cost + 1) / 2;
+    const int pair = static_cast<int>(f.pairs.size());
+    PlanItem half[2] = {it, it};
+    int tiles = 0;
+    int h = 0;
+    half[0].seg_begin = static_cast<int32_t>(f.segs.size());
+    for (int si = 0; si < it.seg_count; ++si) {
+      PlanSegment cur = sg[si];
+      while (cur.k0 < cur.k1) {
+        const int n = (cur.k1 - cur.k0 + kTileRows - 1) / kTileRows;
+        if (h == 0 && tiles + n > first) {
+          // cut the segment where the first half's tiles end
+          PlanSegment a = cur;
+          a.k1 = cur.k0 + (first - tiles) * kTileRows;
+          f.segs.push_back(a);
+          tiles = first;
+          cur.k0 = a.k1;
+        } else {
+          f.segs.push_back(cur);
+          tiles += n;
+          cur.k0 = cur.k1;
+        }
+        if (h == 0 && tiles == first) {
+          half[0].seg_count = static_cast<int32_t>(f.segs.size()) - half[0].seg_begin;
+          half[1].seg_begin = static_cast<int32_t>(f.segs.size());
+          h = 1;
+        }
+      }
+    }
+    half[1].seg_count = static_cast<int32_t>(f.segs.size()) - half[1].seg_begin;
+    half[0].cost = first;
+    half[1].cost = it.cost - first;
+    half[0].part = 2 * pair;
+    half[1].part = 2 * pair + 1;
+    f.items.push_back(half[0]);
+    f.items.push_back(half[1]);
+    SplitPair sp{};
+    for (int x = 0; x < 2; ++x) {
+      sp.q0[x] = it.q0[x];
+      sp.qlen[x] = it.qlen[x];
+      sp.head[x] = it.head[x];
+      sp.part[x] = 2 * pair + x;
+    }
+    f.pairs.push_back(sp);
+  }
+  // ordering groups of consecutive passes, at least 2 num_ctas items each
+  int max_pass = 0;
+  for (const PlanItem& it : plan.items) max_pass = std::max(max_pass, static_cast<int>(it.pass));
+  std::vector<long long> per_pass(max_pass + 1, 0);
+  for (const PlanItem& it : plan.items) ++per_pass[it.pass];
+  std::vector<int> group(max_pass + 1, 0);
+  int g = 0;
+  long long in_group = 0;
+  for (int p = 0; p <= max_pass; ++p) {
+    group[p] = g;
+    in_group += per_pass[p];
+    if (in_group >= 2LL * num_ctas) {
+      ++g;
+      in_group = 0;
+    }
+  }
+  if (in_group > 0 && g > 0)  // a small rest joins the group before it
+    for (int p = 0; p <= max_pass; ++p)
+      if (group[p] == g) group[p] = g - 1;
+  std::stable_sort(f.items.begin(), f.items.end(), [&](const PlanItem& x, const PlanItem& y) {
+    if (group[x.pass] != group[y.pass]) return group[x.pass] < group[y.pass];
+    return x.cost > y.cost;
+  });
+  return f;
 }
 
 BwdPlan build_bwd_plan(const PlanInput& in) {

@@ -27,7 +27,8 @@ struct PlanItem {
   int32_t mask_lo[2];  // per tile: largest first-visible key over its rows
   int32_t mask_hi[2];  // per tile: smallest end-of-visible-keys over its rows
   int32_t pass;        // pass over key/value heads (heads_k_stride groups)
-  int32_t pad;
+  int32_t part;        // -1: writes the output; else the partial-result slot of a
+                       // split item (fused forward only, see build_fused_plan)
 };
 static_assert(sizeof(PlanItem) == 16 * 4, "PlanItem is 16 int32");
 
@@ -78,6 +79,34 @@ struct BwdPlan {
   std::vector<BwdItem> items;
   std::vector<BwdSegment> segs;
 };
+
+// Two items that split one item's key tiles: the same query tiles, each half
+// writing its partial (O, lse) to a slot, merged afterwards.
+struct SplitPair {
+  int32_t q0[2], qlen[2], head[2];
+  int32_t part[2];  // partial-result slots of the first and second half
+};
+static_assert(sizeof(SplitPair) == 8 * 4, "SplitPair is 8 int32");
+
+// The persistent fused forward's work list: the plan's items in claim order,
+// with long items split (see build_fused_plan).
+struct FusedPlan {
+  std::vector<PlanItem> items;
+  std::vector<PlanSegment> segs;
+  std::vector<SplitPair> pairs;
+};
+
+// Claim order and splits of the forward plan for a persistent launch of
+// `num_ctas` CTAs that claim items as they become free:
+//  - passes over key/value heads are merged into ordering groups of at least
+//    2 num_ctas items (the last smaller rest joins the group before it), and
+//    items run longest first inside a group.  A big problem keeps one pass
+//    per group, so the K/V of few heads are in flight at once; a small one
+//    is ordered longest first as a whole, which is what balances it.
+//  - when an item is longer than the mean work per CTA, it is split into two
+//    items over the first and the second half of its key tiles (in ring
+//    order); each half writes a partial (O, lse) that a merge folds together.
+FusedPlan build_fused_plan(const Plan& plan, int num_ctas);
 
 // Builds the key/value-side backward schedule.  `in` must have passed plan_check.
 BwdPlan build_bwd_plan(const PlanInput& in);

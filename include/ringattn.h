@@ -313,7 +313,7 @@ int ringattn_version(void);
  * beyond it and RA_ERR_WORKSPACE is returned with the counts still set.
  *   item:    q0_a, q0_b, qlen_a, qlen_b, head_a, head_b, seg_begin,
  *            seg_count, rank, cost (kv tiles), mask_lo_a, mask_lo_b,
- *            mask_hi_a, mask_hi_b, pass, pad
+ *            mask_hi_a, mask_hi_b, pass, part (-1 here; see below)
  *            (tile a/b: first query row, valid rows, query head; the key
  *            range a tile may skip masking in is [mask_lo, mask_hi))
  *   segment: k0, k1, step, src  (keys [k0, k1) of rank src at ring step)
@@ -325,6 +325,21 @@ ra_status ringattn_plan_fwd(const int32_t* cu_seqlens, ra_dims dims, int num_sha
                             int shard_layout, int causal, int32_t* items, int max_items,
                             int32_t* segments, int max_segments, int* num_items,
                             int* num_segments);
+
+/*
+ * Host-only: the work list the fused forward (ringattn_fwd) runs on a GPU of
+ * num_sms SMs, in the order its persistent CTAs claim it (same item and
+ * segment layout as ringattn_plan_fwd).  Passes over key/value heads are
+ * merged into ordering groups of at least 2 num_sms items, longest first
+ * inside a group; an item longer than the mean work per SM is split into two
+ * items over the first and second half of its key tiles in ring order, whose
+ * `part` fields are 2 i and 2 i + 1 (their partial results are merged with
+ * the log-sum-exp rule after the launch).  Same return conventions.
+ */
+ra_status ringattn_plan_fwd_fused(const int32_t* cu_seqlens, ra_dims dims, int num_shards,
+                                  int shard_layout, int causal, int num_sms, int32_t* items,
+                                  int max_items, int32_t* segments, int max_segments,
+                                  int* num_items, int* num_segments);
 
 /*
  * Host-only backward work list (key side): items of RA_PLAN_BWD_ITEM_FIELDS
