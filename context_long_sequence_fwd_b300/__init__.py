@@ -31,7 +31,7 @@ RA_FP32 = 1
 STATUS = {
     0: "RA_OK", -1: "RA_ERR_INVALID_ARG", -2: "RA_ERR_NOT_DIVISIBLE",
     -3: "RA_ERR_UNSUPPORTED", -4: "RA_ERR_CUDA", -5: "RA_ERR_TIMEOUT",
-    -6: "RA_ERR_WORKSPACE",
+    -6: "RA_ERR_WORKSPACE", -7: "RA_ERR_BOUNDS",
 }
 PLAN_ITEM_FIELDS = 16
 PLAN_SEG_FIELDS = 4
@@ -44,7 +44,10 @@ BWD_ITEM_COLUMNS = ("k0", "klen", "kv_head", "src", "seg_begin", "seg_count", "c
 BWD_SEG_COLUMNS = ("q0", "q1", "step", "rank")
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libringattn.so")
+# RINGATTN_DEBUG=1 selects the bounds-checking build (libringattn_debug.so,
+# `python -m context_long_sequence_fwd_b300.build --debug`)
+DEBUG = os.environ.get("RINGATTN_DEBUG", "0") not in ("", "0")
+LIB_PATH = os.path.join(_HERE, "libringattn_debug.so" if DEBUG else "libringattn.so")
 _lib = None
 
 
@@ -84,7 +87,8 @@ def library():
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(
                 f"{LIB_PATH} is missing: build it with "
-                "`python -m context_long_sequence_fwd_b300.build` (nvcc, sm_103a)")
+                "`python -m context_long_sequence_fwd_b300.build"
+                + (" --debug" if DEBUG else "") + "` (nvcc, sm_103a)")
         lib = ctypes.CDLL(LIB_PATH)
         lib.ringattn_fwd.argtypes = [_vp, _vp, _vp, _i32p, ra_dims, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, _vp, _vp, _vp]
@@ -105,6 +109,9 @@ def library():
         lib.ringattn_status_string.argtypes = [ctypes.c_int]
         lib.ringattn_status_string.restype = ctypes.c_char_p
         lib.ringattn_version.restype = ctypes.c_int
+        lib.ringattn_debug_report.argtypes = [_vp, ctypes.POINTER(ctypes.c_longlong),
+                                              ctypes.POINTER(ctypes.c_longlong)]
+        lib.ringattn_debug_report.restype = ctypes.c_int
         lib.ringattn_plan_fwd.argtypes = [_i32p, ra_dims, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_int, _i32p, ctypes.c_int, _i32p, ctypes.c_int,
                                           _ip, _ip]
@@ -356,6 +363,16 @@ def attn_lse_merge(o_a, lse_a, o_b, lse_b, stream=None):
 def ringattn_get_status(stream=None) -> int:
     """Synchronises the stream; returns and clears the kernel-side error word."""
     return int(library().ringattn_get_status(_stream(stream)))
+
+
+def debug_report(stream=None):
+    """(checks_compiled_in, site, index) of the first failed bounds check since
+    the last call (site 0: none); only the debug build makes checks."""
+    site, index = ctypes.c_longlong(0), ctypes.c_longlong(0)
+    rc = library().ringattn_debug_report(_stream(stream), ctypes.byref(site), ctypes.byref(index))
+    if rc < 0:
+        raise RingAttnError("ringattn_debug_report", -4)
+    return bool(rc), int(site.value), int(index.value)
 
 
 def selftest_wait_timeout(stream=None) -> None:

@@ -19,8 +19,10 @@
 
 namespace ra {
 
-// First kernel-side error since the last ringattn_get_status (0 = none).
-__device__ int g_status_word;
+// Word 0: the first kernel-side error since the last ringattn_get_status
+// (0 = none).  Words 2-3: the debug build's first failed bounds check,
+// (site << 48 | index), 0 = none.
+__device__ __align__(8) int g_status_word[4];
 
 namespace {
 
@@ -87,7 +89,7 @@ ra_status current_device(int* dev_out, DeviceState** st_out) {
     } else {
       void* addr = nullptr;
       if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return RA_ERR_CUDA;
-      if (cudaMemset(addr, 0, sizeof(int)) != cudaSuccess) return RA_ERR_CUDA;
+      if (cudaMemset(addr, 0, 4 * sizeof(int)) != cudaSuccess) return RA_ERR_CUDA;
       st.status = static_cast<int*>(addr);
       st.why = RA_OK;
     }
@@ -311,6 +313,10 @@ FwdParams make_params(const void* q, const void* k, const void* v, void* out, fl
   p.qmap = RowMap{0, INT_MAX, 0};  // whole-sequence buffers
   p.kmap = RowMap{0, INT_MAX, 0};
   p.lse_stride = d.total_tokens;
+  p.num_segs = static_cast<int>(cp.plan.segs.size());
+  p.num_parts = 0;
+  p.q_rows = d.total_tokens;
+  p.k_rows = d.total_tokens;
   return p;
 }
 
@@ -443,6 +449,8 @@ ra_status ringattn_fwd(const void* q, const void* k, const void* v, const int32_
     p.num_ctas = cp->fused_ctas;
     p.part_o = cp->part_o;
     p.part_lse = cp->part_lse;
+    p.num_segs = static_cast<int>(cp->fused.segs.size());
+    p.num_parts = 2 * static_cast<int>(cp->fused.pairs.size());
   }
   const int npairs = tc ? static_cast<int>(cp->fused.pairs.size()) : 0;
   // the plan's partial slots are free once its previous launch is done
@@ -455,7 +463,7 @@ ra_status ringattn_fwd(const void* q, const void* k, const void* v, const int32_
   if ((st = launch_fwd(p, dims, &maps, s)) != RA_OK) return st;
   if (npairs > 0 &&
       launch_split_merge(cp->fpairs, npairs, cp->part_o, cp->part_lse, out, false, lse, dims.hq,
-                         dims.total_tokens, dims.head_dim, s) != cudaSuccess)
+                         dims.total_tokens, dims.head_dim, ds->status, s) != cudaSuccess)
     return RA_ERR_CUDA;
   if (counter_ev && cudaEventRecord(counter_ev, s) != cudaSuccess) return RA_ERR_CUDA;
   if (cudaEventRecord(cp->last_use, s) != cudaSuccess) return RA_ERR_CUDA;
@@ -511,7 +519,7 @@ ra_status ringattn_fwd_stepwise(const void* q, const void* k, const void* v,
       cudaError_t e = launch_lse_merge(acc_o, true, acc_l, stp_o, true, stp_l,
                                        last ? out : static_cast<void*>(acc_o),
                                        last ? out_fp32 : true, last ? lse : acc_l,
-                                       dims.total_tokens, dims.hq, dims.head_dim, s);
+                                       dims.total_tokens, dims.hq, dims.head_dim, ds->status, s);
       if (e != cudaSuccess) return RA_ERR_CUDA;
     }
   }
@@ -619,7 +627,7 @@ extern "C" ra_status ringattn_fwd_stepwise_noalloc(const void* q, const void* k,
       cudaError_t e = launch_lse_merge(acc_o, true, acc_l, stp_o, true, stp_l,
                                        last ? out : static_cast<void*>(acc_o),
                                        last ? out_fp32 : true, last ? lse : acc_l,
-                                       dims.total_tokens, dims.hq, dims.head_dim, s);
+                                       dims.total_tokens, dims.hq, dims.head_dim, ds->status, s);
       if (e != cudaSuccess) return RA_ERR_CUDA;
     }
   }
@@ -662,7 +670,8 @@ ra_status ringattn_bwd(const void* q, const void* k, const void* v, const void* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* Dvec = static_cast<float*>(workspace);
   const bool f32 = dims.dtype == RA_FP32;
-  if (launch_bwd_preprocess(out, dout, f32, Dvec, dims.total_tokens, dims.hq, dims.head_dim, s) !=
+  if (launch_bwd_preprocess(out, dout, f32, Dvec, dims.total_tokens, dims.hq, dims.head_dim,
+                            ds->status, s) !=
       cudaSuccess)
     return RA_ERR_CUDA;
   BwdParams p{};
@@ -697,6 +706,10 @@ ra_status ringattn_bwd(const void* q, const void* k, const void* v, const void* 
   p.kmap = RowMap{0, INT_MAX, 0};
   p.lse_stride = dims.total_tokens;
   p.accumulate = 0;
+  p.num_segs = static_cast<int>(cp->plan.segs.size());
+  p.num_bsegs = static_cast<int>(cp->bwd.segs.size());
+  p.q_rows = dims.total_tokens;
+  p.k_rows = dims.total_tokens;
   cudaError_t e = f32 ? launch_bwd_simt_fp32(p, s)
                       : launch_bwd_tc_bf16(p, maps.q, maps.k, maps.v, map_do, s);
   if (e != cudaSuccess) return RA_ERR_CUDA;
@@ -759,6 +772,8 @@ ra_status ringattn_fwd_rank_step(const void* q, const void* k, const void* v,
   p.qmap = rank_rows(dims.total_tokens, num_shards, shard_layout, rank);
   p.kmap = rank_rows(dims.total_tokens, num_shards, shard_layout, in.k_rank);
   p.lse_stride = Tr;
+  p.q_rows = Tr;
+  p.k_rows = Tr;
   p.out_fp32 = (first && last) ? 0 : 1;
   // every query tile of the rank is an item (one CTA each); a tile that sees
   // no key of this shard writes O = 0, lse = -inf
@@ -766,7 +781,8 @@ ra_status ringattn_fwd_rank_step(const void* q, const void* k, const void* v,
   if (!first) {
     if (launch_lse_merge(o_acc, true, lse_acc, stp_o, true, stp_l,
                          last ? out : static_cast<void*>(o_acc), last ? false : true,
-                         last ? lse : lse_acc, Tr, dims.hq, dims.head_dim, s) != cudaSuccess)
+                         last ? lse : lse_acc, Tr, dims.hq, dims.head_dim, ds->status,
+                         s) != cudaSuccess)
       return RA_ERR_CUDA;
   }
   if (cudaEventRecord(cp->last_use, s) != cudaSuccess) return RA_ERR_CUDA;
@@ -817,7 +833,8 @@ ra_status ringattn_bwd_rank_step(const void* q, const void* k, const void* v, co
   // step 0 computes the rank's D_i once; the caller keeps the workspace
   // for the later steps
   if (step == 0 &&
-      launch_bwd_preprocess(out, dout, false, Dvec, Tr, dims.hq, dims.head_dim, s) != cudaSuccess)
+      launch_bwd_preprocess(out, dout, false, Dvec, Tr, dims.hq, dims.head_dim, ds->status, s) !=
+          cudaSuccess)
     return RA_ERR_CUDA;
   BwdParams p{};
   p.q = q;
@@ -850,6 +867,10 @@ ra_status ringattn_bwd_rank_step(const void* q, const void* k, const void* v, co
   p.qmap = rank_rows(dims.total_tokens, num_shards, shard_layout, rank);
   p.kmap = rank_rows(dims.total_tokens, num_shards, shard_layout, in.k_rank);
   p.lse_stride = Tr;
+  p.num_segs = static_cast<int>(cp->plan.segs.size());
+  p.num_bsegs = static_cast<int>(cp->bwd.segs.size());
+  p.q_rows = Tr;
+  p.k_rows = Tr;
   // step 0 starts dq (this rank's rows) and dk, dv (its own keys, which
   // then travel the ring); later steps add to them
   p.accumulate = step == 0 ? 0 : 1;
@@ -875,7 +896,7 @@ ra_status attn_lse_merge(void* o_a, float* lse_a, const void* o_b, const float* 
   }
   const bool f32 = dtype == RA_FP32;
   cudaError_t e = launch_lse_merge(o_a, f32, lse_a, o_b, f32, lse_b, o_a, f32, lse_a, rows, heads,
-                                   head_dim, static_cast<cudaStream_t>(stream));
+                                   head_dim, ds->status, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? RA_OK : RA_ERR_CUDA;
 }
 
@@ -972,11 +993,33 @@ const char* ringattn_status_string(int status) {
     case RA_ERR_CUDA: return "CUDA runtime error";
     case RA_ERR_TIMEOUT: return "a kernel wait timed out";
     case RA_ERR_WORKSPACE: return "workspace missing or too small";
+    case RA_ERR_BOUNDS: return "an index failed a bounds check of the debug build";
     default: return "unknown status";
   }
 }
 
 int ringattn_version(void) { return 100; }
+
+int ringattn_debug_report(void* stream, long long* site, long long* index) {
+  int dev;
+  DeviceState* ds;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (current_device(&dev, &ds) != RA_OK) return -1;
+  }
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return -1;
+  unsigned long long where = 0;
+  if (cudaMemcpy(&where, ds->status + 2, sizeof(where), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return -1;
+  if (where != 0 && cudaMemset(ds->status + 2, 0, sizeof(where)) != cudaSuccess) return -1;
+  if (site) *site = static_cast<long long>(where >> 48);
+  if (index) *index = static_cast<long long>(where & 0xFFFFFFFFFFFFull);
+#ifdef RINGATTN_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
 
 ra_status ringattn_plan_fwd(const int32_t* cu_seqlens, ra_dims dims, int num_shards,
                             int shard_layout, int causal, int32_t* items, int max_items,

@@ -50,14 +50,16 @@ constexpr int kChunks = 4;
 template <bool kF32>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const void* out, const void* dout,
                                                              float* Dvec, int T, int hq, int D,
-                                                             long long rows) {
+                                                             long long rows, int* status) {
   const int tpr = D / (8 * kChunks);  // threads per row; divides 32
   const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long r = gt / tpr;
   const int part = (int)(gt % tpr);
   float s = 0.f;
   int h = 0, i = 0;
-  if (r < rows) {
+  const bool in = r < rows && index_ok(r * D + (long long)(part + 1) * 8 * kChunks - 1,
+                                       rows * D, status, kSitePreprocess);
+  if (in) {
     i = (int)(r / hq);
     h = (int)(r % hq);
     const size_t idx = ((size_t)i * hq + h) * D + (size_t)part * 8 * kChunks;
@@ -67,22 +69,23 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(const void* out, co
     s = (t[0] + t[1]) + (t[2] + t[3]);
   }
   for (int off = tpr / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (r < rows && part == 0) Dvec[(size_t)h * T + i] = s;
+  if (in && part == 0 && index_ok((long long)h * T + i, rows, status, kSitePreprocess))
+    Dvec[(size_t)h * T + i] = s;
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const void* out, const void* dout, bool fp32, float* Dvec, int T,
-                                  int hq, int D, cudaStream_t stream) {
+                                  int hq, int D, int* status, cudaStream_t stream) {
   const long long rows = (long long)T * hq;
   if (rows == 0) return cudaSuccess;
   const long long threads = rows * (D / (8 * kChunks));
   const long long grid = (threads + 255) / 256;
   TraceScope trace_scope(stream, "bwd_preprocess_kernel");
   if (fp32)
-    bwd_preprocess_kernel<true><<<(unsigned)grid, 256, 0, stream>>>(out, dout, Dvec, T, hq, D, rows);
+    bwd_preprocess_kernel<true><<<(unsigned)grid, 256, 0, stream>>>(out, dout, Dvec, T, hq, D, rows, status);
   else
-    bwd_preprocess_kernel<false><<<(unsigned)grid, 256, 0, stream>>>(out, dout, Dvec, T, hq, D, rows);
+    bwd_preprocess_kernel<false><<<(unsigned)grid, 256, 0, stream>>>(out, dout, Dvec, T, hq, D, rows, status);
   return cudaGetLastError();
 }
 

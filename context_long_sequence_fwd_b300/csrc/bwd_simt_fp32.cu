@@ -26,11 +26,12 @@ template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_simt_kernel(BwdParams p) {
   __shared__ float Ks[kRows][D];
   __shared__ float Vs[kRows][D];
-  const PlanItem it = p.items[blockIdx.x];
+  const PlanItem it = p.items[checked(blockIdx.x, p.num_items, p.status, kSiteSimtBwd)];
   const int tile = threadIdx.x >> 7, r = threadIdx.x & 127;
   const int row = it.q0[tile] + r;
-  const bool valid = r < it.qlen[tile];
   const int h = it.head[tile];
+  const bool valid = r < it.qlen[tile] && index_ok(row, p.q_rows, p.status, kSiteSimtBwd) &&
+                     index_ok(h, p.hq, p.status, kSiteHead);
   const int g = it.head[0] / p.group;
   const float* q = static_cast<const float*>(p.q);
   const float* k = static_cast<const float*>(p.k);
@@ -44,8 +45,10 @@ __global__ void __launch_bounds__(256) bwd_dq_simt_kernel(BwdParams p) {
     doc_bounds(p.cu, p.num_docs, row, &ds, &de);
     lo = ds;
     hi = p.causal ? row + 1 : de;
-    lse = p.lse[(size_t)h * p.lse_stride + row];
-    Dv = p.Dvec[(size_t)h * p.lse_stride + row];
+    const long long at = checked((long long)h * p.lse_stride + row,
+                                 (long long)p.hq * p.lse_stride, p.status, kSiteSimtBwd);
+    lse = p.lse[at];
+    Dv = p.Dvec[at];
   }
 #pragma unroll
   for (int d = 0; d < D; ++d) {
@@ -55,13 +58,13 @@ __global__ void __launch_bounds__(256) bwd_dq_simt_kernel(BwdParams p) {
     dq[d] = 0.f;
   }
   for (int si = 0; si < it.seg_count; ++si) {
-    const PlanSegment sg = p.segs[it.seg_begin + si];
+    const PlanSegment sg = p.segs[checked(it.seg_begin + si, p.num_segs, p.status, kSiteSimtBwd)];
     const int a = max(lo, sg.k0), b = min(hi, sg.k1);
     for (int kt = sg.k0; kt < sg.k1; kt += kRows) {
       __syncthreads();
       for (int x = threadIdx.x; x < kRows * D; x += blockDim.x) {
         const int jj = x / D, d = x % D, key = kt + jj;
-        const bool in = key < sg.k1;
+        const bool in = key < sg.k1 && index_ok(key, p.k_rows, p.status, kSiteSimtBwd);
         Ks[jj][d] = in ? k[((size_t)key * p.hkv + g) * D + d] : 0.f;
         Vs[jj][d] = in ? v[((size_t)key * p.hkv + g) * D + d] : 0.f;
       }
@@ -94,11 +97,12 @@ __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(BwdParams p) {
   __shared__ float Os[kRows][D];  // dO rows
   __shared__ float Ls[kRows], Ds[kRows];
   __shared__ int Lo[kRows], Hi[kRows];
-  const BwdItem it = p.bitems[blockIdx.x];
+  const BwdItem it = p.bitems[checked(blockIdx.x, p.num_bitems, p.status, kSiteSimtBwd)];
   const int g = it.kv_head;
   const int kr = threadIdx.x;
   const int j = it.k0 + kr;
-  const bool valid = kr < it.klen;
+  const bool valid = kr < it.klen && index_ok(j, p.k_rows, p.status, kSiteSimtBwd) &&
+                     index_ok(g, p.hkv, p.status, kSiteHead);
   const float* q = static_cast<const float*>(p.q);
   const float* k = static_cast<const float*>(p.k);
   const float* v = static_cast<const float*>(p.v);
@@ -113,13 +117,13 @@ __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(BwdParams p) {
     dv[d] = 0.f;
   }
   for (int si = 0; si < it.seg_count; ++si) {
-    const BwdSegment sg = p.bsegs[it.seg_begin + si];
+    const BwdSegment sg = p.bsegs[checked(it.seg_begin + si, p.num_bsegs, p.status, kSiteSimtBwd)];
     for (int i0 = sg.q0; i0 < sg.q1; i0 += kRows) {
       for (int h = g * p.group; h < (g + 1) * p.group; ++h) {
         __syncthreads();
         for (int x = threadIdx.x; x < kRows * D; x += blockDim.x) {
           const int rr = x / D, d = x % D, i = i0 + rr;
-          const bool in = i < sg.q1;
+          const bool in = i < sg.q1 && index_ok(i, p.q_rows, p.status, kSiteSimtBwd);
           Qs[rr][d] = in ? q[((size_t)i * p.hq + h) * D + d] : 0.f;
           Os[rr][d] = in ? dout[((size_t)i * p.hq + h) * D + d] : 0.f;
         }
@@ -132,8 +136,10 @@ __global__ void __launch_bounds__(128) bwd_dkdv_simt_kernel(BwdParams p) {
             doc_bounds(p.cu, p.num_docs, i, &ds, &de);
             lo = ds;
             hi = p.causal ? i + 1 : de;
-            l = p.lse[(size_t)h * p.lse_stride + i];
-            dd = p.Dvec[(size_t)h * p.lse_stride + i];
+            const long long at = checked((long long)h * p.lse_stride + i,
+                                         (long long)p.hq * p.lse_stride, p.status, kSiteSimtBwd);
+            l = p.lse[at];
+            dd = p.Dvec[at];
           }
           Lo[threadIdx.x] = lo;
           Hi[threadIdx.x] = hi;

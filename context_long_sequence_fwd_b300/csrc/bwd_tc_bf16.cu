@@ -241,14 +241,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   CtlKV* ctl = reinterpret_cast<CtlKV*>(smem + kOffCtlKV);
   volatile int* abort = &ctl->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const BwdItem it = p.bitems[blockIdx.x];
+  const BwdItem it = p.bitems[checked(blockIdx.x, p.num_bitems, p.status, kSiteBwdItem)];
   const int g = it.kv_head;
   const int G = p.group;
   const int kend = it.k0 + it.klen;
 
   int n = 0;  // (query tile, head) pairs
   for (int si = 0; si < it.seg_count; ++si) {
-    const BwdSegment sg = p.bsegs[it.seg_begin + si];
+    const BwdSegment sg = p.bsegs[checked(it.seg_begin + si, p.num_bsegs, p.status, kSiteBwdSeg)];
     n += (sg.q1 - sg.q0 + kTile - 1) / kTile * G;
   }
 
@@ -284,13 +284,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&map_do);
       mbar_arrive_expect_tx(&ctl->kv_full, 2 * kTileBytes);
       const int k0l = local_row(p.kmap, it.k0);
+      index_ok(k0l, p.k_rows, p.status, kSiteBwdKvRow);
+      index_ok(g, p.hkv, p.status, kSiteHead);
       const uint64_t once = l2_evict_first_policy(), again = l2_evict_last_policy();
       load_tile<kD>(smem + kOffK, &map_k, &ctl->kv_full, g, k0l, once);
       load_tile<kD>(smem + kOffV, &map_v, &ctl->kv_full, g, k0l, once);
       int li = 0;
       bool ok = true;
       for (int si = 0; si < it.seg_count && ok; ++si) {
-        const BwdSegment sg = p.bsegs[it.seg_begin + si];
+        const BwdSegment sg =
+            p.bsegs[checked(it.seg_begin + si, p.num_bsegs, p.status, kSiteBwdSeg)];
         for (int i0 = sg.q0; i0 < sg.q1 && ok; i0 += kTile) {
           for (int h = g * G; h < (g + 1) * G; ++h, ++li) {
             const int slot = li % kKvStages;
@@ -302,6 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint8_t* st = smem + kOffStage + slot * kStageBytes;
             mbar_arrive_expect_tx(&ctl->q_full[slot], 2 * kTileBytes);
             const int i0l = local_row(p.qmap, i0);
+            index_ok(i0l, p.q_rows, p.status, kSiteBwdQRow);
+            index_ok(h, p.hq, p.status, kSiteHead);
             load_tile<kD>(st, &map_q, &ctl->q_full[slot], h, i0l, again);
             load_tile<kD>(st + kTileBytes, &map_do, &ctl->q_full[slot], h, i0l, again);
           }
@@ -322,7 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int li = 0;
     bool ok = true;
     for (int si = 0; si < it.seg_count && ok; ++si) {
-      const BwdSegment sg = p.bsegs[it.seg_begin + si];
+      const BwdSegment sg =
+          p.bsegs[checked(it.seg_begin + si, p.num_bsegs, p.status, kSiteBwdSeg)];
       for (int i0 = sg.q0; i0 < sg.q1 && ok; i0 += kTile) {
         // the document of the stage's first row; rows past its end search again
         int ds0, de0;
@@ -342,7 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 2; ++k) {
             const int i = i0 + rbase + lane + 32 * k;
             const bool valid = i < sg.q1;
-            const size_t at = (size_t)h * p.lse_stride + (valid ? local_row(p.qmap, i) : 0);
+            const size_t at =
+                checked((long long)h * p.lse_stride + (valid ? local_row(p.qmap, i) : 0),
+                        (long long)p.hq * p.lse_stride, p.status, kSiteBwdRowStat);
             lv[k] = valid ? p.lse[at] : 0.f;
             dv[k] = valid ? p.Dvec[at] : 0.f;
           }
@@ -471,7 +479,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     // epilogue: half 0 writes dV, half 1 writes dK (times the softmax scale)
     const uint32_t tAcc = tmem + lane_off + (x == 0 ? 256 : 384);
-    const size_t off = ((size_t)local_row(p.kmap, j) * p.hkv + g) * kD;
+    const int jl = local_row(p.kmap, j);
+    const bool store = kr < it.klen && index_ok(jl, p.k_rows, p.status, kSiteBwdDkDv) &&
+                       index_ok(g, p.hkv, p.status, kSiteHead);
+    const size_t off = ((size_t)jl * p.hkv + g) * kD;
     void* dst = x == 0 ? p.dv : p.dk;
     const float mul = x == 0 ? 1.f : p.scale;
 #pragma unroll
@@ -483,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) u[i] = 0u;
       }
-      if (ok && kr < it.klen) {
+      if (ok && store) {
         if (p.accumulate)
           add_f32x32(static_cast<float*>(dst) + off + c * 32, u, mul);
         else if (p.grad_fp32)
@@ -576,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kKSlots = Cfg::kKSlots, kVSlots = Cfg::kVSlots;
   constexpr int kOffQ = Cfg::kOffQ, kOffDO = Cfg::kOffDO, kOffKq = Cfg::kOffKq;
   constexpr int kOffVq = Cfg::kOffVq, kOffCtlQ = Cfg::kOffCtlQ;
-  const PlanItem it = p.items[blockIdx.x >> 1];
+  const PlanItem it = p.items[checked(blockIdx.x >> 1, p.num_items, p.status, kSiteBwdItem)];
   const bool second = (blockIdx.x & 1) != 0;  // which of the item's two query tiles
   const int qlen = second ? it.qlen[1] : it.qlen[0];
   if (qlen == 0) return;  // whole CTA: this item has one query tile
@@ -592,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   int n = 0;  // key tiles
   for (int si = 0; si < it.seg_count; ++si) {
-    const PlanSegment sg = p.segs[it.seg_begin + si];
+    const PlanSegment sg = p.segs[checked(it.seg_begin + si, p.num_segs, p.status, kSiteBwdSeg)];
     n += (sg.k1 - sg.k0 + kTile - 1) / kTile;
   }
 
@@ -634,15 +645,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&map_v);
       mbar_arrive_expect_tx(&ctl->qd_full, 2 * kTileBytes);
       const int q0l = local_row(p.qmap, q0);
+      index_ok(q0l, p.q_rows, p.status, kSiteBwdQRow);
+      index_ok(head, p.hq, p.status, kSiteHead);
+      index_ok(g, p.hkv, p.status, kSiteHead);
       const uint64_t once = l2_evict_first_policy(), again = l2_evict_last_policy();
       load_tile<kD>(smem + kOffQ, &map_q, &ctl->qd_full, head, q0l, once);
       load_tile<kD>(smem + kOffDO, &map_do, &ctl->qd_full, head, q0l, once);
       int j = 0, nk = 0, nv = 0;  // tiles visited, K and V loads issued
       bool ok = true;
       for (int si = 0; si < it.seg_count && ok; ++si) {
-        const PlanSegment sg = p.segs[it.seg_begin + si];
+        const PlanSegment sg =
+            p.segs[checked(it.seg_begin + si, p.num_segs, p.status, kSiteBwdSeg)];
         for (int kt = sg.k0; kt < sg.k1; kt += kTile, ++j) {
           const int ks = j % kKSlots, vs = j % kVSlots;
+          index_ok(local_row(p.kmap, kt), p.k_rows, p.status, kSiteBwdKvRow);
           if (j >= kKSlots &&
               !mbar_wait(&ctl->k_empty[ks], ((j / kKSlots) - 1) & 1, p.status, abort)) {
             ok = false;
@@ -752,7 +768,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       doc_bounds(p.cu, p.num_docs, row, &ds, &de);
       lo = ds;
       hi = p.causal ? row + 1 : de;
-      const size_t at = (size_t)head * p.lse_stride + local_row(p.qmap, row);
+      const size_t at = checked((long long)head * p.lse_stride + local_row(p.qmap, row),
+                                (long long)p.hq * p.lse_stride, p.status, kSiteBwdRowStat);
       lse2 = p.lse[at] * kLog2e;
       Dv = p.Dvec[at];
     }
@@ -764,7 +781,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int j = 0;
     for (int si = 0; si < it.seg_count && ok; ++si) {
-      const PlanSegment sg = p.segs[it.seg_begin + si];
+      const PlanSegment sg =
+          p.segs[checked(it.seg_begin + si, p.num_segs, p.status, kSiteBwdSeg)];
       const int a = max(lo, sg.k0), b = min(hi, sg.k1);
       const int full_lo = max(sg.k0, mlo), full_hi = min(sg.k1, mhi);
       for (int kt = sg.k0; kt < sg.k1; kt += kTile, ++j) {
@@ -804,7 +822,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->acc_full, 0, p.status, abort));
     tc_fence_after_sync();
     // epilogue: warpgroup w writes columns [w D / 2, (w + 1) D / 2) of its row of dQ
-    const size_t off = ((size_t)(valid ? local_row(p.qmap, row) : 0) * p.hq + head) * kD + w * (kD / 2);
+    const int lrow = valid ? local_row(p.qmap, row) : 0;
+    const bool store = valid && index_ok(lrow, p.q_rows, p.status, kSiteBwdDq) &&
+                       index_ok(head, p.hq, p.status, kSiteHead);
+    const size_t off = ((size_t)lrow * p.hq + head) * kD + w * (kD / 2);
 #pragma unroll
     for (int c = 0; c < kD / 64; ++c) {
       uint32_t u[32];
@@ -814,7 +835,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) u[i] = 0u;
       }
-      if (ok && valid) {
+      if (ok && store) {
         if (p.accumulate)
           add_f32x32(static_cast<float*>(p.dq) + off + c * 32, u, p.scale);
         else if (p.grad_fp32)

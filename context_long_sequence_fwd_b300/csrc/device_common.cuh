@@ -7,6 +7,49 @@
 
 namespace ra {
 
+// ------------------------------------------------------------ debug checks
+// The debug build (compiled with -DRINGATTN_DEBUG into libringattn_debug.so)
+// checks every computed global index before it is used.  An index outside
+// its array records RA_ERR_BOUNDS (-7) in the status word and, for the first
+// failure only, (site << 48 | index) in the 8 bytes after it; the access is
+// then skipped (a store) or made at element 0 (a load), so nothing outside
+// the buffers is touched and nothing traps.  In the normal build every check
+// is the constant true and compiles to nothing.
+#ifdef RINGATTN_DEBUG
+constexpr bool kBoundsChecks = true;
+#else
+constexpr bool kBoundsChecks = false;
+#endif
+
+// Where a failed check was made (the site recorded with the index).
+enum CheckSite : int {
+  kSiteFwdItem = 1, kSiteFwdSeg, kSiteFwdQRow, kSiteFwdKvRow, kSiteFwdOut, kSiteFwdLse,
+  kSiteFwdPart, kSiteBwdItem, kSiteBwdSeg, kSiteBwdQRow, kSiteBwdKvRow, kSiteBwdRowStat,
+  kSiteBwdDq, kSiteBwdDkDv, kSiteMerge, kSiteSplitMerge, kSitePreprocess, kSiteSimtFwd,
+  kSiteSimtBwd, kSiteHead, kSiteSsd
+};
+
+__device__ __forceinline__ bool index_ok(long long i, long long n, int* status, int site) {
+  if constexpr (!kBoundsChecks) {
+    return true;
+  } else {
+    if (i >= 0 && i < n) return true;
+    if (status != nullptr) {
+      atomicCAS(status, 0, -7 /* RA_ERR_BOUNDS */);
+      unsigned long long* where = reinterpret_cast<unsigned long long*>(status + 2);
+      atomicCAS(where, 0ull,
+                (static_cast<unsigned long long>(site) << 48) |
+                    (static_cast<unsigned long long>(i) & 0xFFFFFFFFFFFFull));
+    }
+    return false;
+  }
+}
+
+// A load index: i itself, or 0 (after recording the failure) when outside [0, n).
+__device__ __forceinline__ long long checked(long long i, long long n, int* status, int site) {
+  return index_ok(i, n, status, site) ? i : 0;
+}
+
 // Where global token t lives in a buffer: chunk [a0, b0) holds rows
 // [0, b0 - a0) and chunk [a1, ...) the rows after them.  Whole-sequence
 // buffers use the identity (a0 = 0, b0 = INT_MAX); one rank's shard-local
@@ -50,6 +93,10 @@ struct FwdParams {
   // their lse at part_lse + s * 2 * 128
   float* part_o;
   float* part_lse;
+  // extents for the debug build's checks
+  int num_segs;           // entries of segs
+  int num_parts;          // partial-result slots
+  int q_rows, k_rows;     // rows of the q / out buffers and of the k, v buffers
 };
 
 struct BwdParams {
@@ -80,6 +127,9 @@ struct BwdParams {
   RowMap kmap;              // rows of k, v, dk and dv
   int lse_stride;           // rows per head of lse and Dvec
   int accumulate;           // 1: add into fp32 dq, dk, dv instead of writing them
+  // extents for the debug build's checks
+  int num_segs, num_bsegs;  // entries of segs and bsegs
+  int q_rows, k_rows;       // rows of the q-side buffers and of the k-side buffers
 };
 
 // Context-parallel selective scan (Mamba2 SSD), fp32.

@@ -26,11 +26,12 @@ template <int D>
 __global__ void __launch_bounds__(256) fwd_simt_fp32_kernel(FwdParams p) {
   __shared__ float Ks[kKeys][D];
   __shared__ float Vs[kKeys][D];
-  const PlanItem it = p.items[blockIdx.x];
+  const PlanItem it = p.items[checked(blockIdx.x, p.num_items, p.status, kSiteSimtFwd)];
   const int tile = threadIdx.x >> 7, r = threadIdx.x & 127;
   const int row = it.q0[tile] + r;
-  const bool valid = r < it.qlen[tile];
   const int h = it.head[tile];
+  const bool valid = r < it.qlen[tile] && index_ok(row, p.q_rows, p.status, kSiteSimtFwd) &&
+                     index_ok(h, p.hq, p.status, kSiteHead);
   const int g = it.head[0] / p.group;
   const float* q = static_cast<const float*>(p.q);
   const float* k = static_cast<const float*>(p.k);
@@ -53,7 +54,7 @@ __global__ void __launch_bounds__(256) fwd_simt_fp32_kernel(FwdParams p) {
   float m = -INFINITY, l = 0.f;
 
   for (int si = 0; si < it.seg_count; ++si) {
-    const PlanSegment seg = p.segs[it.seg_begin + si];
+    const PlanSegment seg = p.segs[checked(it.seg_begin + si, p.num_segs, p.status, kSiteSimtFwd)];
     if (!seg_selected(seg, p.step_filter)) continue;
     const int a = max(lo, seg.k0), b = min(hi, seg.k1);
     for (int kt = seg.k0; kt < seg.k1; kt += kKeys) {
@@ -61,7 +62,7 @@ __global__ void __launch_bounds__(256) fwd_simt_fp32_kernel(FwdParams p) {
       for (int x = threadIdx.x; x < kKeys * D; x += blockDim.x) {
         const int j = x / D, d = x % D, key = kt + j;
         float kv = 0.f, vv = 0.f;
-        if (key < seg.k1) {
+        if (key < seg.k1 && index_ok(key, p.k_rows, p.status, kSiteSimtFwd)) {
           kv = k[((size_t)key * p.hkv + g) * D + d];
           vv = v[((size_t)key * p.hkv + g) * D + d];
         }
@@ -109,7 +110,9 @@ __global__ void __launch_bounds__(256) fwd_simt_fp32_kernel(FwdParams p) {
 #pragma unroll
     for (int d = 0; d < D; ++d) out[ob + d] = __float2bfloat16_rn(empty ? 0.f : o[d] / l);
   }
-  p.lse[(size_t)h * p.lse_stride + row] = empty ? -INFINITY : m + logf(l);
+  if (index_ok((long long)h * p.lse_stride + row, (long long)p.hq * p.lse_stride, p.status,
+               kSiteSimtFwd))
+    p.lse[(size_t)h * p.lse_stride + row] = empty ? -INFINITY : m + logf(l);
 }
 
 }  // namespace

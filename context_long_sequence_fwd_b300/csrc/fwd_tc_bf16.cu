@@ -118,7 +118,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
 __device__ __forceinline__ int item_tiles(const PlanItem& it, const FwdParams& p) {
   int n = 0;
   for (int si = 0; si < it.seg_count; ++si) {
-    const PlanSegment sg = p.segs[it.seg_begin + si];
+    const PlanSegment sg = p.segs[checked(it.seg_begin + si, p.num_segs, p.status, kSiteFwdSeg)];
     if (seg_selected(sg, p.step_filter)) n += (sg.k1 - sg.k0 + kBN - 1) / kBN;
   }
   return n;
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&ctl->sched_full[s]);
         ++spos;
         if (k < 0) break;
-        const PlanItem it = p.items[k];
+        const PlanItem it = p.items[checked(k, p.num_items, p.status, kSiteFwdItem)];
         const int n = item_tiles(it, p);
         if (n == 0) continue;
         const bool has_b = it.qlen[1] > 0;
@@ -229,6 +229,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive_expect_tx(&ctl->q_full, (has_b ? 2 : 1) * kTileBytes);
         const int qa = local_row(p.qmap, it.q0[0]), qb = local_row(p.qmap, it.q0[1]);
+        index_ok(qa, p.q_rows, p.status, kSiteFwdQRow);
+        index_ok(it.head[0], p.hq, p.status, kSiteHead);
+        if (has_b) {
+          index_ok(qb, p.q_rows, p.status, kSiteFwdQRow);
+          index_ok(it.head[1], p.hq, p.status, kSiteHead);
+        }
+        index_ok(g, p.hkv, p.status, kSiteHead);
         for (int hf = 0; hf < kD / 64; ++hf) {
           tma_load_3d(smem + kOffQ + hf * kHalfBytes, &map_q, &ctl->q_full, hf * 64, it.head[0],
                       qa);
@@ -238,7 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++items;
         for (int si = 0; si < it.seg_count && ok; ++si) {
-          const PlanSegment sg = p.segs[it.seg_begin + si];
+          const PlanSegment sg =
+              p.segs[checked(it.seg_begin + si, p.num_segs, p.status, kSiteFwdSeg)];
           if (!seg_selected(sg, p.step_filter)) continue;
           for (int kt = sg.k0; kt < sg.k1 && ok; kt += kBN) {
             for (int kv = 0; kv < 2; ++kv, ++li) {
@@ -250,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               mbar_arrive_expect_tx(&ctl->kv_full[slot], kTileBytes);
               const CUtensorMap* map = kv == 0 ? &map_k : &map_v;
+              index_ok(local_row(p.kmap, kt), p.k_rows, p.status, kSiteFwdKvRow);
               for (int hf = 0; hf < kD / 64; ++hf)
                 tma_load_3d(smem + kOffKV + slot * kTileBytes + hf * kHalfBytes, map,
                             &ctl->kv_full[slot], hf * 64, g, local_row(p.kmap, kt));
@@ -283,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (;;) {
         const int k = next_item(&spos, &ok);
         if (k < 0) break;
-        const PlanItem it = p.items[k];
+        const PlanItem it = p.items[checked(k, p.num_items, p.status, kSiteFwdItem)];
         const int n = item_tiles(it, p);
         if (n == 0) continue;
         const bool has_b = it.qlen[1] > 0;
@@ -353,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (;;) {
       const int k = next_item(&spos, &ok);
       if (k < 0) break;
-      const PlanItem it = p.items[k];
+      const PlanItem it = p.items[checked(k, p.num_items, p.status, kSiteFwdItem)];
       if (x == 1 && it.qlen[1] == 0) continue;
       const int n = item_tiles(it, p);
       // x is uniform per warp: select fields instead of indexing the item
@@ -368,7 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float l = 0.f;
       int j = 0;
       for (int si = 0; si < it.seg_count && ok; ++si) {
-        const PlanSegment sg = p.segs[it.seg_begin + si];
+        const PlanSegment sg =
+            p.segs[checked(it.seg_begin + si, p.num_segs, p.status, kSiteFwdSeg)];
         if (!seg_selected(sg, p.step_filter)) continue;
         const int a = max(lo, sg.k0), b = min(hi, sg.k1);
         const int full_lo = max(sg.k0, mlo), full_hi = min(sg.k1, mhi);
@@ -464,6 +474,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // half of a split item: its partial (O / l, lse) goes to its fp32 slot
       const bool to_part = it.part >= 0;
       const size_t pslot = ((size_t)it.part * 2 + x) * 128 + r;
+      const bool store = valid && (to_part ? index_ok(pslot, (long long)p.num_parts * 256, p.status,
+                                                      kSiteFwdPart)
+                                           : index_ok(lrow, p.q_rows, p.status, kSiteFwdOut) &&
+                                                 index_ok(head, p.hq, p.status, kSiteHead));
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t u[32];
@@ -473,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) u[i] = 0u;
         }
-        if (valid) {
+        if (store) {
           if (to_part || p.out_fp32) {
             float* base = to_part ? p.part_o + pslot * kD : static_cast<float*>(p.out) + ob;
             float4* dst = reinterpret_cast<float4*>(base + c * 32);
@@ -498,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (valid) {
+      if (store) {
         const float L = empty ? -INFINITY : (m2 + log2f(l)) * 0.69314718055994530942f;
         if (to_part)
           p.part_lse[pslot] = L;

@@ -35,17 +35,18 @@ cudaError_t launch_fwd_tc_bf16(const FwdParams& p, const CUtensorMap& map_q,
 // them is fp32 when its *_fp32 flag is set, else bf16.  lse_* are [heads, rows].
 cudaError_t launch_lse_merge(const void* o_a, bool a_fp32, const float* lse_a, const void* o_b,
                              bool b_fp32, const float* lse_b, void* o_out, bool out_fp32,
-                             float* lse_out, int rows, int heads, int D, cudaStream_t stream);
+                             float* lse_out, int rows, int heads, int D, int* status,
+                             cudaStream_t stream);
 
 // Folds the two halves of each split item of the fused forward (fp32 partial
 // slots) into out [T, Hq, D] (bf16, or fp32 when out_fp32) and lse [Hq, lse_stride].
 cudaError_t launch_split_merge(const SplitPair* pairs, int num_pairs, const float* part_o,
                                const float* part_lse, void* out, bool out_fp32, float* lse,
-                               int hq, int lse_stride, int D, cudaStream_t stream);
+                               int hq, int lse_stride, int D, int* status, cudaStream_t stream);
 
 // D_i = dO_i . O_i into Dvec [Hq, T] (O, dO fp32 when `fp32`, else bf16).
 cudaError_t launch_bwd_preprocess(const void* out, const void* dout, bool fp32, float* Dvec, int T,
-                                  int hq, int D, cudaStream_t stream);
+                                  int hq, int D, int* status, cudaStream_t stream);
 
 // bf16 backward on tcgen05 (D = 64 or 128): dQ (query-tile-major, over the forward
 // plan) and dK, dV (key-tile-major, over the backward plan).  Tensor maps as

@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(256, 3) lse_merge_kernel(const void* o_a, bool
                                                         bool b_fp32, const float* lse_b,
                                                         void* o_out, bool out_fp32,
                                                         float* lse_out, int rows, int heads,
-                                                        int D, long long pairs) {
+                                                        int D, long long pairs, int* status) {
   const int tpp = D / (8 * kC);  // threads per (row, head) pair; divides 32
   const long long gt = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const long long pair = gt / tpp;
@@ -86,22 +86,29 @@ __global__ void __launch_bounds__(256, 3) lse_merge_kernel(const void* o_a, bool
   int h = 0, row = 0;
   Vec8 x[kC], y[kC];
   size_t idx = 0;
+  const long long n_o = (long long)rows * heads * D, n_l = (long long)rows * heads;
+  bool in = active;
   if (active) {
     row = (int)(pair / heads);
     h = (int)(pair % heads);
-    a = lse_a[(size_t)h * rows + row];
-    b = lse_b[(size_t)h * rows + row];
+    const long long at = checked((long long)h * rows + row, n_l, status, kSiteMerge);
+    a = lse_a[at];
+    b = lse_b[at];
     idx = ((size_t)row * heads + h) * D + (size_t)part * 8 * kC;
+    // the thread's last value lies inside o as well
+    in = index_ok((long long)idx + 8 * kC - 1, n_o, status, kSiteMerge);
     // a side with lse = -inf is read too (its values are then not used)
+    if (in) {
 #pragma unroll
-    for (int c = 0; c < kC; ++c) {
-      x[c] = load8(o_a, a_fp32, idx + 8 * c);
-      y[c] = load8(o_b, b_fp32, idx + 8 * c);
+      for (int c = 0; c < kC; ++c) {
+        x[c] = load8(o_a, a_fp32, idx + 8 * c);
+        y[c] = load8(o_b, b_fp32, idx + 8 * c);
+      }
     }
   }
   // every lane of the pair has read lse_a before any lane overwrites it
   __syncwarp();
-  if (!active) return;
+  if (!in) return;
   const bool ea = a == -INFINITY, eb = b == -INFINITY;
   float L = -INFINITY, wa = 0.f, wb = 0.f;
   if (!ea && !eb) {
@@ -124,7 +131,8 @@ __global__ void __launch_bounds__(256, 3) lse_merge_kernel(const void* o_a, bool
                   : (eb ? x[c].x[i] : fmaf(wa, x[c].x[i], wb * y[c].x[i]));
     store8(o_out, out_fp32, idx + 8 * c, r);
   }
-  if (part == 0) lse_out[(size_t)h * rows + row] = L;
+  if (part == 0 && index_ok((long long)h * rows + row, n_l, status, kSiteMerge))
+    lse_out[(size_t)h * rows + row] = L;
 }
 
 // The two halves of each split item of the fused forward.  One warp per row
@@ -138,16 +146,20 @@ __global__ void __launch_bounds__(128) split_merge_kernel(const SplitPair* pairs
                                                           const float* part_o,
                                                           const float* part_lse, void* out,
                                                           bool out_fp32, float* lse, int hq,
-                                                          int lse_stride) {
+                                                          int lse_stride, int num_pairs,
+                                                          int* status) {
   constexpr int kV = kD / 32;  // values per lane: 4 (D = 128) or 2 (D = 64)
   const int pair = blockIdx.x >> 6;
   const int x = (blockIdx.x >> 5) & 1;
   const int r = (blockIdx.x & 31) * 4 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  const SplitPair sp = pairs[pair];
+  const SplitPair sp = pairs[checked(pair, num_pairs, status, kSiteSplitMerge)];
   if (r >= sp.qlen[x]) return;
-  const size_t sa = ((size_t)sp.part[0] * 2 + x) * 128 + r;
-  const size_t sb = ((size_t)sp.part[1] * 2 + x) * 128 + r;
+  const long long n_slot = (long long)num_pairs * 2 * 256;  // rows of all partial slots
+  const size_t sa = checked(((long long)sp.part[0] * 2 + x) * 128 + r, n_slot, status,
+                            kSiteSplitMerge);
+  const size_t sb = checked(((long long)sp.part[1] * 2 + x) * 128 + r, n_slot, status,
+                            kSiteSplitMerge);
   const float a = part_lse[sa], b = part_lse[sb];
   float oa[kV], ob[kV];
   if constexpr (kV == 4) {
@@ -179,6 +191,9 @@ __global__ void __launch_bounds__(128) split_merge_kernel(const SplitPair* pairs
 #pragma unroll
   for (int i = 0; i < kV; ++i) o[i] = (ea ? 0.f : wa * oa[i]) + (eb ? 0.f : wb * ob[i]);
   const int row = sp.q0[x] + r;
+  if (!index_ok(row, lse_stride, status, kSiteSplitMerge) ||
+      !index_ok(sp.head[x], hq, status, kSiteHead))
+    return;
   const size_t at = ((size_t)row * hq + sp.head[x]) * kD + lane * kV;
   if (out_fp32) {
 #pragma unroll
@@ -201,15 +216,15 @@ __global__ void __launch_bounds__(128) split_merge_kernel(const SplitPair* pairs
 
 cudaError_t launch_split_merge(const SplitPair* pairs, int num_pairs, const float* part_o,
                                const float* part_lse, void* out, bool out_fp32, float* lse,
-                               int hq, int lse_stride, int D, cudaStream_t stream) {
+                               int hq, int lse_stride, int D, int* status, cudaStream_t stream) {
   if (num_pairs == 0) return cudaSuccess;
   TraceScope trace_scope(stream, "split_merge_kernel");
   if (D == 128)
-    split_merge_kernel<128><<<64 * num_pairs, 128, 0, stream>>>(pairs, part_o, part_lse, out,
-                                                                out_fp32, lse, hq, lse_stride);
+    split_merge_kernel<128><<<64 * num_pairs, 128, 0, stream>>>(
+        pairs, part_o, part_lse, out, out_fp32, lse, hq, lse_stride, num_pairs, status);
   else if (D == 64)
-    split_merge_kernel<64><<<64 * num_pairs, 128, 0, stream>>>(pairs, part_o, part_lse, out,
-                                                               out_fp32, lse, hq, lse_stride);
+    split_merge_kernel<64><<<64 * num_pairs, 128, 0, stream>>>(
+        pairs, part_o, part_lse, out, out_fp32, lse, hq, lse_stride, num_pairs, status);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
@@ -217,7 +232,8 @@ cudaError_t launch_split_merge(const SplitPair* pairs, int num_pairs, const floa
 
 cudaError_t launch_lse_merge(const void* o_a, bool a_fp32, const float* lse_a, const void* o_b,
                              bool b_fp32, const float* lse_b, void* o_out, bool out_fp32,
-                             float* lse_out, int rows, int heads, int D, cudaStream_t stream) {
+                             float* lse_out, int rows, int heads, int D, int* status,
+                             cudaStream_t stream) {
   const long long pairs = (long long)rows * heads;
   if (pairs == 0) return cudaSuccess;
   const int chunks = D / 8 < 4 ? D / 8 : 4;
@@ -227,13 +243,13 @@ cudaError_t launch_lse_merge(const void* o_a, bool a_fp32, const float* lse_a, c
   TraceScope trace_scope(stream, "lse_merge_kernel");
   if (chunks == 4)
     lse_merge_kernel<4><<<grid, block, 0, stream>>>(o_a, a_fp32, lse_a, o_b, b_fp32, lse_b, o_out,
-                                                    out_fp32, lse_out, rows, heads, D, pairs);
+                                                    out_fp32, lse_out, rows, heads, D, pairs, status);
   else if (chunks == 2)
     lse_merge_kernel<2><<<grid, block, 0, stream>>>(o_a, a_fp32, lse_a, o_b, b_fp32, lse_b, o_out,
-                                                    out_fp32, lse_out, rows, heads, D, pairs);
+                                                    out_fp32, lse_out, rows, heads, D, pairs, status);
   else
     lse_merge_kernel<1><<<grid, block, 0, stream>>>(o_a, a_fp32, lse_a, o_b, b_fp32, lse_b, o_out,
-                                                    out_fp32, lse_out, rows, heads, D, pairs);
+                                                    out_fp32, lse_out, rows, heads, D, pairs, status);
   return cudaGetLastError();
 }
 

@@ -68,7 +68,8 @@ typedef enum {
   RA_ERR_UNSUPPORTED = -3,   /* dtype / head_dim / device not supported */
   RA_ERR_CUDA = -4,          /* a CUDA runtime call failed */
   RA_ERR_TIMEOUT = -5,       /* a kernel's bounded wait gave up */
-  RA_ERR_WORKSPACE = -6      /* workspace missing or too small */
+  RA_ERR_WORKSPACE = -6,     /* workspace missing or too small */
+  RA_ERR_BOUNDS = -7         /* debug build only: an index failed its bounds check */
 } ra_status;
 
 typedef enum { RA_BF16 = 0, RA_FP32 = 1 } ra_dtype;
@@ -298,6 +299,21 @@ ra_status ringattn_get_status(void* stream);
  * ringattn_get_status would otherwise report (and clear) this timeout.
  */
 ra_status ringattn_selftest_wait_timeout(void* stream);
+
+/*
+ * Debug build.  libringattn_debug.so is this library compiled with
+ * RINGATTN_DEBUG: every kernel checks each global index it computes (work-list
+ * entries, tensor rows and heads, output, lse and partial-result offsets)
+ * against its array's extent before using it.  A failed check records
+ * RA_ERR_BOUNDS in the status word (read by ringattn_get_status) and skips the
+ * access (a load reads element 0 instead), so the kernel neither touches
+ * memory outside its buffers nor traps.  ringattn_debug_report synchronises
+ * `stream`, stores the first failed check since its last call as a site
+ * number and the index (both 0 if none), clears it, and returns 1 in the
+ * debug build, 0 in the normal build (which makes no checks) and -1 on a CUDA
+ * error.
+ */
+int ringattn_debug_report(void* stream, long long* site, long long* index);
 
 /* Static text for a status code. */
 const char* ringattn_status_string(int status);

@@ -118,3 +118,16 @@ def test_rank_step_argument_errors_without_gpu(lib):
     b = lib.ringattn_bwd_rank_step
     assert b(16, 16, 16, 16, 16, 16, None, dims(), 2, 0, 1, 0, 0, 16, 16, 16, None, 0,
              None) == -6
+
+
+def test_debug_library_loads_and_exports_every_symbol():
+    """The bounds-checking build exports the same C ABI; its status string
+    for a failed check exists."""
+    import ctypes as ct
+    if not os.path.exists(ra_build.LIB_DEBUG):
+        ra_build.build(debug=True)
+    dbg = ct.CDLL(ra_build.LIB_DEBUG)
+    missing = [n for n in declared_functions() if not hasattr(dbg, n)]
+    assert not missing, missing
+    dbg.ringattn_status_string.restype = ct.c_char_p
+    assert b"bounds" in dbg.ringattn_status_string(-7)

@@ -1,0 +1,116 @@
+"""The bounds-checking build (libringattn_debug.so) on the small edge cases.
+
+The debug build checks every global index its kernels compute against the
+array it indexes; a failed check records RA_ERR_BOUNDS and the (site, index)
+of the first failure and skips the access instead of trapping.  It stands in
+for a memory checker: the edge cases below (ragged tiles, zigzag chunks
+shorter than a tile, packed and empty documents, GQA groups, head dimension
+64, the fp32 path, split forward items, the stepwise and multi-GPU ring
+forms, the backward with bf16 and fp32 gradients) must run with a clean
+status word, no recorded failure, and results that still match the oracle.
+The cases run in a child process that sets RINGATTN_DEBUG=1, which makes the
+binding load the debug library.
+"""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+SCRIPT = r"""
+import json, sys
+import numpy as np, torch
+sys.path.insert(0, ROOT)
+import context_long_sequence_fwd_b300 as ra
+assert ra.DEBUG and ra.LIB_PATH.endswith("libringattn_debug.so"), ra.LIB_PATH
+import oracle
+from context_long_sequence_fwd_b300 import ring
+from context_long_sequence_fwd_b300.workloads import make_qkv
+
+dev = "cuda:0"
+failures, worst = [], {}
+
+def err(a, b):
+    a = a.detach().float().cpu().numpy() if hasattr(a, "detach") else a
+    return float(np.max(np.abs(np.asarray(a, np.float64) - b))) if np.size(b) else 0.0
+
+def clean(name):
+    st = ra.ringattn_get_status()
+    checks, site, index = ra.debug_report()
+    assert checks, "the debug library makes checks"
+    if st != 0 or site != 0:
+        failures.append([name, st, site, index])
+
+CASES = [  # T, hq, hkv, d, P, layout, causal, cu
+    (1000, 2, 2, 128, 2, ra.CONTIGUOUS, True, None),
+    (1040, 4, 1, 128, 4, ra.ZIGZAG, True, None),
+    (16, 2, 1, 128, 2, ra.ZIGZAG, True, None),
+    (2, 1, 1, 128, 1, ra.CONTIGUOUS, True, None),
+    (2048, 4, 2, 128, 8, ra.CONTIGUOUS, True, [0, 300, 301, 900, 1500, 2048]),
+    (1024, 2, 2, 128, 2, ra.CONTIGUOUS, True, [0, 200, 200, 700, 1024]),
+    (1536, 8, 2, 128, 3, ra.CONTIGUOUS, False, None),
+    (1024, 16, 2, 128, 4, ra.ZIGZAG, True, None),
+    (1024, 4, 4, 64, 2, ra.ZIGZAG, True, [0, 100, 100, 700, 1024]),
+]
+for i, (T, hq, hkv, d, P, lay, causal, cu) in enumerate(CASES):
+    q, k, v, do = make_qkv(T, hq, hkv, d, "bf16", seed=50 + i, with_dout=True)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    ro, rl = oracle.attention_fwd(q, k, v, causal=causal, cu_seqlens=cu)
+    rq, rk, rv, _, _ = oracle.attention_bwd(q, k, v, do, causal=causal, cu_seqlens=cu)
+    o, l = ra.ringattn_fwd(qd, kd, vd, cu, P, lay, causal)
+    clean(f"fwd {i}")
+    worst[f"fwd {i}"] = max(err(o, ro), err(l, rl) * 20)
+    o2, l2 = ra.ringattn_fwd_stepwise(qd, kd, vd, cu, P, lay, causal)
+    clean(f"stepwise {i}")
+    worst[f"stepwise {i}"] = max(err(o2, ro), err(l2, rl) * 20)
+    # dK, dV sum over the G query heads of a group, and P, dS reach the tensor
+    # cores as bf16, so their rounding grows with G: the 2e-2 bound of the
+    # workloads (groups of 4) is scaled by G / 4 for larger groups
+    gs = max(1.0, (hq // hkv) / 4)
+    for gf in (True, False):
+        g = ra.ringattn_bwd(qd, kd, vd, o, l, dod, cu, P, lay, causal, grad_fp32=gf)
+        clean(f"bwd {i} fp32grad={gf}")
+        if gf:
+            worst[f"bwd {i}"] = max(err(a, b) for a, b in zip(g, (rq, rk, rv))) / gs
+    o3, l3 = ring.emulate_ring_fwd(qd, kd, vd, num_shards=P, layout=lay, causal=causal,
+                                   cu_seqlens=cu)
+    g3 = ring.emulate_ring_bwd(qd, kd, vd, o3, l3, dod, num_shards=P, layout=lay,
+                               causal=causal, cu_seqlens=cu)
+    clean(f"ring {i}")
+    worst[f"ring {i}"] = max([err(o3, ro), err(l3, rl) * 20] +
+                             [err(a, b) / gs for a, b in zip(g3, (rq, rk, rv))])
+# the fp32 path
+q, k, v, do = make_qkv(300, 4, 2, 64, "fp32", seed=60, with_dout=True)
+o, l = ra.ringattn_fwd(q.to(dev), k.to(dev), v.to(dev), [0, 37, 38, 300], 3, ra.CONTIGUOUS, True)
+g = ra.ringattn_bwd(q.to(dev), k.to(dev), v.to(dev), o, l, do.to(dev), [0, 37, 38, 300], 3,
+                    ra.CONTIGUOUS, True)
+clean("fp32")
+ro, rl = oracle.attention_fwd(q, k, v, causal=True, cu_seqlens=[0, 37, 38, 300])
+worst["fp32"] = max(err(o, ro), err(l, rl)) * 1000
+# the standalone merge
+oa, ob = torch.randn(257, 3, 128, device=dev), torch.randn(257, 3, 128, device=dev)
+la, lb = torch.randn(3, 257, device=dev), torch.randn(3, 257, device=dev)
+ra.attn_lse_merge(oa, la, ob, lb)
+clean("merge")
+print(json.dumps({"failures": failures, "worst": worst}))
+"""
+
+
+def test_debug_build_edge_cases_are_clean():
+    from context_long_sequence_fwd_b300 import build as ra_build
+    if not os.path.exists(ra_build.LIB_DEBUG):
+        ra_build.build(debug=True)
+    env = dict(os.environ, RINGATTN_DEBUG="1")
+    r = subprocess.run([sys.executable, "-c", f"ROOT = {ROOT!r}\n" + SCRIPT], env=env,
+                       capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-3000:]
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    assert res["failures"] == [], res["failures"]
+    # outputs within the bf16 bounds (lse scaled by 20, fp32 by 1000 and the
+    # gradients of groups larger than 4 by 4 / G onto 2e-2)
+    bad = {k: v for k, v in res["worst"].items() if not v <= 2e-2}
+    assert not bad, bad
