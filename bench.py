@@ -70,6 +70,25 @@ def power_capped(clk: dict) -> bool:
                 and mhz < 0.9 * top)
 
 
+def workload_config(w, cu, pass_, world, seed) -> dict:
+    """The `config` object of the JSON line, the same for both arms."""
+    f_step = fwd_flops(w, cu) * (3.5 if pass_ == "fwdbwd" else 1.0)
+    elem = 2 if w.dtype == "bf16" else 4
+    read_mb = (w.total_tokens * (w.hq + 2 * w.hkv) * w.head_dim * elem
+               + (2 * w.total_tokens * w.hq * w.head_dim * elem if pass_ == "fwdbwd" else 0)) / 1e6
+    return {"workload": w.name, "total_tokens": w.total_tokens, "hq": w.hq, "hkv": w.hkv,
+            "head_dim": w.head_dim, "num_shards": w.num_shards,
+            "layout": "zigzag" if w.layout == 1 else "contiguous",
+            "causal": w.causal, "varlen_docs": None if cu is None else len(cu) - 1,
+            "kv_exchange": "allgather" if w.kv_exchange else "ring",
+            "heads_k_stride": w.heads_k_stride,
+            "pass": pass_, "flops_per_step": f_step,
+            "visible_pairs_per_head": visible_pairs(w, cu),
+            "parallelism": f"replicas{world}" if world > 1 else "1gpu",
+            "l2": "inputs larger than L2 (%.0f MB read per step), no flush" % read_mb,
+            "seed": seed}
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -477,19 +496,7 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q, k, v, dO rounded to bf16)",
-        "config": {"workload": args.workload, "total_tokens": w.total_tokens, "hq": w.hq,
-                   "hkv": w.hkv, "head_dim": w.head_dim, "num_shards": w.num_shards,
-                   "layout": "zigzag" if w.layout == 1 else "contiguous",
-                   "causal": w.causal, "varlen_docs": None if cu is None else len(cu) - 1,
-                   "kv_exchange": "allgather" if w.kv_exchange else "ring",
-                   "heads_k_stride": w.heads_k_stride,
-                   "pass": args.pass_, "flops_per_step": f_step,
-                   "visible_pairs_per_head": visible_pairs(w, cu),
-                   "parallelism": f"replicas{world}" if world > 1 else "1gpu",
-                   "l2": "inputs larger than L2 (%.0f MB read per step), no flush" %
-                         (sum(t.numel() * t.element_size() for t in (q, k, v)) / 1e6 +
-                          (2 * do.numel() * do.element_size() / 1e6 if backward else 0)),
-                   "seed": args.seed},
+        "config": workload_config(w, cu, args.pass_, world, args.seed),
         "fwd": {"ms": round(fwd_mean, 4), "tflops": round(fwd_tf, 2),
                 "frac": round(fwd_tf / peak, 4), "frac_of_sustained": round(fwd_tf / peak_s, 4)},
         "roofline": roof,
@@ -678,9 +685,9 @@ def run_reference(args):
         "ms_per_full_step_extrapolated": round(f_step / (value * 1e12) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) q, k, v, dO rounded to bf16)",
-        "config": {"workload": args.workload, "total_tokens": w.total_tokens, "hq": w.hq,
-                   "hkv": w.hkv, "head_dim": w.head_dim, "num_shards": w.num_shards,
-                   "pass": args.pass_, "sampled": True},
+        "config": workload_config(w, x["cu_seqlens"], args.pass_, world, args.seed),
+        "sampled": "each step times the oracle on a bounded random sample of the workload's "
+                   "rows (see cpu_baseline.sample)",
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
                          "sample": f"per step: {descs[0]} (random head and row); "
                                    f"{args.steps} steps, {ts:.1f} s"},

@@ -951,6 +951,7 @@ ra_status ssd_cp_fwd(const float* x, const float* dt, const float* A, const floa
   p.G = dims.groups;
   p.N = dims.state_dim;
   p.R = num_shards;
+  p.status = ds->status;
   return launch_ssd_cp(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? RA_OK
                                                                             : RA_ERR_CUDA;
 }

@@ -147,6 +147,7 @@ struct SsdParams {
   float* incoming;       // workspace [R, H, P, N]: the state each rank receives
   float* carry;          // workspace [R, H]: how much of an incoming state survives a chunk
   int T, H, G, N, R;     // tokens, heads, groups, state size, ranks (shards)
+  int* status;           // device status word (the debug build's checks)
 };
 
 // Start and end of the document holding token t (binary search over cu).

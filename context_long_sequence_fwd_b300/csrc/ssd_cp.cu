@@ -189,6 +189,12 @@ __global__ void __launch_bounds__(kThreads, 4) ssd_chunk_scan_kernel(const SsdPa
   const int rp = threadIdx.x >> 3, cs = threadIdx.x & 7;
   const int L = p.T / p.R;
   const int c0 = r * L;
+  // every index below is the CTA's head, group and rank plus offsets inside
+  // [0, kP), [0, N) and the chunk's rows: checking those checks them all
+  if (!index_ok(h, p.H, p.status, kSiteSsd) || !index_ok(g, p.G, p.status, kSiteSsd) ||
+      !index_ok(r, p.R, p.status, kSiteSsd) ||
+      !index_ok((long long)c0 + L - 1, p.T, p.status, kSiteSsd))
+    return;
   const float A = p.A[h];
   const float Dh = p.D ? p.D[h] : 0.f;
   // rows 2 rp and 2 rp + 1 of S~, two adjacent columns per 64-bit register
@@ -294,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 4) ssd_chunk_scan_kernel(const SsdPa
 // the last rank.  One CTA per head; each thread owns P N / 256 entries.
 __global__ void __launch_bounds__(kThreads) ssd_state_pass_kernel(const SsdParams p) {
   const int h = blockIdx.x;
+  if (!index_ok(h, p.H, p.status, kSiteSsd)) return;
   const int per = kP * p.N;
   for (int e = threadIdx.x; e < per; e += kThreads) {
     float Hs = 0.f;  // rank 0 starts from zero
@@ -332,6 +339,10 @@ __global__ void __launch_bounds__(kThreads) ssd_correction_kernel(const SsdParam
   CorrStage<N>& st = *reinterpret_cast<CorrStage<N>*>(smem_raw);
   const int h = blockIdx.x, r = blockIdx.y + 1;
   const int g = h / (p.H / p.G);
+  if (!index_ok(h, p.H, p.status, kSiteSsd) || !index_ok(g, p.G, p.status, kSiteSsd) ||
+      !index_ok(r, p.R, p.status, kSiteSsd) ||
+      !index_ok((long long)(r + 1) * (p.T / p.R) - 1, p.T, p.status, kSiteSsd))
+    return;
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int L = p.T / p.R;

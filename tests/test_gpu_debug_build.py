@@ -91,6 +91,17 @@ g = ra.ringattn_bwd(q.to(dev), k.to(dev), v.to(dev), o, l, do.to(dev), [0, 37, 3
 clean("fp32")
 ro, rl = oracle.attention_fwd(q, k, v, causal=True, cu_seqlens=[0, 37, 38, 300])
 worst["fp32"] = max(err(o, ro), err(l, rl)) * 1000
+# the Mamba2 scan (ragged token blocks, packed samples)
+from context_long_sequence_fwd_b300.workloads import make_ssd_inputs, position_ids_from_lengths
+inp = make_ssd_inputs(1000, 4, 64, 128, 2, seed=3, packed=False)
+inp["position_ids"] = position_ids_from_lengths([300, 5, 1, 694])
+t = {kk: (None if vv is None else vv.to(dev)) for kk, vv in inp.items()}
+y, hT = ra.ssd_cp_fwd(t["x"], t["dt"], t["A"], t["B"], t["C"], t["D"], t["position_ids"], 4,
+                      want_final_state=True)
+clean("ssd")
+ry, rh = oracle.ssd_scan(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                         inp["position_ids"])
+worst["ssd"] = err(y, ry) / max(1.0, float(np.max(np.abs(ry)))) * 1000
 # the standalone merge
 oa, ob = torch.randn(257, 3, 128, device=dev), torch.randn(257, 3, 128, device=dev)
 la, lb = torch.randn(3, 257, device=dev), torch.randn(3, 257, device=dev)
@@ -110,7 +121,8 @@ def test_debug_build_edge_cases_are_clean():
     assert r.returncode == 0, r.stderr[-3000:]
     res = json.loads(r.stdout.strip().splitlines()[-1])
     assert res["failures"] == [], res["failures"]
-    # outputs within the bf16 bounds (lse scaled by 20, fp32 by 1000 and the
-    # gradients of groups larger than 4 by 4 / G onto 2e-2)
+    # outputs within the bf16 bounds (lse scaled by 20, fp32 by 1000, the scan's
+    # relative error by 1000 and the gradients of groups larger than 4 by 4 / G
+    # onto 2e-2)
     bad = {k: v for k, v in res["worst"].items() if not v <= 2e-2}
     assert not bad, bad

@@ -5,8 +5,9 @@ only hands out input and output buffers, cannot call cudaMalloc where they
 run attention.  ringattn_fwd_stepwise_noalloc serves them from a fixed
 library-owned scratch array.  This file checks, through the C ABI, that two
 calls in a row give the same result as the workspace-taking
-ringattn_fwd_stepwise (within the parity tolerances the other tests use), and
-that a problem too large for the array is refused before any launch.  It is
+ringattn_fwd_stepwise (within the parity tolerances the other tests use),
+that the result matches the fp64 oracle, and that a problem too large for
+the array is refused before any launch.  It is
 named so that pytest collects it last.
 """
 import ctypes
@@ -66,6 +67,18 @@ def test_two_calls_match_the_workspace_entry_point():
         for o, l in (first, second):
             assert max_err(to_np(o), to_np(ref_o)) <= tol_o
             assert max_err(to_np(l), to_np(ref_l)) <= tol_l
+
+
+def test_result_matches_the_oracle():
+    """The same cases against the fp64 oracle's whole-sequence attention."""
+    import oracle
+    for (T, hq, hkv, d, dt, P, layout, causal, cu) in CASES:
+        qc, kc, vc = make_qkv(T, hq, hkv, d, dt, seed=T)
+        o, l = call_noalloc(qc.to(DEV), kc.to(DEV), vc.to(DEV), cu, P, layout, causal)
+        assert ra.ringattn_get_status() == 0
+        ro, rl = oracle.attention_fwd(qc, kc, vc, causal=causal, cu_seqlens=cu)
+        tol_o, tol_l = (TOL_FP32, TOL_FP32) if dt == "fp32" else (TOL_BF16_O, TOL_BF16_LSE)
+        assert max_err(to_np(o), ro) <= tol_o and max_err(to_np(l), rl) <= tol_l
 
 
 def test_oversized_problem_is_refused():
