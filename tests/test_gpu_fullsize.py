@@ -9,7 +9,8 @@ workloads, not a sample:
   forward then backward with bf16 gradients, exactly as the bench runs it):
   every row of query heads 0-3 and 28-31 for O, lse and dQ, and every key of
   key/value heads 0 and 7 for dK and dV (heads are independent, and a key
-  head's gradients need exactly its group's query heads);
+  head's gradients need exactly its group's query heads); the same outputs
+  of the stepwise forward and of the multi-GPU ring emulated on this GPU;
 * packed documents, 65536 tokens, 8 contiguous shards that split documents:
   every row of query heads 0-3 and 28-31.
 
@@ -59,28 +60,70 @@ def test_causal_mha_t8192_p4_zigzag_every_output():
     assert max_err(to_np(lse), rl) <= TOL_BF16_LSE
 
 
-def test_causal_gqa_t32768_p8_zigzag_benched_step_every_row_of_edge_groups():
-    """The benched step (fused forward, then the backward with bf16 dq, dk,
-    dv) against the oracle on q heads 0-3, 28-31 and kv heads 0, 7."""
+@pytest.fixture(scope="module")
+def gqa32k():
+    """The 32K workload's inputs and the oracle's O, lse, dQ (q heads 0-3,
+    28-31), dK and dV (kv heads 0, 7), computed once for the tests below."""
     w = WORKLOADS["causal_gqa_t32768_p8_zigzag"]
     x = make_inputs(w, seed=0, with_dout=True)
+    kvh = [0, w.hkv - 1]
+    rq, rk, rv, _, rl, ro = oracle.blas.attention_bwd(x["q"], x["k"], x["v"], x["dout"],
+                                                      causal=True, kv_heads=kvh,
+                                                      return_out=True)
+    return w, x, kvh, dict(o=ro, lse=rl, dq=rq, dk=rk, dv=rv)
+
+
+def check_edge_groups(ref, kvh, out=None, lse=None, dq=None, dk=None, dv=None, grad_bf16=False):
+    h = EDGE_HEADS
+    if out is not None:
+        assert max_err(to_np(out[:, h]), ref["o"][:, h]) <= TOL_BF16_O
+        assert max_err(to_np(lse[h]), ref["lse"][h]) <= TOL_BF16_LSE
+    if dq is None:
+        return
+    for got, r in ((to_np(dq[:, h]), ref["dq"][:, h]), (to_np(dk[:, kvh]), ref["dk"][:, kvh]),
+                   (to_np(dv[:, kvh]), ref["dv"][:, kvh])):
+        bound = bf16_output_bound(r, TOL_BF16_O) if grad_bf16 else TOL_BF16_O
+        assert np.all(np.abs(got - r) <= bound), max_err(got, r)
+
+
+def test_causal_gqa_t32768_p8_zigzag_benched_step_every_row_of_edge_groups(gqa32k):
+    """The benched step (fused forward, then the backward with bf16 dq, dk,
+    dv) against the oracle on q heads 0-3, 28-31 and kv heads 0, 7."""
+    w, x, kvh, ref = gqa32k
     q, k, v, out, lse = gpu_forward(w, x)
     do = x["dout"].to(DEV)
     dq, dk, dv = (torch.full_like(t, float("nan")) for t in (q, k, v))
     ra.ringattn_bwd(q, k, v, out, lse, do, None, w.num_shards, w.layout, w.causal, dq, dk, dv)
     assert ra.ringattn_get_status() == 0
-    kvh = [0, w.hkv - 1]
-    rq, rk, rv, _, rl, ro = oracle.blas.attention_bwd(x["q"], x["k"], x["v"], x["dout"],
-                                                      causal=True, kv_heads=kvh,
-                                                      return_out=True)
-    h = EDGE_HEADS
-    assert max_err(to_np(out[:, h]), ro[:, h]) <= TOL_BF16_O
-    assert max_err(to_np(lse[h]), rl[h]) <= TOL_BF16_LSE
-    for got, ref in ((to_np(dq[:, h]), rq[:, h]), (to_np(dk[:, kvh]), rk[:, kvh]),
-                     (to_np(dv[:, kvh]), rv[:, kvh])):
-        assert np.all(np.abs(got - ref) <= bf16_output_bound(ref, TOL_BF16_O)), max_err(got, ref)
+    check_edge_groups(ref, kvh, out, lse, dq, dk, dv, grad_bf16=True)
     for t in (out, lse, dq, dk, dv):
         assert bool(torch.isfinite(t).all())
+
+
+def test_causal_gqa_t32768_p8_zigzag_stepwise_every_row_of_edge_groups(gqa32k):
+    """The literal ring form (one launch per ring step, log-sum-exp merges)
+    at full size."""
+    w, x, kvh, ref = gqa32k
+    q, k, v = (x[n].to(DEV) for n in ("q", "k", "v"))
+    out, lse = ra.ringattn_fwd_stepwise(q, k, v, None, w.num_shards, w.layout, w.causal)
+    assert ra.ringattn_get_status() == 0
+    check_edge_groups(ref, kvh, out, lse)
+
+
+def test_causal_gqa_t32768_p8_zigzag_multi_gpu_ring_emulated(gqa32k):
+    """The multi-GPU ring's schedule with its 8 ranks emulated on this GPU
+    (own buffers and streams per rank, device-to-device shard transfers):
+    forward and fp32-gradient backward against the oracle."""
+    from context_long_sequence_fwd_b300 import ring
+    w, x, kvh, ref = gqa32k
+    q, k, v, do = (x[n].to(DEV) for n in ("q", "k", "v", "dout"))
+    out, lse = ring.emulate_ring_fwd(q, k, v, num_shards=w.num_shards, layout=w.layout,
+                                     causal=w.causal)
+    dq, dk, dv = ring.emulate_ring_bwd(q, k, v, out, lse, do, num_shards=w.num_shards,
+                                       layout=w.layout, causal=w.causal)
+    torch.cuda.synchronize()
+    assert ra.ringattn_get_status() == 0
+    check_edge_groups(ref, kvh, out, lse, dq, dk, dv)
 
 
 def test_varlen_causal_gqa_t65536_p8_contiguous_every_row_of_edge_groups():
