@@ -12,7 +12,9 @@ workloads, not a sample:
   head's gradients need exactly its group's query heads); the same outputs
   of the stepwise forward and of the multi-GPU ring emulated on this GPU;
 * packed documents, 65536 tokens, 8 contiguous shards that split documents:
-  every row of query heads 0-3 and 28-31.
+  every O and lse;
+* causal GQA, 65536 tokens, forward then backward (fp32 gradients): every
+  row of query heads 0-3 and 28-31 and every key of KV heads 0 and 7.
 
 The ring schedule reaches the whole-sequence result by re-ordering the sum
 (axolotl "Sequence Parallelism" page, introduction: results aggregated
@@ -126,12 +128,34 @@ def test_causal_gqa_t32768_p8_zigzag_multi_gpu_ring_emulated(gqa32k):
     check_edge_groups(ref, kvh, out, lse, dq, dk, dv)
 
 
-def test_varlen_causal_gqa_t65536_p8_contiguous_every_row_of_edge_groups():
+def test_varlen_causal_gqa_t65536_p8_contiguous_every_output():
+    """The packed workload in full: every O and lse of all 32 query heads."""
     w = WORKLOADS["varlen_causal_gqa_t65536_p8_contiguous"]
     x = make_inputs(w, seed=0)
     _, _, _, out, lse = gpu_forward(w, x)
     ro, rl = oracle.blas.attention_fwd(x["q"], x["k"], x["v"], causal=True,
-                                       cu_seqlens=x["cu_seqlens"], heads=EDGE_HEADS)
-    assert max_err(to_np(out[:, EDGE_HEADS]), ro[:, EDGE_HEADS]) <= TOL_BF16_O
-    assert max_err(to_np(lse[EDGE_HEADS]), rl[EDGE_HEADS]) <= TOL_BF16_LSE
-    assert bool(torch.isfinite(out).all()) and bool(torch.isfinite(lse).all())
+                                       cu_seqlens=x["cu_seqlens"])
+    assert max_err(to_np(out), ro) <= TOL_BF16_O
+    assert max_err(to_np(lse), rl) <= TOL_BF16_LSE
+
+
+def test_causal_gqa_fwdbwd_t65536_p8_zigzag_every_row_of_edge_groups():
+    """The 64K fwd+bwd workload on the head subset its check plan names:
+    every row of q heads 0-3 and 28-31 for O, lse and dQ, and every key of
+    kv heads 0 and 7 for dK and dV (fp32 gradient outputs: the strict
+    2e-2 bound)."""
+    w = WORKLOADS["causal_gqa_fwdbwd_t65536_p8_zigzag"]
+    x = make_inputs(w, seed=0, with_dout=True)
+    q, k, v, out, lse = gpu_forward(w, x)
+    do = x["dout"].to(DEV)
+    dq, dk, dv = (torch.full(t.shape, float("nan"), device=DEV) for t in (q, k, v))
+    ra.ringattn_bwd(q, k, v, out, lse, do, None, w.num_shards, w.layout, w.causal, dq, dk, dv,
+                    grad_fp32=True)
+    assert ra.ringattn_get_status() == 0
+    kvh = [0, w.hkv - 1]
+    rq, rk, rv, _, rl, ro = oracle.blas.attention_bwd(x["q"], x["k"], x["v"], x["dout"],
+                                                      causal=True, kv_heads=kvh,
+                                                      return_out=True)
+    check_edge_groups(dict(o=ro, lse=rl, dq=rq, dk=rk, dv=rv), kvh, out, lse, dq, dk, dv)
+    for t in (out, lse, dq, dk, dv):
+        assert bool(torch.isfinite(t).all())
