@@ -126,6 +126,20 @@ bool encode_thd(CUtensorMap* map, const void* ptr, int T, int H, int D) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [T, M, inner] tensor viewed as 3-D (inner, M, T); box inner x 1 x rows,
+// no swizzle (the rows land in shared memory as they are in memory).
+bool encode_f32_rows(CUtensorMap* map, const void* ptr, int T, int M, int inner, int rows) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)M, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)inner * 4, (cuuint64_t)M * inner * 4};
+  cuuint32_t box[3] = {(cuuint32_t)inner, 1, (cuuint32_t)rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 PlanInput make_input(const int32_t* cu_seqlens, const ra_dims& d, int P, int layout, int causal) {
@@ -920,6 +934,10 @@ ra_status ssd_cp_fwd(const float* x, const float* dt, const float* A, const floa
   if ((long long)dims.total_tokens * dims.heads * 64 >= (1LL << 40)) return RA_ERR_UNSUPPORTED;
   if (dims.total_tokens == 0) return RA_OK;
   if (!x || !dt || !A || !B || !C || !y) return RA_ERR_INVALID_ARG;
+  // the kernels move x, B, C and y in 16-byte pieces
+  for (const void* q : {static_cast<const void*>(x), static_cast<const void*>(B),
+                        static_cast<const void*>(C), static_cast<const void*>(y)})
+    if (reinterpret_cast<uintptr_t>(q) & 15u) return RA_ERR_INVALID_ARG;
   const size_t need = ssd_cp_workspace_size(dims, num_shards);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return RA_ERR_WORKSPACE;
@@ -952,8 +970,16 @@ ra_status ssd_cp_fwd(const float* x, const float* dt, const float* A, const floa
   p.N = dims.state_dim;
   p.R = num_shards;
   p.status = ds->status;
-  return launch_ssd_cp(p, static_cast<cudaStream_t>(stream)) == cudaSuccess ? RA_OK
-                                                                            : RA_ERR_CUDA;
+  SsdMaps maps;
+  if (dims.state_dim == 128 &&
+      (!encode_f32_rows(&maps.c, C, dims.total_tokens, dims.groups, 128, 32) ||
+       !encode_f32_rows(&maps.b, B, dims.total_tokens, dims.groups, 128, 32) ||
+       !encode_f32_rows(&maps.x, x, dims.total_tokens, dims.heads, 64, 128)))
+    return RA_ERR_CUDA;
+  return launch_ssd_cp(p, dims.state_dim == 128 ? &maps : nullptr,
+                       static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? RA_OK
+             : RA_ERR_CUDA;
 }
 
 ra_status ringattn_get_status(void* stream) {

@@ -64,6 +64,18 @@ cudaError_t launch_bwd_simt_fp32(const BwdParams& p, cudaStream_t stream);
 
 // Context-parallel selective scan (Mamba2 SSD): chunk scans, state passing
 // and the additive correction (head_dim 64, state size 64 or 128).
-cudaError_t launch_ssd_cp(const SsdParams& p, cudaStream_t stream);
+// `maps` (host memory) describes C, B and x for the tensor-core chunk scan
+// of state size 128 (see SsdMaps); it may be null for state size 64.
+struct SsdMaps {
+  CUtensorMap c;  // C [T, G, 128] fp32 as (state, group, token); box 128 x 1 x 32
+  CUtensorMap b;  // B, the same
+  CUtensorMap x;  // x [T, H, 64] fp32 as (head dim, head, token); box 64 x 1 x 128
+};
+cudaError_t launch_ssd_cp(const SsdParams& p, const SsdMaps* maps, cudaStream_t stream);
+
+// The chunk scan of launch_ssd_cp on the tensor cores (state size 128): y of
+// every rank's chunk from a zero state, the chunks' final states and carries.
+cudaError_t launch_ssd_chunk_scan_tc(const SsdParams& p, const SsdMaps& maps,
+                                     cudaStream_t stream);
 
 }  // namespace ra

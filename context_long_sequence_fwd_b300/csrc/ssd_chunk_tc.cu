@@ -1,0 +1,608 @@
+// Chunk scan of the context-parallel Mamba2 selective scan (SSD) on the
+// sm_103a tensor cores, for state size N = 128.
+//
+// Same contract as ssd_chunk_scan_kernel (ssd_cp.cu): CTA (h, r) scans rank
+// r's chunk of head h from a zero state and writes y of the chunk, the
+// chunk's final state and its carry factor; the state pass and the additive
+// correction that follow are unchanged (axolotl "Sequence Parallelism" page,
+// "Mamba/SSM Hybrid Models": each rank scans its chunk, passes its final
+// state on, and a linear correction accounts for the state it did not start
+// from).
+//
+// The recurrence S <- exp(dt A) S + dt x B^T, y = S C + D x is evaluated a
+// block of Q = 128 tokens at a time in its chunked form.  With
+// l_t = dt_t A log2(e), P_t its running sum over the block, rc_t the number
+// of sample starts (position 0) at or before token t in the block, and S0 the
+// state before the block:
+//   same(t, j) = (j <= t and rc_j == rc_t)            no sample starts in (j, t]
+//   y_t  = [rc_t == 0] 2^P_t (C_t . S0)               the block's incoming state
+//        + sum_j same(t, j) 2^(P_t - P_j) dt_j (C_t . B_j) x_j + D x_t
+//   S    = [rc_end == 0] 2^P_end S0 + sum_j [rc_j == rc_end] 2^(P_end - P_j) dt_j x_j B_j^T
+// as four products on the tensor cores, every one with M = 128:
+//   G    = C B^T           (tokens x tokens, over the state)          TMEM cols   0-127
+//   Yoff = C S0^T          (tokens x head dim, over the state)        TMEM cols 128-191
+//   Ydia = M X, M = G o mask o dt  (tokens x head dim, over tokens)   TMEM cols 192-255
+//   S^T += (v o B)^T X     (state x head dim, over tokens; the fp32   TMEM cols 256-319
+//                           state lives in TMEM across the blocks)
+// The scan is checked to fp32-level accuracy (2e-5 relative), which one
+// 16-bit product per term cannot reach, so every operand a is split into
+// fp16 a_hi + a_lo (a_lo = a - a_hi, rounded again) and each product a b is
+// formed as a_hi b_hi + a_hi b_lo + a_lo b_hi, accumulated in fp32: the
+// dropped a_lo b_lo and the rounding of the lo parts leave about 2^-22 of
+// each product.  fp16 keeps 11 significant bits where bf16 keeps 8; the
+// operands here (inputs of order 1, decay factors <= 1) sit well inside its
+// range.
+//
+// Operands are written into shared memory by the threads (the inputs are
+// fp32 in memory and are split on the way) with the 128-byte swizzle the MMA
+// descriptors describe.  C and M are K-major; B, x, v o B and S0 keep rows of
+// their own K index: B is K-major for G, and read in place as the MN-major A
+// operand of the state update once each row has been scaled by v_j; x is the
+// MN-major B operand of both token contractions, S0 (rows = state) that of
+// Yoff.
+// One CTA per (head, rank), 512 threads; one thread issues the MMAs.  A block
+// runs: G, Yoff issued | the decay scan, while they run | the masked M, the
+// scaling of B by v, the state's decay | Ydia, S^T issued | the next block's
+// rows of C and B loaded into registers, while they run | the next block's
+// operands split into the freed shared memory, S0 out, y out.  Every barrier wait is
+// bounded.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "device_common.cuh"
+#include "launch.h"
+#include "sm103_ptx.cuh"
+#include "trace.h"
+
+namespace ra {
+
+namespace {
+
+constexpr int kQ = 128;       // tokens per block
+constexpr int kP = 64;        // head dimension
+constexpr int kN = 128;       // state size
+constexpr int kThreads = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Each operand is stored as an fp16 hi part followed by its lo part.
+constexpr int kPartCB = kQ * kN * 2;  // 128 rows x 128 fp16: two 16 KB swizzle blocks
+constexpr int kPartX = kQ * kP * 2;   // 128 token rows x 64 fp16
+// B's 128 token rows and S0's 64 head-dim rows share one K-major operand
+// (K = state), so that G and Yoff are one product of N = 192: each 64-value
+// K block holds 192 rows.
+constexpr int kRowsBS = kQ + kP;
+constexpr int kBlkBS = kRowsBS * 128;
+constexpr int kPartBS = 2 * kBlkBS;
+constexpr int kOffC = 0;                      // C; then M
+constexpr int kOffBS = kOffC + 2 * kPartCB;   // B (then v o B) and S0
+constexpr int kOffX = kOffBS + 2 * kPartBS;
+constexpr int kOffVec = kOffX + 2 * kPartX;
+
+struct Vec {
+  // running sum of dt A log2(e) over the block through the token, as an
+  // unevaluated pair hi + lo (summed in float-float arithmetic): differences
+  // of two of them keep fp32 accuracy however large the sums grow
+  float Ph[kQ], Pl[kQ];
+  float dt[kQ];
+  float v[kQ];    // [rc == rc_end] 2^(P_end - P) dt: weight of the token in the final state
+  float w[kQ];    // [rc == 0] 2^P: how much of the incoming state reaches the token
+  int rc[kQ];     // sample starts at or before the token, in the block
+  float wsh[4], wsl[4];  // per-warp totals of the scans
+  int wcnt[4];
+  float Pend;     // P at the block's last token
+  int rcend;
+};
+constexpr int kOffCtl = kOffVec + ((sizeof(Vec) + 127) / 128) * 128;
+
+struct Ctl {
+  uint64_t mma_bar;
+  uint64_t done_bar;
+  uint64_t tma_bar;
+  uint32_t tmem_base;
+  int pad;
+};
+constexpr int kSmem = kOffCtl + 128 + 1024;  // + alignment slack
+static_assert(sizeof(Ctl) <= 128, "control block");
+static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
+
+constexpr uint32_t kColG = 0, kColYoff = 128, kColYdia = 192, kColS = 256;
+
+// Instruction descriptor of kind::f16 with fp16 A and B (format 0) and fp32
+// accumulation; a_mn, b_mn: operand stored MN-major.
+__host__ __device__ constexpr uint32_t make_idesc_f16(uint32_t m, uint32_t n, bool a_mn,
+                                                      bool b_mn) {
+  return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((n >> 3) << 17) |
+         ((m >> 4) << 24);
+}
+constexpr uint32_t kIdescGY = make_idesc_f16(128, 192, false, false);
+constexpr uint32_t kIdescYdia = make_idesc_f16(128, 64, false, true);
+constexpr uint32_t kIdescS = make_idesc_f16(128, 64, true, true);
+
+// Byte offset of 16-byte chunk kc (values 8 kc .. 8 kc + 7 along the row) of
+// row `row` of an operand of `rows` rows: 64-value blocks of rows x 128 B,
+// 8-row atoms of 1024 B, chunk index XOR (row mod 8).
+__device__ __forceinline__ uint32_t sw_chunk(int rows, int row, int kc) {
+  const int blk = kc >> 3, c = kc & 7;
+  return static_cast<uint32_t>(blk * rows * 128 + (row >> 3) * 1024 + (row & 7) * 128 +
+                               ((c ^ (row & 7)) << 4));
+}
+
+// The same for row `row` (B's token rows 0-127, S0's rows 128-191) of the
+// shared B / S0 operand.
+__device__ __forceinline__ uint32_t bs_chunk(int row, int kc) {
+  return static_cast<uint32_t>((kc >> 3) * kBlkBS + (row >> 3) * 1024 + (row & 7) * 128 +
+                               (((kc & 7) ^ (row & 7)) << 4));
+}
+
+// An operand in shared memory: hi part at `base`, lo part `lo` bytes on.
+//   K-major:  rows along M (or N), 128 values of K; `blk` = bytes of one
+//             64-value K block (rows x 128).
+//   MN-major: rows along K (16 per MMA step), 64 values of M (or N) per 128-B
+//             row; `blk` = bytes between 64-wide M (or N) blocks.
+struct Operand {
+  uint32_t base, lo, blk;
+  bool mn;
+};
+
+__device__ __forceinline__ uint64_t op_desc(const Operand& o, bool lo_part, int kk) {
+  const uint32_t a = o.base + (lo_part ? o.lo : 0u);
+  return o.mn ? make_sdesc_sw128(a + kk * 2048, o.blk, 1024)
+              : make_sdesc_sw128(a + (kk >> 2) * o.blk + (kk & 3) * 32, 16, 1024);
+}
+
+// D (+)= A B over K = 128 with split operands: hi hi, hi lo, lo hi.
+// (mma_bf16_ss issues kind::f16; the fp16 type comes from the descriptor.)
+__device__ __forceinline__ void mma_split(uint32_t d_tmem, const Operand& a, const Operand& b,
+                                          uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int pass = 0; pass < 3; ++pass) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      mma_bf16_ss(d_tmem, op_desc(a, pass == 2, kk), op_desc(b, pass == 1, kk), idesc,
+                  (accumulate || pass > 0 || kk > 0) ? 1u : 0u);
+  }
+}
+
+// hi + lo split of a pair of fp32 values into fp16 pairs.  hi is x rounded
+// to 11 significant bits by Veltkamp's splitting (c = (2^13 + 1) x,
+// hi = c - (c - x), in fp32 arithmetic, each step rounded on its own: the
+// _rn intrinsics are never fused into an FMA), so it converts to fp16
+// exactly wherever fp16 is normal; lo = x - hi is exact in fp32 and rounded
+// once to fp16.  One packed conversion per pair and part.
+__device__ __forceinline__ float veltkamp_hi(float x) {
+  const float c = __fmul_rn(x, 8193.f);
+  return __fsub_rn(c, __fsub_rn(c, x));
+}
+__device__ __forceinline__ void split2(float a, float b, uint32_t* hi, uint32_t* lo) {
+  const float ha = veltkamp_hi(a), hb = veltkamp_hi(b);
+  const __half2 h = __floats2half2_rn(ha, hb);
+  const __half2 l = __floats2half2_rn(__fsub_rn(a, ha), __fsub_rn(b, hb));
+  *hi = *reinterpret_cast<const uint32_t*>(&h);
+  *lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// Splits 8 fp32 values into fp16 hi and lo parts, 16 bytes each.
+__device__ __forceinline__ void split8(const float (&v)[8], uint4* hi, uint4* lo) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) split2(v[2 * i], v[2 * i + 1], &h[i], &l[i]);
+  *hi = make_uint4(h[0], h[1], h[2], h[3]);
+  *lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+__device__ __forceinline__ void unpack8(const float4& a, const float4& b, float (&v)[8]) {
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+// (ah, al) += (bh, bl) in float-float arithmetic: the sum's rounding error
+// is carried in the lo word (two-sum, then a renormalising fast two-sum).
+__device__ __forceinline__ void ff_add(float& ah, float& al, float bh, float bl) {
+  const float s = ah + bh;
+  const float bb = s - ah;
+  float e = (ah - (s - bb)) + (bh - bb);
+  e += al + bl;
+  ah = s + e;
+  al = e - (ah - s);
+}
+
+// A block's fp32 rows are staged by TMA in the space of the operands they
+// become: C's 128 rows (512 B each) where C goes; B's in the four 16 KB
+// pieces of the B / S0 operand that B's rows take (32 rows each: K block
+// k & 1 of part k >> 1), S0's rows staying untouched; x's 128 rows (256 B)
+// where x goes.
+constexpr uint32_t kStageBytes = 2 * kQ * kN * 4 + kQ * kP * 4;
+// chunks of 8 values per thread: C and B (16 per token), x (8 per token)
+constexpr int kTasksCB = kQ * 16 / kThreads;
+constexpr int kTasksX = kQ * 8 / kThreads;
+__device__ __forceinline__ uint32_t b_piece(int k) {
+  return static_cast<uint32_t>(kOffBS + (k >> 1) * kPartBS + (k & 1) * kBlkBS);
+}
+
+// Loads 8 staged fp32 values (the 16-byte units 2 c and 2 c + 1 of a row),
+// the unit with the same parity as c >> 2 first: the eight lanes that load
+// c = 8 i .. 8 i + 7 of one row then touch eight different bank groups.
+__device__ __forceinline__ void load_staged8(const uint8_t* row, int c, float (&v)[8]) {
+  const int s = (c >> 2) & 1;
+  const float4 f0 = *reinterpret_cast<const float4*>(row + (2 * c + s) * 16);
+  const float4 f1 = *reinterpret_cast<const float4*>(row + (2 * c + 1 - s) * 16);
+  const float4 lo = s ? f1 : f0, hi = s ? f0 : f1;
+  unpack8(lo, hi, v);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    ssd_chunk_scan_tc_kernel(const SsdParams p, const __grid_constant__ CUtensorMap map_c,
+                             const __grid_constant__ CUtensorMap map_b,
+                             const __grid_constant__ CUtensorMap map_x) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  const uint32_t sbase = smem_u32(smem);
+  Vec& vec = *reinterpret_cast<Vec*>(smem + kOffVec);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + kOffCtl);
+  const int h = blockIdx.x, r = blockIdx.y;
+  const int g = h / (p.H / p.G);
+  const int L = p.T / p.R;
+  const int c0 = r * L;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // every index below is the CTA's head, group and rank plus offsets inside
+  // the tile shapes and the chunk's rows: checking those checks them all
+  if (!index_ok(h, p.H, p.status, kSiteSsd) || !index_ok(g, p.G, p.status, kSiteSsd) ||
+      !index_ok(r, p.R, p.status, kSiteSsd) ||
+      !index_ok((long long)c0 + L - 1, p.T, p.status, kSiteSsd))
+    return;
+  const float A2 = p.A[h] * kLog2e;
+  const float Dh = p.D ? p.D[h] : 0.f;
+
+  const Operand opC{sbase + kOffC, kPartCB, kQ * 128, false};  // also M
+  const Operand opBS{sbase + kOffBS, kPartBS, kBlkBS, false};
+  const Operand opVB{sbase + kOffBS, kPartBS, kBlkBS, true};  // v o B, rows = tokens
+  const Operand opX{sbase + kOffX, kPartX, kPartX, true};
+
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl->mma_bar, 1);
+    mbar_init(&ctl->done_bar, 1);
+    mbar_init(&ctl->tma_bar, 1);
+    fence_barrier_init();
+    tma_prefetch_map(&map_c);
+    tma_prefetch_map(&map_b);
+    tma_prefetch_map(&map_x);
+  }
+  if (warp == 0) {
+    tmem_alloc(&ctl->tmem_base, 512);
+    tmem_relinquish();
+  }
+  // TMEM lanes of this warp (a warp reaches lanes 32 (warp mod 4) ...) and the
+  // quarter of each accumulator's columns it takes
+  const int row = (warp & 3) * 32 + lane;
+  const int cg = warp >> 2;
+  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+
+  // the state before the first block is zero (S0's rows of both K blocks,
+  // hi and lo); then the first block's operands
+  for (int i = threadIdx.x; i < 4 * kP * 128 / 16; i += kThreads) {
+    const int part = i / (kP * 128 / 16), k = i % (kP * 128 / 16);
+    reinterpret_cast<uint4*>(smem + kOffBS + (part >> 1) * kPartBS + (part & 1) * kBlkBS +
+                             kQ * 128)[k] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  // warps 4-7 scan the decays, one token each (warp 0 issues the MMAs):
+  // this thread's token of the next block to scan, its dt and position (a
+  // sample starts at position 0)
+  const bool scanner = warp >= 4 && warp < 8;
+  const int tok = static_cast<int>(threadIdx.x) - 128;
+  float tok_dt = 0.f;
+  int tok_pos = 1;
+  auto load_token = [&](int tb, int nb) {
+    const bool in = scanner && tok < nb;
+    tok_dt = in ? p.dt[(size_t)(tb + tok) * p.H + h] : 0.f;
+    tok_pos = (in && p.pos != nullptr) ? p.pos[tb + tok] : 1;
+  };
+  // thread 0 stages a block's rows (tokens tb ...; rows past the tensor's
+  // end read as zeros, rows past the chunk's end are zeroed in the split)
+  auto stage_rows = [&](int tb) {
+    mbar_arrive_expect_tx(&ctl->tma_bar, kStageBytes);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      tma_load_3d(smem + kOffC + k * 32 * kN * 4, &map_c, &ctl->tma_bar, 0, g, tb + 32 * k);
+      tma_load_3d(smem + b_piece(k), &map_b, &ctl->tma_bar, 0, g, tb + 32 * k);
+    }
+    tma_load_3d(smem + kOffX, &map_x, &ctl->tma_bar, 0, h, tb);
+  };
+  load_token(c0, min(kQ, L));
+  __syncthreads();  // barriers initialised; S0's rows zeroed
+  if (threadIdx.x == 0) stage_rows(c0);
+
+  float log2carry = 0.f;  // sum of dt A log2(e) over the chunk
+  bool reset = false;     // a sample starts inside the chunk
+  int uses = 0;           // phases of mma_bar so far
+  bool ok = true;
+  uint32_t tmem = 0;
+  const int nblocks = (L + kQ - 1) / kQ;
+  for (int b = 0; b < nblocks && ok; ++b) {
+    const int t0 = c0 + b * kQ;
+    const int n = min(kQ, c0 + L - t0);
+    // ---- the block's staged rows, split in place into C, B and x: every
+    // thread reads all its values before any thread overwrites them
+    ok = __syncthreads_and(mbar_wait(&ctl->tma_bar, b & 1, p.status, nullptr)) != 0;
+    if (!ok) break;
+    // B's values stay in registers until they are scaled by v
+    float bv[kTasksCB][8];
+    {
+      float cv[kTasksCB][8], xv[kTasksX][8];
+#pragma unroll
+      for (int u = 0; u < kTasksCB; ++u) {
+        const int q = threadIdx.x + u * kThreads;
+        const int t = q >> 4, kc = q & 15;
+        load_staged8(smem + kOffC + t * kN * 4, kc, cv[u]);
+        load_staged8(smem + b_piece(t >> 5) + (t & 31) * kN * 4, kc, bv[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < kTasksX; ++u) {
+        const int q = threadIdx.x + u * kThreads;
+        load_staged8(smem + kOffX + (q >> 3) * kP * 4, q & 7, xv[u]);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int u = 0; u < kTasksCB; ++u) {
+        const int q = threadIdx.x + u * kThreads;
+        const int t = q >> 4, kc = q & 15;
+        if (t >= n) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) cv[u][i] = bv[u][i] = 0.f;
+        }
+        const uint32_t at = sw_chunk(kQ, t, kc), ab = bs_chunk(t, kc);
+        split8(cv[u], reinterpret_cast<uint4*>(smem + kOffC + at),
+               reinterpret_cast<uint4*>(smem + kOffC + kPartCB + at));
+        split8(bv[u], reinterpret_cast<uint4*>(smem + kOffBS + ab),
+               reinterpret_cast<uint4*>(smem + kOffBS + kPartBS + ab));
+      }
+#pragma unroll
+      for (int u = 0; u < kTasksX; ++u) {
+        const int q = threadIdx.x + u * kThreads;
+        const int t = q >> 3;
+        if (t >= n) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) xv[u][i] = 0.f;
+        }
+        const uint32_t at = sw_chunk(kQ, t, q & 7);
+        split8(xv[u], reinterpret_cast<uint4*>(smem + kOffX + at),
+               reinterpret_cast<uint4*>(smem + kOffX + kPartX + at));
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    tmem = ctl->tmem_base;
+    // ---- [G | Yoff] = C [B | S0]^T
+    if (threadIdx.x == 0) {
+      mma_split(tmem + kColG, opC, opBS, kIdescGY, false);
+      mma_commit(&ctl->mma_bar);
+    }
+    // ---- while it runs: per-token decays and sample starts, inclusive
+    // scans over the block
+    float ph = 0.f, pl = 0.f;  // this token's running sum within its warp
+    int cw = 0;
+    if (scanner) {
+      ph = tok_dt * A2;
+      cw = tok_pos == 0 ? 1 : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float uh = __shfl_up_sync(0xffffffffu, ph, o);
+        const float ul = __shfl_up_sync(0xffffffffu, pl, o);
+        const int cu = __shfl_up_sync(0xffffffffu, cw, o);
+        if (lane >= o) {
+          ff_add(ph, pl, uh, ul);
+          cw += cu;
+        }
+      }
+      if (lane == 31) {
+        vec.wsh[warp - 4] = ph;
+        vec.wsl[warp - 4] = pl;
+        vec.wcnt[warp - 4] = cw;
+      }
+    }
+    __syncthreads();
+    if (scanner) {
+      const int t = tok;
+      float eh = 0.f, el = 0.f;  // P at the block's end
+      int rc = cw, rcend = 0;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        if (w < warp - 4) {
+          ff_add(ph, pl, vec.wsh[w], vec.wsl[w]);
+          rc += vec.wcnt[w];
+        }
+        ff_add(eh, el, vec.wsh[w], vec.wsl[w]);
+        rcend += vec.wcnt[w];
+      }
+      vec.Ph[t] = ph;
+      vec.Pl[t] = pl;
+      vec.rc[t] = rc;
+      vec.dt[t] = tok_dt;
+      vec.v[t] = rc == rcend ? fast_exp2((eh - ph) + (el - pl)) * tok_dt : 0.f;
+      vec.w[t] = rc == 0 ? fast_exp2(ph + pl) : 0.f;
+      if (t == 0) {
+        vec.Pend = eh + el;
+        vec.rcend = rcend;
+      }
+    }
+    ok = __syncthreads_and(mbar_wait(&ctl->mma_bar, uses & 1, p.status, nullptr)) != 0;
+    ++uses;
+    if (!ok) break;
+    tc_fence_after_sync();
+    const float Pend = vec.Pend;
+    const int rcend = vec.rcend;
+    // ---- M = G o mask o dt (rows = tokens t, K = tokens j), into C's place;
+    // a warp whose 32 columns all lie above its 32 rows writes zeros
+    if (cg > (warp & 3)) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t at = sw_chunk(kQ, row, cg * 4 + c);
+        *reinterpret_cast<uint4*>(smem + kOffC + at) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(smem + kOffC + kPartCB + at) = make_uint4(0u, 0u, 0u, 0u);
+      }
+    } else {
+      uint32_t gv[32];
+      tmem_load_32(tmem + lane_off + kColG + cg * 32, gv);
+      const float pht = vec.Ph[row], plt = vec.Pl[row];
+      const int rct = vec.rc[row];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int j0 = cg * 32 + c * 8;
+        float m[8];
+#pragma unroll
+        for (int i4 = 0; i4 < 8; i4 += 4) {
+          const float4 phj = *reinterpret_cast<const float4*>(&vec.Ph[j0 + i4]);
+          const float4 plj = *reinterpret_cast<const float4*>(&vec.Pl[j0 + i4]);
+          const float4 dj = *reinterpret_cast<const float4*>(&vec.dt[j0 + i4]);
+          const int4 rj = *reinterpret_cast<const int4*>(&vec.rc[j0 + i4]);
+          const float phv[4] = {phj.x, phj.y, phj.z, phj.w};
+          const float plv[4] = {plj.x, plj.y, plj.z, plj.w};
+          const float djv[4] = {dj.x, dj.y, dj.z, dj.w};
+          const int rjv[4] = {rj.x, rj.y, rj.z, rj.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int j = j0 + i4 + i;
+            const bool vis = j <= row && rjv[i] == rct;
+            const float e = fast_exp2(vis ? (pht - phv[i]) + (plt - plv[i]) : -INFINITY);
+            m[i4 + i] = __uint_as_float(gv[c * 8 + i4 + i]) * e * djv[i];
+          }
+        }
+        const uint32_t at = sw_chunk(kQ, row, cg * 4 + c);
+        split8(m, reinterpret_cast<uint4*>(smem + kOffC + at),
+               reinterpret_cast<uint4*>(smem + kOffC + kPartCB + at));
+      }
+    }
+    // ---- B_j scaled by v_j, over B's split in place: (v o B) read MN-major
+    // is (v o B)^T
+#pragma unroll
+    for (int u = 0; u < kTasksCB; ++u) {
+      const int q = threadIdx.x + u * kThreads;
+      const int j = q >> 4;
+      const uint32_t at = bs_chunk(j, q & 15);
+      const float vj = vec.v[j];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) bv[u][i] *= vj;
+      split8(bv[u], reinterpret_cast<uint4*>(smem + kOffBS + at),
+             reinterpret_cast<uint4*>(smem + kOffBS + kPartBS + at));
+    }
+    // ---- the state before the block decays through it (or dies at a sample start)
+    if (b > 0) {
+      const float keep = rcend == 0 ? fast_exp2(Pend) : 0.f;
+      uint32_t sv[16];
+      tmem_load_16(tmem + lane_off + kColS + cg * 16, sv);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sv[i] = __float_as_uint(__uint_as_float(sv[i]) * keep);
+      tmem_store_16(tmem + lane_off + kColS + cg * 16, sv);
+      tmem_store_wait();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before_sync();
+    __syncthreads();
+    // ---- Ydia = M X, S^T += (v o B)^T X; meanwhile the scanning warps load
+    // the next block's tokens
+    const bool more = b + 1 < nblocks;
+    const int tn = t0 + kQ;
+    if (more) load_token(tn, min(kQ, c0 + L - tn));
+    if (threadIdx.x == 0) {
+      tc_fence_after_sync();
+      mma_split(tmem + kColYdia, opC, opX, kIdescYdia, false);
+      mma_split(tmem + kColS, opVB, opX, kIdescS, b > 0);
+      mma_commit(&ctl->mma_bar);
+    }
+    ok = __syncthreads_and(mbar_wait(&ctl->mma_bar, uses & 1, p.status, nullptr)) != 0;
+    ++uses;
+    if (!ok) break;
+    tc_fence_after_sync();
+    // C, B and x's space is free again: the next block's rows are staged
+    // there while this block's state and y are written out
+    if (more && threadIdx.x == 0) stage_rows(tn);
+    float4 xr[4];
+    const size_t orow = ((size_t)(t0 + row) * p.H + h) * kP + cg * 16;
+    if (row < n) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) xr[i] = *reinterpret_cast<const float4*>(p.x + orow + 4 * i);
+    }
+    // ---- the state after the block: S0 (rows 128 + p of the B / S0
+    // operand, K = state) for the next block's Yoff, and the chunk's final state
+    {
+      uint32_t sv[16];
+      tmem_load_16(tmem + lane_off + kColS + cg * 16, sv);
+      const int nn = row;  // this lane's state index
+      const uint32_t in_chunk = (nn & 7) * 2;
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) {
+        uint32_t hi, lo;
+        split2(__uint_as_float(sv[i]), __uint_as_float(sv[i + 1]), &hi, &lo);
+        const uint32_t a0 = bs_chunk(kQ + cg * 16 + i, nn >> 3) + in_chunk;
+        const uint32_t a1 = bs_chunk(kQ + cg * 16 + i + 1, nn >> 3) + in_chunk;
+        *reinterpret_cast<uint16_t*>(smem + kOffBS + a0) = static_cast<uint16_t>(hi);
+        *reinterpret_cast<uint16_t*>(smem + kOffBS + a1) = static_cast<uint16_t>(hi >> 16);
+        *reinterpret_cast<uint16_t*>(smem + kOffBS + kPartBS + a0) = static_cast<uint16_t>(lo);
+        *reinterpret_cast<uint16_t*>(smem + kOffBS + kPartBS + a1) = static_cast<uint16_t>(lo >> 16);
+      }
+      if (!more) {
+        float* Sout = p.chunk_state + ((size_t)r * p.H + h) * kP * kN;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) Sout[(size_t)(cg * 16 + i) * kN + nn] = __uint_as_float(sv[i]);
+      }
+    }
+    // ---- y of the block: [rc_t == 0] 2^P_t Yoff + Ydia + D x
+    {
+      uint32_t yo[16], yd[16];
+      tmem_load_16(tmem + lane_off + kColYoff + cg * 16, yo);
+      tmem_load_16(tmem + lane_off + kColYdia + cg * 16, yd);
+      if (row < n) {
+        const float w = vec.w[row];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          float4 yv;
+          yv.x = fmaf(w, __uint_as_float(yo[4 * i]), __uint_as_float(yd[4 * i])) + Dh * xr[i].x;
+          yv.y = fmaf(w, __uint_as_float(yo[4 * i + 1]), __uint_as_float(yd[4 * i + 1])) +
+                 Dh * xr[i].y;
+          yv.z = fmaf(w, __uint_as_float(yo[4 * i + 2]), __uint_as_float(yd[4 * i + 2])) +
+                 Dh * xr[i].z;
+          yv.w = fmaf(w, __uint_as_float(yo[4 * i + 3]), __uint_as_float(yd[4 * i + 3])) +
+                 Dh * xr[i].w;
+          *reinterpret_cast<float4*>(p.y + orow + 4 * i) = yv;
+        }
+      }
+    }
+    log2carry += Pend;
+    reset = reset || rcend > 0;
+  }
+  if (ok && threadIdx.x == 0) p.carry[(size_t)r * p.H + h] = reset ? 0.f : exp2f(log2carry);
+  // every MMA has completed before TMEM is released
+  tc_fence_before_sync();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mma_commit(&ctl->done_bar);
+    mbar_wait(&ctl->done_bar, 0, p.status, nullptr);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc(ctl->tmem_base, 512);
+  }
+}
+
+bool g_configured[64] = {};
+
+}  // namespace
+
+cudaError_t launch_ssd_chunk_scan_tc(const SsdParams& p, const SsdMaps& maps,
+                                     cudaStream_t stream) {
+  cudaError_t e = ensure_smem_limit(ssd_chunk_scan_tc_kernel, kSmem, g_configured);
+  if (e != cudaSuccess) return e;
+  TraceScope trace_scope(stream, "ssd_chunk_scan_tc_kernel");
+  ssd_chunk_scan_tc_kernel<<<dim3(p.H, p.R), kThreads, kSmem, stream>>>(p, maps.c, maps.b,
+                                                                         maps.x);
+  return cudaGetLastError();
+}
+
+}  // namespace ra

@@ -13,12 +13,13 @@
 //   1. ssd_chunk_scan_kernel  (head, rank): the rank's chunk from S = 0; writes
 //      y, the chunk's final state and its carry factor -- exp(A sum dt) over
 //      the chunk, or 0 if a sample starts inside it (the incoming state dies
-//      there).
+//      there).  For state size 128 the tensor-core form of this scan
+//      (ssd_chunk_tc.cu) runs instead; the kernel here serves state size 64.
 //   2. ssd_state_pass_kernel  (head): the ring of states, rank by rank:
 //      H_0 = 0, H_r = carry_{r-1} H_{r-1} + S_{r-1} (what rank r would receive).
 //   3. ssd_correction_kernel  (head, rank >= 1): y_t += exp(A sum_{chunk start
 //      <= u <= t} dt_u) H_r C_t for the chunk's tokens before its first sample
-//      start.
+//      start, up to the block where that factor has underflowed to zero.
 // Threads: 256 per CTA.  A thread owns two rows of the state (2 rp, 2 rp + 1)
 // and N / 8 of their columns: thread cs of a row pair holds columns
 // 32 j + 4 cs + e (e < 4), so each B or C value it reads from shared memory
@@ -69,18 +70,6 @@ struct Stage {
   int pos[kTok];
   float y[kTok][kPX];
 };
-
-// 16-byte global -> shared copy that does not pass through registers
-// (cp.async); with valid == false it writes zeros and reads nothing.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
-               "r"(valid ? 16 : 0)
-               : "memory");
-}
-// Waits for this thread's cp.async copies (a barrier then publishes them).
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-}
 
 // Column of the state a thread's i-th entry (of each of its rows) holds.
 __device__ __forceinline__ int ssd_col(int cs, int i) {
@@ -326,7 +315,15 @@ struct CorrStage {
   float y[kTok][kP + 16];  // rows 16 banks apart: two tokens' rows per warp store
   float decay[kTok];  // exp(A sum dt) from the chunk start through the token
   int m;              // tokens of the block before the first sample start
+  int dead;           // every later token's decay is exactly zero
 };
+
+// A sum dt below which expf is exactly 0 in fp32 (denormals included: it
+// underflows near -103.97).  The running sum only falls: its terms are <= 0,
+// a rounded sum of terms <= 0 is <= 0, and rounding is monotone, so once the
+// sum at a block's end is below this, every later token adds an exact zero
+// to y and the correction can stop there with the same result.
+constexpr float kDeadExponent = -110.f;
 
 // Y[t, :] += exp(A sum_{c0 <= u <= t} dt_u) H C_t for the block's tokens t
 // before the first sample start: a 32 x 64 x N product per block, on CUDA
@@ -382,11 +379,15 @@ __global__ void __launch_bounds__(kThreads) ssd_correction_kernel(const SsdParam
       lam = __shfl_sync(0xffffffffu, lk, 31);
       const unsigned starts =
           __ballot_sync(0xffffffffu, in && p.pos != nullptr && p.pos[t0 + lane] == 0);
-      if (lane == 0) st.m = starts ? __ffs(starts) - 1 : n;
+      if (lane == 0) {
+        st.m = starts ? __ffs(starts) - 1 : n;
+        st.dead = lam < kDeadExponent;
+      }
     }
     cp_async_wait_all();
     __syncthreads();
     const int m = st.m;
+    const bool dead = st.dead != 0;
     if (m > 0) {
       uint64_t acc[2][4];
 #pragma unroll
@@ -441,23 +442,28 @@ __global__ void __launch_bounds__(kThreads) ssd_correction_kernel(const SsdParam
         }
       }
     }
-    if (m < n) break;  // a sample starts here: the received state is gone
+    // a sample starts here, or the received state has decayed to exact zeros
+    if (m < n || dead) break;
   }
 }
 
 template <int N>
-cudaError_t launch_n(const SsdParams& p, cudaStream_t stream) {
+cudaError_t launch_n(const SsdParams& p, const SsdMaps* maps, cudaStream_t stream) {
   const size_t smem = sizeof(Stage<N>), smem_corr = sizeof(CorrStage<N>);
   static bool scan_configured[64] = {}, corr_configured[64] = {};
   cudaError_t e0 = ensure_smem_limit(ssd_chunk_scan_kernel<N>, (int)smem, scan_configured);
   if (e0 == cudaSuccess)
     e0 = ensure_smem_limit(ssd_correction_kernel<N>, (int)smem_corr, corr_configured);
   if (e0 != cudaSuccess) return e0;
-  {
+  cudaError_t e;
+  if (N == 128) {
+    if (maps == nullptr) return cudaErrorInvalidValue;
+    e = launch_ssd_chunk_scan_tc(p, *maps, stream);
+  } else {
     TraceScope trace_scope(stream, "ssd_chunk_scan_kernel");
     ssd_chunk_scan_kernel<N><<<dim3(p.H, p.R), kThreads, smem, stream>>>(p);
+    e = cudaGetLastError();
   }
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   {
     TraceScope trace_scope(stream, "ssd_state_pass_kernel");
@@ -474,9 +480,9 @@ cudaError_t launch_n(const SsdParams& p, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_ssd_cp(const SsdParams& p, cudaStream_t stream) {
+cudaError_t launch_ssd_cp(const SsdParams& p, const SsdMaps* maps, cudaStream_t stream) {
   if (p.T == 0) return cudaSuccess;
-  return p.N == 64 ? launch_n<64>(p, stream) : launch_n<128>(p, stream);
+  return p.N == 64 ? launch_n<64>(p, maps, stream) : launch_n<128>(p, maps, stream);
 }
 
 }  // namespace ra

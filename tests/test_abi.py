@@ -82,6 +82,25 @@ def test_argument_errors_without_gpu(lib):
     assert lib.attn_lse_merge(None, None, None, None, 0, 2, 64, 0, None) == 0
 
 
+def test_ssd_argument_errors_without_gpu(lib):
+    f = lib.ssd_cp_fwd
+    sd = ra.ssd_dims(1024, 4, 64, 128, 2)
+    ws = lib.ssd_cp_workspace_size(sd, 4)
+    # (fake) device pointers: every check below comes before any device work
+    ok = [256, 512, 768, 1024, 1280, None, None]
+    assert f(*ok, ra.ssd_dims(1000, 4, 64, 128, 2), 3, 1536, None, None, ws, None) == -2
+    assert f(*ok, ra.ssd_dims(1024, 4, 64, 96, 2), 4, 1536, None, None, ws, None) == -3
+    assert f(*ok, ra.ssd_dims(1024, 3, 64, 128, 2), 4, 1536, None, None, ws, None) == -1
+    assert f(*ok, sd, 4, 1536, None, None, 0, None) == -6          # no workspace
+    # x, B, C and y are moved in 16-byte pieces
+    for i in (0, 3, 4):
+        bad = list(ok)
+        bad[i] += 4
+        assert f(*bad, sd, 4, 1536, None, None, ws, None) == -1
+    assert f(*ok, sd, 4, 1540, None, None, ws, None) == -1
+    assert f(*ok, ra.ssd_dims(0, 4, 64, 128, 2), 4, 1536, None, None, ws, None) == 0
+
+
 def test_workspace_sizes(lib):
     d = dims(T=1024, hq=4, hkv=2)
     assert lib.ringattn_fwd_stepwise_workspace_size(d) >= 2 * (1024 * 4 * 128 * 4 + 4 * 1024 * 4)
