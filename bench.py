@@ -104,7 +104,8 @@ def load_peaks():
 KERNEL_SOURCES = {"fwd_tc_bf16_kernel": "fwd_tc_bf16.cu", "bwd_dkdv_kernel": "bwd_tc_bf16.cu",
                   "bwd_dq_kernel": "bwd_tc_bf16.cu", "ssd_chunk_scan_kernel": "ssd_cp.cu",
                   "ssd_chunk_scan_tc_kernel": "ssd_chunk_tc.cu",
-                  "ssd_correction_kernel": "ssd_cp.cu"}
+                  "ssd_correction_kernel": "ssd_cp.cu",
+                  "ssd_correction_tc_kernel": "ssd_correction_tc.cu"}
 
 
 def kernel_traffic(kernel: str, workload: str):

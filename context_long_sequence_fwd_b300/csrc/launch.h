@@ -78,4 +78,10 @@ cudaError_t launch_ssd_cp(const SsdParams& p, const SsdMaps* maps, cudaStream_t 
 cudaError_t launch_ssd_chunk_scan_tc(const SsdParams& p, const SsdMaps& maps,
                                      cudaStream_t stream);
 
+// The additive correction of launch_ssd_cp on the tensor cores (state size
+// 128): y_t += exp(A sum dt) H_r C_t on ranks r >= 1 up to their chunk's first
+// sample start.
+cudaError_t launch_ssd_correction_tc(const SsdParams& p, const SsdMaps& maps,
+                                     cudaStream_t stream);
+
 }  // namespace ra

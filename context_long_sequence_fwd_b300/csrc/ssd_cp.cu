@@ -19,7 +19,8 @@
 //      H_0 = 0, H_r = carry_{r-1} H_{r-1} + S_{r-1} (what rank r would receive).
 //   3. ssd_correction_kernel  (head, rank >= 1): y_t += exp(A sum_{chunk start
 //      <= u <= t} dt_u) H_r C_t for the chunk's tokens before its first sample
-//      start, up to the block where that factor has underflowed to zero.
+//      start, up to the block where that factor has underflowed to zero.  For
+//      state size 128 the tensor-core form (ssd_correction_tc.cu) runs instead.
 // Threads: 256 per CTA.  A thread owns two rows of the state (2 rp, 2 rp + 1)
 // and N / 8 of their columns: thread cs of a row pair holds columns
 // 32 j + 4 cs + e (e < 4), so each B or C value it reads from shared memory
@@ -471,6 +472,7 @@ cudaError_t launch_n(const SsdParams& p, const SsdMaps* maps, cudaStream_t strea
   }
   e = cudaGetLastError();
   if (e != cudaSuccess || p.R < 2) return e;
+  if (N == 128) return launch_ssd_correction_tc(p, *maps, stream);
   {
     TraceScope trace_scope(stream, "ssd_correction_kernel");
     ssd_correction_kernel<N><<<dim3(p.H, p.R - 1), kThreads, smem_corr, stream>>>(p);

@@ -270,9 +270,10 @@ ra_status attn_lse_merge(void* o_a, float* lse_a, const void* o_b, const float* 
  * RA_ERR_INVALID_ARG); asynchronous on `stream`; needs a device workspace of
  * ssd_cp_workspace_size(dims, num_shards) bytes (256-byte aligned; each
  * rank's final state, the states passed along the ring, the carry factors).
- * State size 128 scans on the tensor cores with fp16 operands split into
- * hi + lo parts (three products per term, fp32 accumulation); state size 64
- * on fp32 CUDA cores.  Both are accurate to about 1e-6 of the output scale.
+ * State size 128 scans and corrects on the tensor cores with fp16 operands
+ * split into hi + lo parts (three products per term, fp32 accumulation);
+ * state size 64 on fp32 CUDA cores.  Both are accurate to about 1e-6 of the
+ * output scale.
  */
 typedef struct {
   int total_tokens; /* T >= 0 */
