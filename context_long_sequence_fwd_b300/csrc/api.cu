@@ -126,17 +126,21 @@ bool encode_thd(CUtensorMap* map, const void* ptr, int T, int H, int D) {
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// fp32 [T, M, inner] tensor viewed as 3-D (inner, M, T); box inner x 1 x rows,
-// no swizzle (the rows land in shared memory as they are in memory).
-bool encode_f32_rows(CUtensorMap* map, const void* ptr, int T, int M, int inner, int rows) {
+// fp32 [T, M, inner] tensor viewed as 3-D (inner, M, T); box box_inner x 1 x
+// rows.  Without swizzle the rows land in shared memory as they are in
+// memory; with it (box_inner = 32: 128-byte rows) the 16-byte units of row t
+// of the box are permuted by XOR with t mod 8.
+bool encode_f32_rows(CUtensorMap* map, const void* ptr, int T, int M, int inner, int box_inner,
+                     int rows, bool swizzle) {
   auto enc = encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)M, (cuuint64_t)T};
   cuuint64_t strides[2] = {(cuuint64_t)inner * 4, (cuuint64_t)M * inner * 4};
-  cuuint32_t box[3] = {(cuuint32_t)inner, 1, (cuuint32_t)rows};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, 1, (cuuint32_t)rows};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box,
-             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -972,9 +976,10 @@ ra_status ssd_cp_fwd(const float* x, const float* dt, const float* A, const floa
   p.status = ds->status;
   SsdMaps maps;
   if (dims.state_dim == 128 &&
-      (!encode_f32_rows(&maps.c, C, dims.total_tokens, dims.groups, 128, 32) ||
-       !encode_f32_rows(&maps.b, B, dims.total_tokens, dims.groups, 128, 32) ||
-       !encode_f32_rows(&maps.x, x, dims.total_tokens, dims.heads, 64, 128)))
+      (!encode_f32_rows(&maps.c, C, dims.total_tokens, dims.groups, 128, 128, 32, false) ||
+       !encode_f32_rows(&maps.c_sw, C, dims.total_tokens, dims.groups, 128, 32, 128, true) ||
+       !encode_f32_rows(&maps.b, B, dims.total_tokens, dims.groups, 128, 128, 32, false) ||
+       !encode_f32_rows(&maps.x, x, dims.total_tokens, dims.heads, 64, 64, 128, false)))
     return RA_ERR_CUDA;
   return launch_ssd_cp(p, dims.state_dim == 128 ? &maps : nullptr,
                        static_cast<cudaStream_t>(stream)) == cudaSuccess

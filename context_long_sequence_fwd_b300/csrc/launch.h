@@ -67,9 +67,10 @@ cudaError_t launch_bwd_simt_fp32(const BwdParams& p, cudaStream_t stream);
 // `maps` (host memory) describes C, B and x for the tensor-core chunk scan
 // of state size 128 (see SsdMaps); it may be null for state size 64.
 struct SsdMaps {
-  CUtensorMap c;  // C [T, G, 128] fp32 as (state, group, token); box 128 x 1 x 32
-  CUtensorMap b;  // B, the same
-  CUtensorMap x;  // x [T, H, 64] fp32 as (head dim, head, token); box 64 x 1 x 128
+  CUtensorMap c;     // C [T, G, 128] fp32 as (state, group, token); box 128 x 1 x 32
+  CUtensorMap c_sw;  // C as above; box 32 x 1 x 128, 128-byte swizzle
+  CUtensorMap b;     // B, as c
+  CUtensorMap x;     // x [T, H, 64] fp32 as (head dim, head, token); box 64 x 1 x 128
 };
 cudaError_t launch_ssd_cp(const SsdParams& p, const SsdMaps* maps, cudaStream_t stream);
 

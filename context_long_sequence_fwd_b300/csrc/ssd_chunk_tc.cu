@@ -79,7 +79,7 @@ constexpr int kPartX = kQ * kP * 2;   // 128 token rows x 64 fp16
 constexpr int kRowsBS = kQ + kP;
 constexpr int kBlkBS = kRowsBS * 128;
 constexpr int kPartBS = 2 * kBlkBS;
-constexpr int kOffC = 0;                      // C; then M
+constexpr int kOffC = 0;  // C's fp32 rows, staged (C and M themselves live in TMEM)
 constexpr int kOffBS = kOffC + 2 * kPartCB;   // B (then v o B) and S0
 constexpr int kOffX = kOffBS + 2 * kPartBS;
 constexpr int kOffVec = kOffX + 2 * kPartX;
@@ -103,7 +103,8 @@ constexpr int kOffCtl = kOffVec + ((sizeof(Vec) + 127) / 128) * 128;
 struct Ctl {
   uint64_t mma_bar;
   uint64_t done_bar;
-  uint64_t tma_bar;
+  uint64_t tma_c_bar;   // C's rows of a block
+  uint64_t tma_bx_bar;  // B's and x's rows of a block
   uint32_t tmem_base;
   int pad;
 };
@@ -112,6 +113,9 @@ static_assert(sizeof(Ctl) <= 128, "control block");
 static_assert(kSmem <= 232448, "dynamic shared memory of one CTA");
 
 constexpr uint32_t kColG = 0, kColYoff = 128, kColYdia = 192, kColS = 256;
+// C's split parts (hi 320-383, lo 384-447: the A operand of [G | Yoff]), then
+// M's (the A operand of Ydia), two fp16 per column
+constexpr uint32_t kColA = 320, kColAlo = 384;
 
 constexpr uint32_t kIdescGY = make_idesc_f16(128, 192, false, false);
 constexpr uint32_t kIdescYdia = make_idesc_f16(128, 64, false, true);
@@ -124,12 +128,15 @@ __device__ __forceinline__ uint32_t bs_chunk(int row, int kc) {
                                (((kc & 7) ^ (row & 7)) << 4));
 }
 
-// A block's fp32 rows are staged by TMA in the space of the operands they
-// become: C's 128 rows (512 B each) where C goes; B's in the four 16 KB
+// A block's fp32 rows are staged by TMA.  C's go to their own 64 KB, as four
+// boxes of 32 state values x 128 tokens with the 128-byte swizzle (16-byte
+// unit u of row t at unit u ^ (t mod 8)), so that each thread reads the 32
+// values of its own token without bank conflicts.  B's go to the four 16 KB
 // pieces of the B / S0 operand that B's rows take (32 rows each: K block
 // k & 1 of part k >> 1), S0's rows staying untouched; x's 128 rows (256 B)
-// where x goes.
-constexpr uint32_t kStageBytes = 2 * kQ * kN * 4 + kQ * kP * 4;
+// to where x goes.  Those two are split in place.
+constexpr uint32_t kStageBytesC = kQ * kN * 4;
+constexpr uint32_t kStageBytesBX = kQ * kN * 4 + kQ * kP * 4;
 // chunks of 8 values per thread: C and B (16 per token), x (8 per token)
 constexpr int kTasksCB = kQ * 16 / kThreads;
 constexpr int kTasksX = kQ * 8 / kThreads;
@@ -138,7 +145,7 @@ __device__ __forceinline__ uint32_t b_piece(int k) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    ssd_chunk_scan_tc_kernel(const SsdParams p, const __grid_constant__ CUtensorMap map_c,
+    ssd_chunk_scan_tc_kernel(const SsdParams p, const __grid_constant__ CUtensorMap map_c_sw,
                              const __grid_constant__ CUtensorMap map_b,
                              const __grid_constant__ CUtensorMap map_x) {
   extern __shared__ uint8_t smem_raw[];
@@ -161,7 +168,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float A2 = p.A[h] * kLog2e;
   const float Dh = p.D ? p.D[h] : 0.f;
 
-  const Operand opC{sbase + kOffC, kPartCB, kQ * 128, false};  // also M
   const Operand opBS{sbase + kOffBS, kPartBS, kBlkBS, false};
   const Operand opVB{sbase + kOffBS, kPartBS, kBlkBS, true};  // v o B, rows = tokens
   const Operand opX{sbase + kOffX, kPartX, kPartX, true};
@@ -169,15 +175,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&ctl->mma_bar, 1);
     mbar_init(&ctl->done_bar, 1);
-    mbar_init(&ctl->tma_bar, 1);
+    mbar_init(&ctl->tma_c_bar, 1);
+    mbar_init(&ctl->tma_bx_bar, 1);
     fence_barrier_init();
-    tma_prefetch_map(&map_c);
+    tma_prefetch_map(&map_c_sw);
     tma_prefetch_map(&map_b);
     tma_prefetch_map(&map_x);
   }
   if (warp == 0) {
     tmem_alloc(&ctl->tmem_base, 512);
     tmem_relinquish();
+    tc_fence_before_sync();
   }
   // TMEM lanes of this warp (a warp reaches lanes 32 (warp mod 4) ...) and the
   // quarter of each accumulator's columns it takes
@@ -206,41 +214,73 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   // thread 0 stages a block's rows (tokens tb ...; rows past the tensor's
   // end read as zeros, rows past the chunk's end are zeroed in the split)
-  auto stage_rows = [&](int tb) {
-    mbar_arrive_expect_tx(&ctl->tma_bar, kStageBytes);
+  auto stage_c = [&](int tb) {
+    mbar_arrive_expect_tx(&ctl->tma_c_bar, kStageBytesC);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      tma_load_3d(smem + kOffC + k * 32 * kN * 4, &map_c, &ctl->tma_bar, 0, g, tb + 32 * k);
-      tma_load_3d(smem + b_piece(k), &map_b, &ctl->tma_bar, 0, g, tb + 32 * k);
-    }
-    tma_load_3d(smem + kOffX, &map_x, &ctl->tma_bar, 0, h, tb);
+    for (int k = 0; k < 4; ++k)
+      tma_load_3d(smem + kOffC + k * kQ * 128, &map_c_sw, &ctl->tma_c_bar, 32 * k, g, tb);
+  };
+  auto stage_bx = [&](int tb) {
+    mbar_arrive_expect_tx(&ctl->tma_bx_bar, kStageBytesBX);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      tma_load_3d(smem + b_piece(k), &map_b, &ctl->tma_bx_bar, 0, g, tb + 32 * k);
+    tma_load_3d(smem + kOffX, &map_x, &ctl->tma_bx_bar, 0, h, tb);
   };
   load_token(c0, min(kQ, L));
-  __syncthreads();  // barriers initialised; S0's rows zeroed
-  if (threadIdx.x == 0) stage_rows(c0);
+  __syncthreads();  // barriers initialised; S0's rows zeroed; TMEM allocated
+  tc_fence_after_sync();
+  const uint32_t tmem = ctl->tmem_base;
+  if (threadIdx.x == 0) {
+    stage_c(c0);
+    stage_bx(c0);
+  }
 
   float log2carry = 0.f;  // sum of dt A log2(e) over the chunk
   bool reset = false;     // a sample starts inside the chunk
   int uses = 0;           // phases of mma_bar so far
   bool ok = true;
-  uint32_t tmem = 0;
   const int nblocks = (L + kQ - 1) / kQ;
   for (int b = 0; b < nblocks && ok; ++b) {
     const int t0 = c0 + b * kQ;
     const int n = min(kQ, c0 + L - t0);
-    // ---- the block's staged rows, split in place into C, B and x: every
-    // thread reads all its values before any thread overwrites them
-    ok = __syncthreads_and(mbar_wait(&ctl->tma_bar, b & 1, p.status, nullptr)) != 0;
+    // ---- the block's staged rows, split: C into TMEM (this thread's token,
+    // 32 state values), B and x in place (every thread reads all its values
+    // before any thread overwrites them)
+    ok = __syncthreads_and(mbar_wait(&ctl->tma_c_bar, b & 1, p.status, nullptr) &&
+                           mbar_wait(&ctl->tma_bx_bar, b & 1, p.status, nullptr)) != 0;
     if (!ok) break;
+    tc_fence_after_sync();
+    {
+      const uint8_t* crow = smem + kOffC + cg * kQ * 128 + row * 128;
+      float cv[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float4 f = *reinterpret_cast<const float4*>(crow + ((u ^ (row & 7)) << 4));
+        cv[4 * u] = f.x;
+        cv[4 * u + 1] = f.y;
+        cv[4 * u + 2] = f.z;
+        cv[4 * u + 3] = f.w;
+      }
+      uint32_t hi[16], lo[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (row < n)
+          split2(cv[2 * i], cv[2 * i + 1], &hi[i], &lo[i]);
+        else
+          hi[i] = lo[i] = 0u;
+      }
+      tmem_store_16(tmem + lane_off + kColA + cg * 16, hi);
+      tmem_store_16(tmem + lane_off + kColAlo + cg * 16, lo);
+    }
     // B's values stay in registers until they are scaled by v
     float bv[kTasksCB][8];
     {
-      float cv[kTasksCB][8], xv[kTasksX][8];
+      float xv[kTasksX][8];
 #pragma unroll
       for (int u = 0; u < kTasksCB; ++u) {
         const int q = threadIdx.x + u * kThreads;
         const int t = q >> 4, kc = q & 15;
-        load_staged8(smem + kOffC + t * kN * 4, kc, cv[u]);
         load_staged8(smem + b_piece(t >> 5) + (t & 31) * kN * 4, kc, bv[u]);
       }
 #pragma unroll
@@ -255,11 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = q >> 4, kc = q & 15;
         if (t >= n) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) cv[u][i] = bv[u][i] = 0.f;
+          for (int i = 0; i < 8; ++i) bv[u][i] = 0.f;
         }
-        const uint32_t at = sw_chunk(kQ, t, kc), ab = bs_chunk(t, kc);
-        split8(cv[u], reinterpret_cast<uint4*>(smem + kOffC + at),
-               reinterpret_cast<uint4*>(smem + kOffC + kPartCB + at));
+        const uint32_t ab = bs_chunk(t, kc);
         split8(bv[u], reinterpret_cast<uint4*>(smem + kOffBS + ab),
                reinterpret_cast<uint4*>(smem + kOffBS + kPartBS + ab));
       }
@@ -276,15 +314,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                reinterpret_cast<uint4*>(smem + kOffX + kPartX + at));
       }
     }
+    tmem_store_wait();
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    tmem = ctl->tmem_base;
-    // ---- [G | Yoff] = C [B | S0]^T
+    const bool more = b + 1 < nblocks;
+    const int tn = t0 + kQ;
+    // ---- [G | Yoff] = C [B | S0]^T; C's staging is free again, so the next
+    // block's rows of C are staged from here on
     if (threadIdx.x == 0) {
-      mma_split(tmem + kColG, opC, opBS, kIdescGY, false);
+      mma_split_ta(tmem + kColG, tmem + kColA, tmem + kColAlo, opBS, kIdescGY, false);
       mma_commit(&ctl->mma_bar);
+      if (more) stage_c(tn);
     }
     // ---- while it runs: per-token decays and sample starts, inclusive
     // scans over the block
@@ -334,52 +376,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         vec.rcend = rcend;
       }
     }
-    ok = __syncthreads_and(mbar_wait(&ctl->mma_bar, uses & 1, p.status, nullptr)) != 0;
+    ok = cta_wait_mma(&ctl->mma_bar, uses & 1, p.status);
     ++uses;
     if (!ok) break;
     tc_fence_after_sync();
     const float Pend = vec.Pend;
     const int rcend = vec.rcend;
-    // ---- M = G o mask o dt (rows = tokens t, K = tokens j), into C's place;
-    // a warp whose 32 columns all lie above its 32 rows writes zeros
-    if (cg > (warp & 3)) {
+    // ---- M = G o mask o dt (rows = tokens t, K = tokens j), into C's TMEM
+    // columns; a warp whose 32 columns all lie above its 32 rows writes zeros
+    {
+      uint32_t hi[16], lo[16];
+      if (cg > (warp & 3)) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t at = sw_chunk(kQ, row, cg * 4 + c);
-        *reinterpret_cast<uint4*>(smem + kOffC + at) = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(smem + kOffC + kPartCB + at) = make_uint4(0u, 0u, 0u, 0u);
-      }
-    } else {
-      uint32_t gv[32];
-      tmem_load_32(tmem + lane_off + kColG + cg * 32, gv);
-      const float pht = vec.Ph[row], plt = vec.Pl[row];
-      const int rct = vec.rc[row];
+        for (int i = 0; i < 16; ++i) hi[i] = lo[i] = 0u;
+      } else {
+        uint32_t gv[32];
+        tmem_load_32(tmem + lane_off + kColG + cg * 32, gv);
+        const float pht = vec.Ph[row], plt = vec.Pl[row];
+        const int rct = vec.rc[row];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int j0 = cg * 32 + c * 8;
-        float m[8];
-#pragma unroll
-        for (int i4 = 0; i4 < 8; i4 += 4) {
-          const float4 phj = *reinterpret_cast<const float4*>(&vec.Ph[j0 + i4]);
-          const float4 plj = *reinterpret_cast<const float4*>(&vec.Pl[j0 + i4]);
-          const float4 dj = *reinterpret_cast<const float4*>(&vec.dt[j0 + i4]);
-          const int4 rj = *reinterpret_cast<const int4*>(&vec.rc[j0 + i4]);
+        for (int i4 = 0; i4 < 32; i4 += 4) {
+          const int j0 = cg * 32 + i4;
+          const float4 phj = *reinterpret_cast<const float4*>(&vec.Ph[j0]);
+          const float4 plj = *reinterpret_cast<const float4*>(&vec.Pl[j0]);
+          const float4 dj = *reinterpret_cast<const float4*>(&vec.dt[j0]);
+          const int4 rj = *reinterpret_cast<const int4*>(&vec.rc[j0]);
           const float phv[4] = {phj.x, phj.y, phj.z, phj.w};
           const float plv[4] = {plj.x, plj.y, plj.z, plj.w};
           const float djv[4] = {dj.x, dj.y, dj.z, dj.w};
           const int rjv[4] = {rj.x, rj.y, rj.z, rj.w};
+          float m[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const int j = j0 + i4 + i;
+            const int j = j0 + i;
             const bool vis = j <= row && rjv[i] == rct;
             const float e = fast_exp2(vis ? (pht - phv[i]) + (plt - plv[i]) : -INFINITY);
-            m[i4 + i] = __uint_as_float(gv[c * 8 + i4 + i]) * e * djv[i];
+            m[i] = __uint_as_float(gv[i4 + i]) * e * djv[i];
           }
+          split2(m[0], m[1], &hi[i4 / 2], &lo[i4 / 2]);
+          split2(m[2], m[3], &hi[i4 / 2 + 1], &lo[i4 / 2 + 1]);
         }
-        const uint32_t at = sw_chunk(kQ, row, cg * 4 + c);
-        split8(m, reinterpret_cast<uint4*>(smem + kOffC + at),
-               reinterpret_cast<uint4*>(smem + kOffC + kPartCB + at));
       }
+      tmem_store_16(tmem + lane_off + kColA + cg * 16, hi);
+      tmem_store_16(tmem + lane_off + kColAlo + cg * 16, lo);
     }
     // ---- B_j scaled by v_j, over B's split in place: (v o B) read MN-major
     // is (v o B)^T
@@ -402,29 +441,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 16; ++i) sv[i] = __float_as_uint(__uint_as_float(sv[i]) * keep);
       tmem_store_16(tmem + lane_off + kColS + cg * 16, sv);
-      tmem_store_wait();
     }
+    tmem_store_wait();
     fence_proxy_async_smem();
     tc_fence_before_sync();
     __syncthreads();
     // ---- Ydia = M X, S^T += (v o B)^T X; meanwhile the scanning warps load
     // the next block's tokens
-    const bool more = b + 1 < nblocks;
-    const int tn = t0 + kQ;
     if (more) load_token(tn, min(kQ, c0 + L - tn));
     if (threadIdx.x == 0) {
       tc_fence_after_sync();
-      mma_split(tmem + kColYdia, opC, opX, kIdescYdia, false);
+      mma_split_ta(tmem + kColYdia, tmem + kColA, tmem + kColAlo, opX, kIdescYdia, false);
       mma_split(tmem + kColS, opVB, opX, kIdescS, b > 0);
       mma_commit(&ctl->mma_bar);
     }
-    ok = __syncthreads_and(mbar_wait(&ctl->mma_bar, uses & 1, p.status, nullptr)) != 0;
+    ok = cta_wait_mma(&ctl->mma_bar, uses & 1, p.status);
     ++uses;
     if (!ok) break;
     tc_fence_after_sync();
-    // C, B and x's space is free again: the next block's rows are staged
+    // B's and x's space is free again: the next block's rows are staged
     // there while this block's state and y are written out
-    if (more && threadIdx.x == 0) stage_rows(tn);
+    if (more && threadIdx.x == 0) stage_bx(tn);
     float4 xr[4];
     const size_t orow = ((size_t)(t0 + row) * p.H + h) * kP + cg * 16;
     if (row < n) {
@@ -504,7 +541,7 @@ cudaError_t launch_ssd_chunk_scan_tc(const SsdParams& p, const SsdMaps& maps,
   cudaError_t e = ensure_smem_limit(ssd_chunk_scan_tc_kernel, kSmem, g_configured);
   if (e != cudaSuccess) return e;
   TraceScope trace_scope(stream, "ssd_chunk_scan_tc_kernel");
-  ssd_chunk_scan_tc_kernel<<<dim3(p.H, p.R), kThreads, kSmem, stream>>>(p, maps.c, maps.b,
+  ssd_chunk_scan_tc_kernel<<<dim3(p.H, p.R), kThreads, kSmem, stream>>>(p, maps.c_sw, maps.b,
                                                                          maps.x);
   return cudaGetLastError();
 }

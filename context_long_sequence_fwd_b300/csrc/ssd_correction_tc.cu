@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int tn = t0 + kQ;
       load_token(tn, min(kQ, c0 + L - tn));
     }
-    ok = __syncthreads_and(mbar_wait(&ctl->mma_bar, b & 1, p.status, nullptr)) != 0;
+    ok = cta_wait_mma(&ctl->mma_bar, b & 1, p.status);
     if (!ok) break;
     tc_fence_after_sync();
     // C's space is free: the next block's rows are staged under the y update

@@ -57,6 +57,31 @@ __device__ __forceinline__ void mma_split(uint32_t d_tmem, const Operand& a, con
   }
 }
 
+// The same with A's split parts in TMEM (hi at a_hi, lo at a_lo: 128 lanes
+// x 64 columns each, two fp16 per column, K index 2c in the low half of
+// column c) and B in shared memory.
+__device__ __forceinline__ void mma_split_ta(uint32_t d_tmem, uint32_t a_hi, uint32_t a_lo,
+                                             const Operand& b, uint32_t idesc, bool accumulate) {
+#pragma unroll
+  for (int pass = 0; pass < 3; ++pass) {
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk)
+      mma_bf16_ts(d_tmem, (pass == 2 ? a_lo : a_hi) + kk * 8, op_desc(b, pass == 1, kk), idesc,
+                  (accumulate || pass > 0 || kk > 0) ? 1u : 0u);
+  }
+}
+
+// Waits for the MMAs committed to `bar` (phase `parity`): thread 0 polls the
+// mbarrier (bounded) and the rest of the CTA waits at a barrier, which does
+// not compete with the tensor core for shared-memory bandwidth the way 512
+// polling threads do.  Returns false for the whole CTA if the wait gave up.
+// The threads read the results (TMEM) after tcgen05.fence::after_thread_sync.
+__device__ __forceinline__ bool cta_wait_mma(uint64_t* bar, uint32_t parity, int* status) {
+  bool ok = true;
+  if (threadIdx.x == 0) ok = mbar_wait(bar, parity, status, nullptr);
+  return __syncthreads_and(ok) != 0;
+}
+
 // hi + lo split of a pair of fp32 values into fp16 pairs.  hi is x rounded
 // to 11 significant bits by Veltkamp's splitting (c = (2^13 + 1) x,
 // hi = c - (c - x), in fp32 arithmetic, each step rounded on its own: the
