@@ -18,9 +18,11 @@ from tests._util import max_err, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
-# fp32 arithmetic against fp64: each output sums at most a few hundred
-# decayed terms of magnitude ~1 (dt <= 0.1, |A| >= 1), so the rounding of the
-# fp32 path stays below 1e-5 relative to the outputs' scale.
+# fp32-level arithmetic against fp64 (state size 64: fp32 on CUDA cores;
+# state size 128: fp16 hi + lo split products, three per term, about 2^-22
+# of each product, accumulated in fp32): each output sums at most a few
+# hundred decayed terms of magnitude ~1 (dt <= 0.1, |A| >= 1), so the
+# rounding stays below 1e-5 relative to the outputs' scale.
 REL_TOL = 2e-5
 
 
@@ -51,6 +53,9 @@ CASES = [
     (2048, 4, 128, 4, 8, [300, 5, 1, 700, 1042]),
     (2048, 8, 64, 2, 8, [100] * 20 + [48]),       # samples shorter than a chunk
     (1536, 2, 128, 1, 3, [1536]),                 # positions from 0, one sample
+    (384, 2, 128, 1, 4, None),                    # chunks of 96: shorter than a 128-token block
+    (600, 4, 128, 2, 8, [37, 200, 1, 362]),       # chunks of 75 with sample starts inside
+    (512, 2, 128, 1, 1, None),                    # one rank: no state passing, no correction
 ]
 
 
