@@ -298,6 +298,7 @@ def run_ours(args):
     import torch
 
     import context_long_sequence_fwd_b300 as ra
+    from context_long_sequence_fwd_b300 import ring as ra_ring
     from context_long_sequence_fwd_b300.workloads import WORKLOADS, make_inputs
 
     world, rank, local = dist_setup()
@@ -320,13 +321,70 @@ def run_ours(args):
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         ws = torch.empty(max(ra.bwd_workspace_size(q, k), 16), dtype=torch.uint8, device=dev)
 
+    # The schedule: the fused single-GPU path (the default); the literal ring
+    # form, one launch per ring step plus log-sum-exp merges (forward); or the
+    # multi-GPU ring's per-rank schedule with all P ranks emulated on this GPU
+    # (each rank's own rows, buffers and stream; shard transfers by
+    # device-to-device copies), set up once outside the timed region.
+    sched = args.schedule
+    if sched == "stepwise" and backward:
+        raise SystemExit("--schedule stepwise times the forward: use --pass fwd")
+    if sched == "ring" and w.kv_exchange != ra.RING:
+        raise SystemExit("--schedule ring runs the ring exchange; this workload all-gathers K/V")
+    if sched == "stepwise":
+        ws_step = torch.empty(ra.fwd_stepwise_workspace_size(q, k, w.heads_k_stride),
+                              dtype=torch.uint8, device=dev)
+
+    def fwd_on(b):
+        if sched == "stepwise":
+            ra.ringattn_fwd_stepwise(b["q"], b["k"], b["v"], cu, w.num_shards, w.layout,
+                                     w.causal, b["out"], b["lse"], ws_step, stream,
+                                     w.heads_k_stride, w.kv_exchange)
+        elif sched == "ring":
+            o, l = ra_ring.emulate_ring_fwd(b["q"], b["k"], b["v"], num_shards=w.num_shards,
+                                            layout=w.layout, causal=w.causal, cu_seqlens=cu)
+            b["out"].copy_(o)
+            b["lse"].copy_(l)
+        else:
+            ra.ringattn_fwd(b["q"], b["k"], b["v"], cu, w.num_shards, w.layout, w.causal,
+                            b["out"], b["lse"], stream, w.heads_k_stride, w.kv_exchange)
+
+    def bwd_on(b):
+        if sched == "ring":
+            g = ra_ring.emulate_ring_bwd(b["q"], b["k"], b["v"], b["out"], b["lse"], b["do"],
+                                         num_shards=w.num_shards, layout=w.layout,
+                                         causal=w.causal, cu_seqlens=cu)
+            for n, t in zip(("dq", "dk", "dv"), g):
+                b[n].copy_(t)
+        else:
+            ra.ringattn_bwd(b["q"], b["k"], b["v"], b["out"], b["lse"], b["do"], cu,
+                            w.num_shards, w.layout, w.causal, b["dq"], b["dk"], b["dv"], ws,
+                            stream, w.heads_k_stride, kv_exchange=w.kv_exchange)
+
+    main_set = {"q": q, "k": k, "v": v, "out": out, "lse": lse}
+    if backward:
+        main_set.update(do=do, dq=dq, dk=dk, dv=dv)
+    emu = None
+    if sched == "ring":
+        # steady state of the emulated ring: the ranks already hold their rows
+        emu = ra_ring.EmulatedRing(q, k, v, num_shards=w.num_shards, layout=w.layout,
+                                   causal=w.causal, cu_seqlens=cu)
+        if backward:
+            ra.ringattn_fwd(q, k, v, cu, w.num_shards, w.layout, w.causal, out, lse, stream,
+                            w.heads_k_stride, w.kv_exchange)
+            emu.prepare_bwd(out, lse, do)
+
     def fwd():
-        ra.ringattn_fwd(q, k, v, cu, w.num_shards, w.layout, w.causal, out, lse, stream,
-                        w.heads_k_stride, w.kv_exchange)
+        if emu is not None:
+            emu.fwd()
+        else:
+            fwd_on(main_set)
 
     def bwd():
-        ra.ringattn_bwd(q, k, v, out, lse, do, cu, w.num_shards, w.layout, w.causal, dq, dk,
-                        dv, ws, stream, w.heads_k_stride, kv_exchange=w.kv_exchange)
+        if emu is not None:
+            emu.bwd()
+        else:
+            bwd_on(main_set)
 
     f_fwd = fwd_flops(w, cu)
     f_step = f_fwd * (3.5 if backward else 1.0)
@@ -420,9 +478,7 @@ def run_ours(args):
     # with compute: step i+1's inputs travel while step i computes, and step
     # i's outputs travel while step i+1 computes.
     h_in = [x[n].pin_memory() for n in (("q", "k", "v", "dout") if backward else ("q", "k", "v"))]
-    sets = [{"q": q, "k": k, "v": v, "out": out, "lse": lse}]
-    if backward:
-        sets[0].update(do=do, dq=dq, dk=dk, dv=dv)
+    sets = [main_set]
     sets.append({n: torch.empty_like(t) for n, t in sets[0].items()})
     in_names = ["q", "k", "v", "do"][:len(h_in)]
     out_names = ["out", "lse"] + (["dq", "dk", "dv"] if backward else [])
@@ -445,12 +501,9 @@ def run_ours(args):
         stream.wait_event(ev_in[i % 2])
         if i >= 2:
             stream.wait_event(ev_out[i % 2])       # step i-2's outputs have left this set
-        ra.ringattn_fwd(b["q"], b["k"], b["v"], cu, w.num_shards, w.layout, w.causal, b["out"],
-                        b["lse"], stream, w.heads_k_stride, w.kv_exchange)
+        fwd_on(b)
         if backward:
-            ra.ringattn_bwd(b["q"], b["k"], b["v"], b["out"], b["lse"], b["do"], cu,
-                            w.num_shards, w.layout, w.causal, b["dq"], b["dk"], b["dv"], ws,
-                            stream, w.heads_k_stride, kv_exchange=w.kv_exchange)
+            bwd_on(b)
         ev_done[i % 2].record(stream)
         with torch.cuda.stream(cout):
             cout.wait_event(ev_done[i % 2])
@@ -495,7 +548,10 @@ def run_ours(args):
     for name, (n, ms) in sorted(kernels.items(), key=lambda kv: -kv[1][1]):
         ent = {"launches": n, "avg_ms": round(ms / n, 4), "share": round(ms / k_total, 4)}
         if name in KERNEL_FWD_UNITS:
-            ent["tflops"] = round(KERNEL_FWD_UNITS[name] * f_fwd / (ms / n * 1e-3) / 1e12, 2)
+            # credited work per step over the kernel's device time per step (its
+            # launches per step: 1 fused, one per ring step and rank otherwise)
+            ent["tflops"] = round(KERNEL_FWD_UNITS[name] * f_fwd * args.steps / (ms * 1e-3)
+                                  / 1e12, 2)
         ktab[name] = ent
     top = max((n for n in ktab if n in KERNEL_FWD_UNITS), key=lambda n: ktab[n]["share"])
     achieved = ktab[top]["tflops"]
@@ -505,7 +561,7 @@ def run_ours(args):
             "frac_of_sustained": round(achieved / peak_s, 4),
             "power_capped": power_capped(clk),
             "traffic": kernel_traffic(top, args.workload),
-            "flops_per_launch": KERNEL_FWD_UNITS[top] * f_fwd}
+            "flops_per_launch": KERNEL_FWD_UNITS[top] * f_fwd * args.steps / ktab[top]["launches"]}
     fwd_mean = statistics.mean(fwd_ms)
     fwd_tf = f_fwd / (fwd_mean * 1e-3) / 1e12
     line = {
@@ -513,7 +569,8 @@ def run_ours(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q, k, v, dO rounded to bf16)",
-        "config": workload_config(w, cu, args.pass_, world, args.seed),
+        "config": {**workload_config(w, cu, args.pass_, world, args.seed),
+                   **({} if sched == "fused" else {"schedule": sched})},
         "fwd": {"ms": round(fwd_mean, 4), "tflops": round(fwd_tf, 2),
                 "frac": round(fwd_tf / peak, 4), "frac_of_sustained": round(fwd_tf / peak_s, 4)},
         "roofline": roof,
@@ -747,6 +804,10 @@ def main():
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "fwdbwd"], default="fwdbwd",
                     help="fwd: forward only; fwdbwd: forward then backward (the whole path)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--schedule", choices=["fused", "stepwise", "ring"], default="fused",
+                    help="fused single-GPU path; stepwise: one launch per ring step plus "
+                         "merges (forward); ring: the multi-GPU ring's per-rank schedule with "
+                         "the P ranks emulated on this GPU")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample")

@@ -21,10 +21,10 @@ with the log-sum-exp merge).  Two transports share the schedule:
 * ring_fwd / ring_bwd: one process per rank, torch.distributed point-to-point
   operations on the default process group (NCCL between GPUs; the
   bookkeeping works with any backend);
-* emulate_ring_fwd / emulate_ring_bwd: all P ranks in one process on one GPU,
-  each rank with its own device buffers and its own stream, the shards passed
-  by device-to-device copies ordered with events -- the same schedule, to
-  check it without P GPUs.
+* EmulatedRing (and emulate_ring_fwd / emulate_ring_bwd on top of it): all P
+  ranks in one process on one GPU, each rank with its own device buffers and
+  its own stream, the shards passed by device-to-device copies ordered with
+  events -- the same schedule, to check and time it without P GPUs.
 
 Buffers of rank r hold its rows back to back: CONTIGUOUS tokens
 [r T/P, (r+1) T/P); ZIGZAG chunk r then chunk 2P-1-r of 2P equal chunks.
@@ -202,35 +202,83 @@ def ring_bwd(q, k, v, out, lse, dout, *, total_tokens, layout, causal, cu_seqlen
 
 # --------------------------------------- every rank on one GPU (emulation)
 
-def emulate_ring_fwd(q, k, v, *, num_shards, layout, causal, cu_seqlens=None):
-    """The multi-GPU ring forward with all P ranks on this GPU.
+class EmulatedRing:
+    """The multi-GPU ring with all P ranks on this GPU, set up once and run as
+    often as wanted.  Each rank holds its own rows (copied in here), its own
+    receive buffers (two per field: double buffering) and its own stream; the
+    shards move by device-to-device copies on the sender's stream, ordered by
+    events -- the schedule of ring_fwd / ring_bwd without P GPUs.
 
-    q, k, v are whole-sequence tensors; each rank gets its own copies of its
-    rows, its own stream and its own receive buffers, and the shards move by
-    device-to-device copies on the sender's stream, ordered by events.
-    Returns whole-sequence (out, lse) gathered from the ranks."""
-    import torch
-    P, T = num_shards, q.shape[0]
-    qs = [shard(q, P, layout, r) for r in range(P)]
-    cur = [[shard(k, P, layout, r), shard(v, P, layout, r)] for r in range(P)]
-    bufs = [[[torch.empty_like(t) for t in cur[r]] for _ in range(2)] for r in range(P)]
-    streams = [torch.cuda.Stream(device=q.device) for _ in range(P)]
-    ranks = [FwdRank(qs[r], T, P, layout, causal, r, cu_seqlens) for r in range(P)]
-    start = torch.cuda.current_stream(q.device)
-    for st in streams:
-        st.wait_stream(start)
-    for s in range(P):
-        computed = [torch.cuda.Event() for _ in range(P)]
-        for r in range(P):
-            with torch.cuda.stream(streams[r]):
-                ranks[r](s, *cur[r], stream=streams[r])
-                computed[r].record(streams[r])
-        if s + 1 < P:
-            _emulated_pass_on(cur, bufs, s, streams, computed, range(2))
-    for st in streams:
-        start.wait_stream(st)
-    outs, lses = zip(*(rk.result() for rk in ranks))
-    return unshard(outs, P, layout), unshard(lses, P, layout, dim=1)
+    fwd() returns every rank's (out, lse) rows; bwd(), after
+    prepare_bwd(out, lse, dout), every rank's fp32 (dq, dk, dv) rows."""
+
+    def __init__(self, q, k, v, *, num_shards, layout, causal, cu_seqlens=None):
+        import torch
+        P, T = num_shards, q.shape[0]
+        self.P, self.T, self.layout, self.causal, self.cu = P, T, layout, causal, cu_seqlens
+        self.kv = [[shard(k, P, layout, r), shard(v, P, layout, r)] for r in range(P)]
+        self.fwd_ranks = [FwdRank(shard(q, P, layout, r), T, P, layout, causal, r, cu_seqlens)
+                          for r in range(P)]
+        self.fwd_bufs = [[[torch.empty_like(t) for t in self.kv[r]] for _ in range(2)]
+                         for r in range(P)]
+        self.streams = [torch.cuda.Stream(device=q.device) for _ in range(P)]
+        self.bwd_ranks = None
+
+    def _run(self, ranks, cur, bufs, fields):
+        """The P ring steps: every rank computes step s on its stream, then
+        passes what it holds on to the next rank (none after the last step)."""
+        import torch
+        P = self.P
+        start = torch.cuda.current_stream(self.streams[0].device)
+        for st in self.streams:
+            st.wait_stream(start)
+        for s in range(P):
+            computed = [torch.cuda.Event() for _ in range(P)]
+            for r in range(P):
+                with torch.cuda.stream(self.streams[r]):
+                    ranks[r](s, *cur[r], stream=self.streams[r])
+                    computed[r].record(self.streams[r])
+            if s + 1 < P:
+                _emulated_pass_on(cur, bufs, s, self.streams, computed, fields)
+        for st in self.streams:
+            start.wait_stream(st)
+
+    def fwd(self):
+        self._run(self.fwd_ranks, [list(kv) for kv in self.kv], self.fwd_bufs, range(2))
+        return [rk.result() for rk in self.fwd_ranks]
+
+    def prepare_bwd(self, out, lse, dout):
+        """The backward's per-rank rows of the whole-sequence forward results
+        out [T, Hq, D], lse [Hq, T] and of dout, and its buffers."""
+        import torch
+        P, layout = self.P, self.layout
+        self.bwd_ranks = [BwdRank(self.fwd_ranks[r].q, shard(out, P, layout, r),
+                                  shard(lse.t(), P, layout, r).t().contiguous(),
+                                  shard(dout, P, layout, r), self.T, P, layout, self.causal, r,
+                                  self.cu) for r in range(P)]
+        f32 = dict(dtype=torch.float32, device=out.device)
+        self.dkv = [[torch.empty(kv[0].shape, **f32), torch.empty(kv[1].shape, **f32)]
+                    for kv in self.kv]
+        self.bwd_bufs = [[[torch.empty_like(t) for t in self.kv[r] + self.dkv[r]]
+                          for _ in range(2)] for r in range(P)]
+
+    def bwd(self):
+        P = self.P
+        cur = [self.kv[r] + self.dkv[r] for r in range(P)]
+        self._run(self.bwd_ranks, cur, self.bwd_bufs, range(4))
+        # rank r holds the finished dK/dV of rank (r + 1) mod P
+        return ([rk.dq for rk in self.bwd_ranks], [cur[(r - 1) % P][2] for r in range(P)],
+                [cur[(r - 1) % P][3] for r in range(P)])
+
+
+def emulate_ring_fwd(q, k, v, *, num_shards, layout, causal, cu_seqlens=None):
+    """The multi-GPU ring forward with all P ranks on this GPU (EmulatedRing).
+    q, k, v are whole-sequence tensors; returns whole-sequence (out, lse)
+    gathered from the ranks."""
+    ring = EmulatedRing(q, k, v, num_shards=num_shards, layout=layout, causal=causal,
+                        cu_seqlens=cu_seqlens)
+    outs, lses = zip(*ring.fwd())
+    return unshard(outs, num_shards, layout), unshard(lses, num_shards, layout, dim=1)
 
 
 def _emulated_pass_on(cur, bufs, s, streams, computed, fields):
@@ -255,36 +303,12 @@ def _emulated_pass_on(cur, bufs, s, streams, computed, fields):
 
 
 def emulate_ring_bwd(q, k, v, out, lse, dout, *, num_shards, layout, causal, cu_seqlens=None):
-    """The multi-GPU ring backward with all P ranks on this GPU (see
-    emulate_ring_fwd).  out and lse are whole-sequence forward results.
-    Returns whole-sequence fp32 (dq, dk, dv)."""
-    import torch
-    P, T = num_shards, q.shape[0]
-    f32 = dict(dtype=torch.float32, device=k.device)
-    ranks = [BwdRank(shard(q, P, layout, r), shard(out, P, layout, r),
-                     shard(lse.t(), P, layout, r).t().contiguous(), shard(dout, P, layout, r),
-                     T, P, layout, causal, r, cu_seqlens) for r in range(P)]
-    cur = []
-    for r in range(P):
-        kr, vr = shard(k, P, layout, r), shard(v, P, layout, r)
-        cur.append([kr, vr, torch.empty(kr.shape, **f32), torch.empty(vr.shape, **f32)])
-    bufs = [[[torch.empty_like(t) for t in cur[r]] for _ in range(2)] for r in range(P)]
-    streams = [torch.cuda.Stream(device=q.device) for _ in range(P)]
-    start = torch.cuda.current_stream(q.device)
-    for st in streams:
-        st.wait_stream(start)
-    for s in range(P):
-        computed = [torch.cuda.Event() for _ in range(P)]
-        for r in range(P):
-            with torch.cuda.stream(streams[r]):
-                ranks[r](s, *cur[r], stream=streams[r])
-                computed[r].record(streams[r])
-        if s + 1 < P:
-            _emulated_pass_on(cur, bufs, s, streams, computed, range(4))
-    for st in streams:
-        start.wait_stream(st)
-    # rank r holds the finished dK/dV of rank (r + 1) mod P
-    dks = [cur[(r - 1) % P][2] for r in range(P)]
-    dvs = [cur[(r - 1) % P][3] for r in range(P)]
-    return (unshard([rk.dq for rk in ranks], P, layout), unshard(dks, P, layout),
-            unshard(dvs, P, layout))
+    """The multi-GPU ring backward with all P ranks on this GPU (EmulatedRing).
+    out and lse are whole-sequence forward results.  Returns whole-sequence
+    fp32 (dq, dk, dv)."""
+    ring = EmulatedRing(q, k, v, num_shards=num_shards, layout=layout, causal=causal,
+                        cu_seqlens=cu_seqlens)
+    ring.prepare_bwd(out, lse, dout)
+    dqs, dks, dvs = ring.bwd()
+    return (unshard(dqs, num_shards, layout), unshard(dks, num_shards, layout),
+            unshard(dvs, num_shards, layout))
