@@ -31,6 +31,19 @@ def test_flop_accounting():
     assert bench.visible_pairs(v, cu) == 1000 * 1001 // 2 + 64536 * 64537 // 2
 
 
+def test_ssd_flop_accounting():
+    # the recurrence: one multiply-add into the state and one into y per
+    # token, head and state entry
+    assert bench.ssd_flops(32768, 128, 64, 128) == 4.0 * 32768 * 128 * 64 * 128
+    # the chunk scan's executed fp16 products per 128-token block:
+    # [G | Yoff] 128 x (128 + 64) x 128, Ydia 128 x 64 x 128, S^T 128 x 64 x 128,
+    # three products each for the hi/lo split
+    per_block = 3 * 2.0 * (128 * 192 * 128 + 128 * 64 * 128 + 128 * 64 * 128)
+    assert bench.ssd_tc_flops(32768, 128, 64, 128, 8) == 8 * 128 * 32 * per_block
+    # chunks of 250 tokens: two blocks each, the second one partial
+    assert bench.ssd_tc_flops(1000, 4, 64, 128, 4) == 4 * 4 * 2 * per_block
+
+
 def free_port():
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))
