@@ -135,6 +135,81 @@ __global__ void __launch_bounds__(256, 3) lse_merge_kernel(const void* o_a, bool
     lse_out[(size_t)h * rows + row] = L;
 }
 
+// Both inputs fp32 (the stepwise forward's running result and a step's
+// partial): one warp per (row, head) pair and 16 bytes per lane, so each load
+// instruction of a warp reads one pair's D contiguous floats (512 B at
+// D = 128; at D = 64 a half-warp per pair, two pairs per instruction); each
+// warp keeps kPairs pairs' loads in flight before it computes.
+template <int kD, int kPairs>
+__global__ void __launch_bounds__(256) lse_merge_f32_kernel(const float* o_a, const float* lse_a,
+                                                          const float* o_b, const float* lse_b,
+                                                          void* o_out, bool out_fp32,
+                                                          float* lse_out, int rows, int heads,
+                                                          long long pairs, int* status) {
+  constexpr int kLanes = kD / 4;        // lanes per pair
+  constexpr int kPerWarp = 32 / kLanes;  // pairs per warp instruction
+  const int lane = threadIdx.x & 31;
+  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int sub = lane / kLanes, col = (lane % kLanes) * 4;
+  const long long n_l = (long long)rows * heads;
+  float4 x[kPairs], y[kPairs];
+  float a[kPairs], b[kPairs];
+  long long pr[kPairs];
+#pragma unroll
+  for (int i = 0; i < kPairs; ++i) {
+    pr[i] = (warp * kPairs + i) * kPerWarp + sub;  // pair = row * heads + head
+    a[i] = b[i] = -INFINITY;
+    if (pr[i] < pairs && !index_ok(pr[i] * kD + col + 3, pairs * kD, status, kSiteMerge))
+      pr[i] = pairs;  // (debug build) a failed check skips the pair
+    if (pr[i] < pairs) {
+      const int row = (int)(pr[i] / heads), h = (int)(pr[i] % heads);
+      const long long at = checked((long long)h * rows + row, n_l, status, kSiteMerge);
+      a[i] = lse_a[at];
+      b[i] = lse_b[at];
+      x[i] = *reinterpret_cast<const float4*>(o_a + pr[i] * kD + col);
+      y[i] = *reinterpret_cast<const float4*>(o_b + pr[i] * kD + col);
+    }
+  }
+  // every lane of a pair has read lse_a before any lane overwrites it
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < kPairs; ++i) {
+    if (pr[i] >= pairs) continue;
+    const bool ea = a[i] == -INFINITY, eb = b[i] == -INFINITY;
+    float L = -INFINITY, wa = 0.f, wb = 0.f;
+    if (!ea && !eb) {
+      const float mx = fmaxf(a[i], b[i]);
+      L = mx + log1pf(expf(-fabsf(a[i] - b[i])));
+      wa = expf(a[i] - L);
+      wb = expf(b[i] - L);
+    } else if (!ea) {
+      L = a[i];
+      wa = 1.f;
+    } else if (!eb) {
+      L = b[i];
+      wb = 1.f;
+    }
+    // an empty side contributes exactly nothing, whatever its o holds
+    float r[4];
+    const float xa[4] = {x[i].x, x[i].y, x[i].z, x[i].w}, yb[4] = {y[i].x, y[i].y, y[i].z, y[i].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      r[e] = ea ? (eb ? 0.f : yb[e]) : (eb ? xa[e] : fmaf(wa, xa[e], wb * yb[e]));
+    const long long idx = pr[i] * kD + col;
+    if (out_fp32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(o_out) + idx) = make_float4(r[0], r[1], r[2], r[3]);
+    } else {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(r[0], r[1]), hi = __floats2bfloat162_rn(r[2], r[3]);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(o_out) + idx) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+    }
+    if (col == 0) {
+      const int row = (int)(pr[i] / heads), h = (int)(pr[i] % heads);
+      lse_out[(size_t)h * rows + row] = L;
+    }
+  }
+}
+
 // The two halves of each split item of the fused forward.  One warp per row
 // of a split query tile (CTA c covers rows 4 (c % 32) .. + 3 of tile
 // (c / 32) % 2 of pair c / 64), so every row's loads are in flight at once;
@@ -236,6 +311,21 @@ cudaError_t launch_lse_merge(const void* o_a, bool a_fp32, const float* lse_a, c
                              cudaStream_t stream) {
   const long long pairs = (long long)rows * heads;
   if (pairs == 0) return cudaSuccess;
+  if (a_fp32 && b_fp32 && (D == 128 || D == 64)) {
+    constexpr int kPairs = 4;
+    const long long warps = (pairs * (D / 4) / 32 + kPairs - 1) / kPairs;
+    const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
+    TraceScope trace_scope(stream, "lse_merge_kernel");
+    if (D == 128)
+      lse_merge_f32_kernel<128, kPairs><<<grid, 256, 0, stream>>>(
+          static_cast<const float*>(o_a), lse_a, static_cast<const float*>(o_b), lse_b, o_out,
+          out_fp32, lse_out, rows, heads, pairs, status);
+    else
+      lse_merge_f32_kernel<64, kPairs><<<grid, 256, 0, stream>>>(
+          static_cast<const float*>(o_a), lse_a, static_cast<const float*>(o_b), lse_b, o_out,
+          out_fp32, lse_out, rows, heads, pairs, status);
+    return cudaGetLastError();
+  }
   const int chunks = D / 8 < 4 ? D / 8 : 4;
   const long long threads = pairs * (D / 8 / chunks);
   const int block = 256;
