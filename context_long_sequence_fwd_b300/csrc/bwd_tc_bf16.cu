@@ -8,10 +8,12 @@
 // with atomics and the result does not depend on scheduling:
 //
 //   bwd_dkdv_kernel  one CTA per 128-key tile of one key/value head.  It walks
-//     the query tiles that see the keys in ring order (at step s the keys of
-//     rank src sit on rank (src + s) mod P) and, for GQA, every query head of
-//     the group, accumulating dK and dV in TMEM (so they come out summed over
-//     the group).  Each query tile is split into two 64-row halves handled
+//     the query tiles that see the keys -- those of the ring steps: at step s
+//     the keys of rank src sit on rank (src + s) mod P -- in the order of its
+//     plan's segments (the whole-GPU plan goes from the end of the sequence
+//     down, for L2 reuse across CTAs) and, for GQA, every query head of the
+//     group, accumulating dK and dV in TMEM (so they come out summed over the
+//     group).  Each query tile is split into two 64-row halves handled
 //     by two softmax warpgroups, so one half's elementwise work overlaps the
 //     other half's MMAs:
 //       S^T  = K Q_h^T        (M = 128 keys, N = 64 queries, K = D)

@@ -289,6 +289,16 @@ BwdPlan build_bwd_plan(const PlanInput& in) {
               }
             }
             it.seg_count = static_cast<int32_t>(plan.segs.size()) - it.seg_begin;
+            // The whole-GPU plan walks an item's query segments from the end of
+            // the sequence down instead of in ring order: the co-resident CTAs
+            // of a pass then read the same query chunks at about the same
+            // time, so each Q/dO tile comes from DRAM about once per pass
+            // instead of once per CTA that misses it in L2.  The sum over the
+            // segments is the same up to fp32 rounding order; each segment
+            // keeps its ring step and rank.
+            if (in.q_rank < 0 && in.k_rank < 0)
+              std::sort(plan.segs.begin() + it.seg_begin, plan.segs.end(),
+                        [](const BwdSegment& x, const BwdSegment& y) { return x.q0 > y.q0; });
             it.cost = cost;
             plan.items.push_back(it);
           }

@@ -55,8 +55,10 @@ struct Plan {
 };
 
 // Backward, key/value side: one CTA per 128-key tile of one key/value head.
-// Its query ranges come in ring order: at step s the K/V shard of rank `src`
-// sits on rank (src + s) mod P, whose queries contribute to its dK, dV.
+// Its query ranges are those of the ring steps: at step s the K/V shard of
+// rank `src` sits on rank (src + s) mod P, whose queries contribute to its
+// dK, dV.  In the whole-GPU plan they come from the end of the sequence down
+// (L2 reuse across co-resident CTAs); with a rank filter, in ring order.
 struct BwdItem {
   int32_t k0;         // first key of the tile
   int32_t klen;       // keys of the tile (<= 128; the tile stays in one chunk)
