@@ -9,11 +9,13 @@
 // Parallelism" page, "Mamba/SSM Hybrid Models": an additive correction, no
 // second forward pass).
 //
-// CTA (h, r), 256 threads, a block of 128 tokens at a time:
+// CTA (h, r, segment), 256 threads, a block of 128 tokens at a time:
 //   Yc = C H_r^T    (M = 128 tokens, N = 64 head dims, K = 128 state) in TMEM,
 //   y_t += w_t Yc_t,  w_t = 2^(lam_t) before the first sample start, else 0,
 // with lam_t the running sum of dt A log2(e) from the chunk start, kept in
-// float-float arithmetic.  C and H are split into fp16 hi + lo and the
+// float-float arithmetic.  A chunk's blocks are cut into kSegs segments, one
+// CTA each, which starts from the exponent summed over the chunk's tokens
+// before it.  C and H are split into fp16 hi + lo and the
 // product is formed from three fp16 products (ssd_tc_common.cuh), which
 // keeps fp32-level accuracy.  C's fp32 rows are staged by TMA in the space
 // of their split operand and split in place; the next block's rows are
@@ -48,6 +50,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 // log2 of a factor that is exactly zero in fp32 (denormals underflow below
 // 2^-149), with a margin for the float-float rounding of the exponent
 constexpr float kDeadLog2 = -160.f;
+// A chunk's blocks are split into this many segments, one CTA each: the
+// chains of weakly decaying heads without an early sample start, which walk
+// the whole chunk, would otherwise set the kernel's length.
+constexpr int kSegs = 4;
 
 constexpr int kPartH = kP * kN * 2;  // H_r: 64 rows x 128 fp16, two 8 KB K blocks
 constexpr int kPartC = kQ * kN * 2;  // C: 128 rows x 128 fp16, two 16 KB K blocks
@@ -61,6 +67,8 @@ struct Vec {
   int wcnt[4];           // per-warp sample starts
   float lam_h, lam_l;    // exponent at the end of the blocks so far
   int stop;              // the CTA ends after this block
+  float red_h[8], red_l[8];  // per-warp parts of the segment's starting exponent
+  int red_c[8];              // and of the sample starts before it
 };
 constexpr int kOffCtl = kOffVec + ((sizeof(Vec) + 127) / 128) * 128;
 
@@ -100,6 +108,44 @@ __global__ void __launch_bounds__(kThreads, 2)
       !index_ok((long long)c0 + L - 1, p.T, p.status, kSiteSsd))
     return;
   const float A2 = p.A[h] * kLog2e;
+  // this CTA's segment: blocks [bb, be) of the chunk
+  const int nblocks = (L + kQ - 1) / kQ;
+  const int bps = (nblocks + kSegs - 1) / kSegs;
+  const int bb = blockIdx.z * bps, be = min(bb + bps, nblocks);
+  if (bb >= be) return;
+  const int s0 = c0 + bb * kQ;  // the segment's first token
+  // the exponent at the segment's start (float-float sum of dt A log2(e) over
+  // the chunk's tokens before it) and the sample starts there: after one,
+  // or once the exponent is dead, the segment corrects nothing
+  float lam0_h = 0.f, lam0_l = 0.f;
+  {
+    float sh = 0.f, sl = 0.f;
+    int starts = 0;
+    for (int t = c0 + static_cast<int>(threadIdx.x); t < s0; t += kThreads) {
+      ff_add(sh, sl, p.dt[(size_t)t * p.H + h] * A2, 0.f);
+      if (p.pos != nullptr && p.pos[t] == 0) ++starts;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float uh = __shfl_down_sync(0xffffffffu, sh, o);
+      const float ul = __shfl_down_sync(0xffffffffu, sl, o);
+      starts += __shfl_down_sync(0xffffffffu, starts, o);
+      ff_add(sh, sl, uh, ul);
+    }
+    if (lane == 0) {
+      vec.red_h[warp] = sh;
+      vec.red_l[warp] = sl;
+      vec.red_c[warp] = starts;
+    }
+    __syncthreads();
+    int total = 0;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+      ff_add(lam0_h, lam0_l, vec.red_h[w], vec.red_l[w]);
+      total += vec.red_c[w];
+    }
+    if (total > 0 || lam0_h + lam0_l < kDeadLog2) return;  // the same for every thread
+  }
 
   const Operand opC{sbase + kOffC, kPartC, kQ * 128, false};
   const Operand opH{sbase + kOffH, kPartH, kP * 128, false};
@@ -110,7 +156,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     mbar_init(&ctl->done_bar, 1);
     fence_barrier_init();
     tma_prefetch_map(&map_c);
-    vec.lam_h = vec.lam_l = 0.f;
+    vec.lam_h = lam0_h;
+    vec.lam_l = lam0_l;
   }
   if (warp == 0) {
     tmem_alloc(&ctl->tmem_base, 64);
@@ -148,9 +195,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     tok_dt = in ? p.dt[(size_t)(tb + threadIdx.x) * p.H + h] : 0.f;
     tok_pos = (in && p.pos != nullptr) ? p.pos[tb + threadIdx.x] : 1;
   };
-  load_token(c0, min(kQ, L));
+  load_token(s0, min(kQ, c0 + L - s0));
   __syncthreads();  // barriers initialised
-  if (threadIdx.x == 0) stage_rows(c0);
+  if (threadIdx.x == 0) stage_rows(s0);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -160,11 +207,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
   bool ok = true;
-  const int nblocks = (L + kQ - 1) / kQ;
-  for (int b = 0; b < nblocks; ++b) {
+  for (int b = bb; b < be; ++b) {
     const int t0 = c0 + b * kQ;
     const int n = min(kQ, c0 + L - t0);
-    ok = __syncthreads_and(mbar_wait(&ctl->tma_bar, b & 1, p.status, nullptr)) != 0;
+    const uint32_t phase = (b - bb) & 1;
+    ok = __syncthreads_and(mbar_wait(&ctl->tma_bar, phase, p.status, nullptr)) != 0;
     if (!ok) break;
     // ---- the exponent of each token and the sample starts: inclusive scans
     // (warps 0-3, one token each), on top of the blocks before
@@ -244,12 +291,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       mma_split(tmem, opC, opH, kIdesc, false);
       mma_commit(&ctl->mma_bar);
     }
-    const bool last = vec.stop != 0 || b + 1 == nblocks;
+    const bool last = vec.stop != 0 || b + 1 == be;
     if (!last) {
       const int tn = t0 + kQ;
       load_token(tn, min(kQ, c0 + L - tn));
     }
-    ok = cta_wait_mma(&ctl->mma_bar, b & 1, p.status);
+    ok = cta_wait_mma(&ctl->mma_bar, phase, p.status);
     if (!ok) break;
     tc_fence_after_sync();
     // C's space is free: the next block's rows are staged under the y update
@@ -303,7 +350,7 @@ cudaError_t launch_ssd_correction_tc(const SsdParams& p, const SsdMaps& maps,
   cudaError_t e = ensure_smem_limit(ssd_correction_tc_kernel, kSmem, g_configured);
   if (e != cudaSuccess) return e;
   TraceScope trace_scope(stream, "ssd_correction_tc_kernel");
-  ssd_correction_tc_kernel<<<dim3(p.H, p.R - 1), kThreads, kSmem, stream>>>(p, maps.c);
+  ssd_correction_tc_kernel<<<dim3(p.H, p.R - 1, kSegs), kThreads, kSmem, stream>>>(p, maps.c);
   return cudaGetLastError();
 }
 
