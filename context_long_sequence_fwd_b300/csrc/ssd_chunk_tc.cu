@@ -18,34 +18,35 @@
 //   y_t  = [rc_t == 0] 2^P_t (C_t . S0)               the block's incoming state
 //        + sum_j same(t, j) 2^(P_t - P_j) dt_j (C_t . B_j) x_j + D x_t
 //   S    = [rc_end == 0] 2^P_end S0 + sum_j [rc_j == rc_end] 2^(P_end - P_j) dt_j x_j B_j^T
-// as four products on the tensor cores, every one with M = 128:
-//   G    = C B^T           (tokens x tokens, over the state)          TMEM cols   0-127
-//   Yoff = C S0^T          (tokens x head dim, over the state)        TMEM cols 128-191
-//   Ydia = M X, M = G o mask o dt  (tokens x head dim, over tokens)   TMEM cols 192-255
-//   S^T += (v o B)^T X     (state x head dim, over tokens; the fp32   TMEM cols 256-319
-//                           state lives in TMEM across the blocks)
+// as products on the tensor cores, every one with M = 128:
+//   [G | Yoff] = C [B | S0]^T  (tokens x (tokens + head dim), over the     TMEM cols 0-191
+//                              state: one N = 192 product)
+//   Ydia = M X, M = G o mask o dt  (tokens x head dim, over tokens)        TMEM cols 192-255
+//   S^T += (v o B)^T X     (state x head dim, over tokens; the fp32 state   TMEM cols 256-319
+//                           lives in TMEM across the blocks)
 // The scan is checked to fp32-level accuracy (2e-5 relative), which one
 // 16-bit product per term cannot reach, so every operand a is split into
-// fp16 a_hi + a_lo (a_lo = a - a_hi, rounded again) and each product a b is
-// formed as a_hi b_hi + a_hi b_lo + a_lo b_hi, accumulated in fp32: the
-// dropped a_lo b_lo and the rounding of the lo parts leave about 2^-22 of
-// each product.  fp16 keeps 11 significant bits where bf16 keeps 8; the
-// operands here (inputs of order 1, decay factors <= 1) sit well inside its
-// range.
+// fp16 a_hi + a_lo (a_hi: a rounded to 11 significant bits; a_lo = a - a_hi,
+// rounded once) and each product a b is formed as a_hi b_hi + a_hi b_lo +
+// a_lo b_hi, accumulated in fp32: the dropped a_lo b_lo and the rounding of
+// the lo parts leave about 2^-22 of each product.  fp16 keeps 11 significant
+// bits where bf16 keeps 8; the operands here (inputs of order 1, decay
+// factors <= 1) sit well inside its range.
 //
-// Operands are written into shared memory by the threads (the inputs are
-// fp32 in memory and are split on the way) with the 128-byte swizzle the MMA
-// descriptors describe.  C and M are K-major; B, x, v o B and S0 keep rows of
-// their own K index: B is K-major for G, and read in place as the MN-major A
-// operand of the state update once each row has been scaled by v_j; x is the
-// MN-major B operand of both token contractions, S0 (rows = state) that of
-// Yoff.
+// C and M, the A operands of the token products, live in TMEM (cols 320-447,
+// two fp16 per column), written by the threads with tcgen05.st.  B, x, v o B
+// and S0 are in shared memory with the 128-byte swizzle the MMA descriptors
+// describe: B's 128 token rows and S0's 64 rows form one K-major operand
+// (K = state); B's rows, once scaled by v_j in place, are read as the
+// MN-major A operand of the state update; x is the MN-major B operand of both
+// token contractions.  The inputs are fp32 in memory: TMA stages a block's
+// rows (C in swizzled boxes of its own, B and x in the space of their split
+// operands) and the threads split them.
 // One CTA per (head, rank), 512 threads; one thread issues the MMAs.  A block
-// runs: G, Yoff issued | the decay scan, while they run | the masked M, the
-// scaling of B by v, the state's decay | Ydia, S^T issued | the next block's
-// rows of C and B loaded into registers, while they run | the next block's
-// operands split into the freed shared memory, S0 out, y out.  Every barrier wait is
-// bounded.
+// runs: C, B and x split | [G | Yoff] issued, the next block's C staged and
+// the decay scan while it runs | the masked M, the scaling of B by v, the
+// state's decay | Ydia, S^T issued | the next block's B and x staged, S0 out,
+// y out.  Every barrier wait is bounded.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
