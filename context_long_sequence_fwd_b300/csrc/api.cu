@@ -16,6 +16,7 @@
 #include "launch.h"
 #include "planner.h"
 #include "ringattn.h"
+#include "trace.h"
 
 namespace ra {
 
@@ -443,6 +444,7 @@ extern "C" {
 ra_status ringattn_fwd(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
                        ra_dims dims, int num_shards, int shard_layout, int causal, void* out,
                        float* lse, void* stream) {
+  NvtxRange nvtx("ringattn_fwd");
   PlanInput in;
   ra_status st = check_problem(cu_seqlens, dims, num_shards, shard_layout, causal, &in);
   if (st != RA_OK) return st;
@@ -497,6 +499,7 @@ ra_status ringattn_fwd_stepwise(const void* q, const void* k, const void* v,
                                 const int32_t* cu_seqlens, ra_dims dims, int num_shards,
                                 int shard_layout, int causal, void* out, float* lse,
                                 void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx("ringattn_fwd_stepwise");
   PlanInput in;
   ra_status st = check_problem(cu_seqlens, dims, num_shards, shard_layout, causal, &in);
   if (st != RA_OK) return st;
@@ -591,6 +594,7 @@ extern "C" ra_status ringattn_fwd_stepwise_noalloc(const void* q, const void* k,
                                                    const int32_t* cu_seqlens, ra_dims dims,
                                                    int num_shards, int shard_layout, int causal,
                                                    void* out, float* lse, void* stream) {
+  NvtxRange nvtx("ringattn_fwd_stepwise_noalloc");
   PlanInput in;
   ra_status st = check_problem(cu_seqlens, dims, num_shards, shard_layout, causal, &in);
   if (st != RA_OK) return st;
@@ -663,6 +667,7 @@ ra_status ringattn_bwd(const void* q, const void* k, const void* v, const void* 
                        const float* lse, const void* dout, const int32_t* cu_seqlens,
                        ra_dims dims, int num_shards, int shard_layout, int causal, void* dq,
                        void* dk, void* dv, void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx("ringattn_bwd");
   PlanInput in;
   ra_status st = check_problem(cu_seqlens, dims, num_shards, shard_layout, causal, &in);
   if (st != RA_OK) return st;
@@ -753,6 +758,7 @@ ra_status ringattn_fwd_rank_step(const void* q, const void* k, const void* v,
                                  int shard_layout, int causal, int rank, int step, float* o_acc,
                                  float* lse_acc, void* out, float* lse, void* workspace,
                                  size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx("ringattn_fwd_rank_step");
   PlanInput in;
   int Tr = 0;
   ra_status st = check_rank_step(cu_seqlens, dims, num_shards, shard_layout, causal, rank, step,
@@ -819,6 +825,7 @@ ra_status ringattn_bwd_rank_step(const void* q, const void* k, const void* v, co
                                  ra_dims dims, int num_shards, int shard_layout, int causal,
                                  int rank, int step, float* dq, float* dk, float* dv,
                                  void* workspace, size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx("ringattn_bwd_rank_step");
   PlanInput in;
   int Tr = 0;
   ra_status st = check_rank_step(cu_seqlens, dims, num_shards, shard_layout, causal, rank, step,
@@ -899,6 +906,7 @@ ra_status ringattn_bwd_rank_step(const void* q, const void* k, const void* v, co
 
 ra_status attn_lse_merge(void* o_a, float* lse_a, const void* o_b, const float* lse_b, int rows,
                          int heads, int head_dim, int dtype, void* stream) {
+  NvtxRange nvtx("attn_lse_merge");
   if (rows < 0 || heads < 1 || head_dim < 8 || head_dim % 8 || 32 % (head_dim / 8))
     return RA_ERR_INVALID_ARG;
   if (dtype != RA_BF16 && dtype != RA_FP32) return RA_ERR_UNSUPPORTED;
@@ -929,6 +937,7 @@ ra_status ssd_cp_fwd(const float* x, const float* dt, const float* A, const floa
                      const float* C, const float* D, const int32_t* position_ids, ssd_dims dims,
                      int num_shards, float* y, float* final_state, void* workspace,
                      size_t workspace_bytes, void* stream) {
+  NvtxRange nvtx("ssd_cp_fwd");
   if (dims.total_tokens < 0 || dims.heads < 1 || dims.groups < 1 || num_shards < 1)
     return RA_ERR_INVALID_ARG;
   if (dims.heads % dims.groups) return RA_ERR_INVALID_ARG;

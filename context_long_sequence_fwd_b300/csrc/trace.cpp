@@ -52,7 +52,8 @@ bool take_pair(int device, cudaEvent_t* s, cudaEvent_t* e) {
 
 bool trace_enabled() { return g_on.load(std::memory_order_relaxed); }
 
-TraceScope::TraceScope(cudaStream_t stream, const char* kernel) : stream_(stream) {
+TraceScope::TraceScope(cudaStream_t stream, const char* kernel)
+    : stream_(stream), nvtx_(kernel) {
   if (!trace_enabled()) return;
   std::lock_guard<std::mutex> lock(g_tmu);
   if (g_records.size() >= kMaxRecords) return;  // silently stop recording

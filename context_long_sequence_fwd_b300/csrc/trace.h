@@ -6,12 +6,25 @@
 // device time.  When tracing is off a launch pays one relaxed atomic load.
 #pragma once
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 namespace ra {
 
 bool trace_enabled();
 
+// An NVTX range over one public call (host-side work and launches), for
+// profilers that read NVTX (ncu --nvtx --nvtx-include); without one attached
+// a push or pop costs a pointer check.
+class NvtxRange {
+ public:
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 // Brackets one kernel launch: construct right before it, destroy right after.
+// The launch also gets an NVTX range named after the kernel.
 class TraceScope {
  public:
   TraceScope(cudaStream_t stream, const char* kernel);
@@ -22,6 +35,7 @@ class TraceScope {
  private:
   cudaStream_t stream_;
   int slot_ = -1;
+  NvtxRange nvtx_;
 };
 
 }  // namespace ra
