@@ -7,10 +7,11 @@ workloads, not a sample:
 * causal MHA, 8192 tokens, 8 heads, 4 zigzag shards: every O and lse;
 * causal GQA, 32768 tokens, 32/8 heads, 8 zigzag shards (the benched step,
   forward then backward with bf16 gradients, exactly as the bench runs it):
-  every row of query heads 0-3 and 28-31 for O, lse and dQ, and every key of
-  key/value heads 0 and 7 for dK and dV (heads are independent, and a key
-  head's gradients need exactly its group's query heads); the same outputs
-  of the stepwise forward and of the multi-GPU ring emulated on this GPU;
+  every O and lse of all 32 query heads; every row of query heads 0-3 and
+  28-31 for dQ, and every key of key/value heads 0 and 7 for dK and dV
+  (heads are independent, and a key head's gradients need exactly its
+  group's query heads); the same outputs of the stepwise forward and of the
+  multi-GPU ring emulated on this GPU;
 * packed documents, 65536 tokens, 8 contiguous shards that split documents:
   every O and lse;
 * causal GQA, 65536 tokens, forward then backward (fp32 gradients): every
@@ -100,6 +101,19 @@ def test_causal_gqa_t32768_p8_zigzag_benched_step_every_row_of_edge_groups(gqa32
     check_edge_groups(ref, kvh, out, lse, dq, dk, dv, grad_bf16=True)
     for t in (out, lse, dq, dk, dv):
         assert bool(torch.isfinite(t).all())
+
+
+def test_causal_gqa_t32768_p8_zigzag_forward_every_head(gqa32k):
+    """The benched shape's forward in full: every O and lse of all 32 query
+    heads (the oracle's forward for the heads the fixture's backward does
+    not cover)."""
+    w, x, kvh, ref = gqa32k
+    _, _, _, out, lse = gpu_forward(w, x)
+    rest = [h for h in range(w.hq) if h not in EDGE_HEADS]
+    ro, rl = oracle.blas.attention_fwd(x["q"], x["k"], x["v"], causal=True, heads=rest)
+    assert max_err(to_np(out[:, rest]), ro[:, rest]) <= TOL_BF16_O
+    assert max_err(to_np(lse[rest]), rl[rest]) <= TOL_BF16_LSE
+    check_edge_groups(ref, kvh, out, lse)
 
 
 def test_causal_gqa_t32768_p8_zigzag_stepwise_every_row_of_edge_groups(gqa32k):
