@@ -10,6 +10,9 @@ Recipe (the same for every workload):
     (when asked) dO, in that order, as fp32 standard normals;
   * each tensor is then cast to the workload's dtype (bf16 rounds to nearest
     even), so the oracle reads exactly the values the GPU reads;
+  * problems too large to draw on the host (billions of values) are drawn the
+    same way by a generator on the device (``make_qkv_device``): the same
+    distribution and order, other values;
   * packed-document lengths come from a second generator seeded ``seed + 1``:
     integers uniform in [lo, hi] inclusive, drawn one at a time until their sum
     reaches the token total, the last one truncated so the sum is exact.
@@ -106,6 +109,23 @@ def make_qkv(total_tokens: int, hq: int, hkv: int, head_dim: int, dtype: str,
         return q, k, v
     do = torch.randn(total_tokens, hq, head_dim, generator=g).to(dt)
     return q, k, v, do
+
+
+def make_qkv_device(total_tokens: int, hq: int, hkv: int, head_dim: int, seed: int,
+                    device, with_dout: bool = False):
+    """bf16 q, k, v (and dO) drawn on `device` by a generator seeded `seed`:
+    fp32 standard normals in the order q, k, v, dO, each rounded to bf16."""
+    g = torch.Generator(device).manual_seed(seed)
+    shapes = [(total_tokens, hq, head_dim), (total_tokens, hkv, head_dim),
+              (total_tokens, hkv, head_dim)] + ([(total_tokens, hq, head_dim)] if with_dout else [])
+    out = []
+    for shp in shapes:
+        t = torch.empty(shp, dtype=torch.bfloat16, device=device)
+        for r0 in range(0, shp[0], 65536):  # fp32 draws a slab at a time
+            r1 = min(shp[0], r0 + 65536)
+            t[r0:r1] = torch.randn((r1 - r0,) + shp[1:], generator=g, device=device)
+        out.append(t)
+    return tuple(out)
 
 
 def make_inputs(w: Workload, seed: int = 0, with_dout: bool | None = None):
