@@ -177,6 +177,22 @@ def position_ids_from_lengths(lengths) -> torch.Tensor:
     return torch.cat([torch.arange(int(n), dtype=torch.int32) for n in lengths])
 
 
+def make_ssd_inputs_device(T, H, P, N, G, seed, device, doc_lo=512, doc_hi=8192):
+    """make_ssd_inputs' recipe (packed samples) drawn by a generator on
+    `device`, for problems too large to draw on the host: the same
+    distributions and order, other values; the sample lengths are the host's."""
+    g = torch.Generator(device).manual_seed(seed)
+    x = torch.randn(T, H, P, generator=g, device=device)
+    lo, hi = torch.log(torch.tensor(1e-3)), torch.log(torch.tensor(1e-1))
+    dt = torch.exp(lo + (hi - lo) * torch.rand(T, H, generator=g, device=device))
+    A = -(1.0 + 15.0 * torch.rand(H, generator=g, device=device))
+    B = torch.randn(T, G, N, generator=g, device=device)
+    C = torch.randn(T, G, N, generator=g, device=device)
+    D = torch.ones(H, device=device)
+    pos = position_ids_from_lengths(doc_lengths(T, doc_lo, doc_hi, seed + 1)).to(device)
+    return {"x": x, "dt": dt, "A": A, "B": B, "C": C, "D": D, "position_ids": pos}
+
+
 def make_ssd_inputs(T, H, P, N, G, seed, packed=True, doc_lo=512, doc_hi=8192):
     """x [T,H,P], dt [T,H], A [H], B, C [T,G,N], D [H] (fp32, CPU) and
     position_ids [T] int32 (None when not packed)."""

@@ -13,6 +13,7 @@ import torch
 import context_long_sequence_fwd_b300 as ra
 import oracle
 from context_long_sequence_fwd_b300.workloads import (SSD_WORKLOADS, make_ssd_inputs,
+                                                      make_ssd_inputs_device,
                                                       position_ids_from_lengths)
 from tests._util import max_err, to_np
 
@@ -122,6 +123,32 @@ def test_mamba2_workload_every_head():
         assert max_err(y[:, h], ry[:, h]) <= REL_TOL * scale, h
         assert max_err(hT[h], rh[h]) <= REL_TOL * max(1.0, float(np.max(np.abs(rh[h])))), h
     assert np.all(np.isfinite(y))
+
+
+def test_mamba2_t1048576_past_int32_offsets():
+    """The 32K workload's shape at 1,048,576 tokens: x and y hold 2^20 x 128 x
+    64 = 8.6e9 values each (byte offsets past 2^34), drawn on the device.
+    Heads 0 and 127 (groups 0 and 7) are checked in full, every y and the
+    final state, against the oracle's scan of each head as its own problem
+    (heads are independent given their group's B and C)."""
+    T, H, P, N, G, R = 1 << 20, 128, 64, 128, 8, 8
+    inp = make_ssd_inputs_device(T, H, P, N, G, seed=4, device=DEV)
+    y, hT = ra.ssd_cp_fwd(inp["x"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["D"],
+                          inp["position_ids"], R, want_final_state=True)
+    torch.cuda.synchronize()
+    assert ra.ringattn_get_status() == 0
+    pos = inp["position_ids"].cpu()
+    for h in (0, H - 1):
+        g = h // (H // G)
+        sub = lambda t: t.contiguous().cpu().double().numpy()
+        ry, rh = oracle.ssd_scan(sub(inp["x"][:, h:h + 1]), sub(inp["dt"][:, h:h + 1]),
+                                 sub(inp["A"][h:h + 1]), sub(inp["B"][:, g:g + 1]),
+                                 sub(inp["C"][:, g:g + 1]), sub(inp["D"][h:h + 1]), pos)
+        ry, rh = np.asarray(ry)[:, 0], np.asarray(rh)[0]
+        scale = max(1.0, float(np.max(np.abs(ry))))
+        assert max_err(to_np(y[:, h]), ry) <= REL_TOL * scale, h
+        assert max_err(to_np(hT[h]), rh) <= REL_TOL * max(1.0, float(np.max(np.abs(rh)))), h
+    assert bool(torch.isfinite(y).all())
 
 
 def test_bad_arguments_are_loud():
