@@ -99,6 +99,8 @@ def library():
         lib.ringattn_fwd_stepwise_workspace_size.restype = ctypes.c_size_t
         lib.ringattn_bwd_workspace_size.argtypes = [ra_dims]
         lib.ringattn_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.ringattn_set_bwd_flush_interval.argtypes = [ctypes.c_int]
+        lib.ringattn_set_bwd_flush_interval.restype = ctypes.c_int
         lib.ringattn_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i32p, ra_dims, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp,
                                      ctypes.c_size_t, _vp]
@@ -254,8 +256,16 @@ def ringattn_fwd_stepwise(q, k, v, cu_seqlens=None, num_shards=1, shard_layout=C
     return out, lse
 
 
-def bwd_workspace_size(q, k, heads_k_stride=1) -> int:
-    return int(library().ringattn_bwd_workspace_size(make_dims(q, k, 0, heads_k_stride)))
+def bwd_workspace_size(q, k, heads_k_stride=1, grad_fp32=False) -> int:
+    return int(library().ringattn_bwd_workspace_size(
+        make_dims(q, k, 0, heads_k_stride, grad_fp32)))
+
+
+def set_bwd_flush_interval(pairs: int) -> None:
+    """(query tile, head) pairs after which the dK/dV kernel moves its
+    tensor-memory sums to fp32 memory and restarts them; 0: never.
+    Process-wide; size backward workspaces after changing it."""
+    _check("ringattn_set_bwd_flush_interval", library().ringattn_set_bwd_flush_interval(int(pairs)))
 
 
 def ringattn_bwd(q, k, v, out, lse, dout, cu_seqlens=None, num_shards=1,
@@ -276,7 +286,7 @@ def ringattn_bwd(q, k, v, out, lse, dout, cu_seqlens=None, num_shards=1,
     _need(dq, "dq", q.shape, gdt)
     _need(dk, "dk", k.shape, gdt)
     _need(dv, "dv", v.shape, gdt)
-    need = bwd_workspace_size(q, k, heads_k_stride)
+    need = bwd_workspace_size(q, k, heads_k_stride, grad_fp32)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
     cu_p, nseq, _keep = _cu_host(cu_seqlens)

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstring>
@@ -433,6 +434,46 @@ size_t fp32_o_bytes(const ra_dims& d) {
   return ((size_t)d.total_tokens * d.hq * d.head_dim * 4 + 255) & ~size_t(255);
 }
 size_t lse_bytes(const ra_dims& d) { return ((size_t)d.hq * d.total_tokens * 4 + 255) & ~size_t(255); }
+size_t kv_f32_bytes(const ra_dims& d) {
+  return ((size_t)d.total_tokens * d.hkv * d.head_dim * 4 + 255) & ~size_t(255);
+}
+
+// (query tile, head) pairs after which the dK/dV kernel moves its TMEM sums
+// to fp32 memory and restarts them (0: never).  The tensor cores' fp32
+// accumulation loses a little toward zero at every step, so bounding the
+// run bounds that loss whatever the sequence length.
+std::atomic<int> g_bwd_flush_pairs{1024};
+
+// Whether some key tile's walk can be longer than `flush` pairs: it visits
+// at most every query tile of every head of its group.
+bool bwd_may_flush(const ra_dims& d, int flush) {
+  if (flush <= 0 || d.hkv < 1 || d.hq % d.hkv) return false;
+  return (long long)((d.total_tokens + 127) / 128) * (d.hq / d.hkv) > flush;
+}
+
+size_t bwd_workspace_bytes(const ra_dims& d, int flush) {
+  size_t n = lse_bytes(d);  // D_i = dO_i . O_i, fp32 [Hq, T]
+  // bf16 gradients whose dK/dV walks can outlast the flush interval: the
+  // fp32 sums of dk and dv
+  if (d.dtype == RA_BF16 && !d.grad_fp32 && bwd_may_flush(d, flush)) n += 2 * kv_f32_bytes(d);
+  return n;
+}
+
+// Where the dK/dV flushes go: fp32 outputs themselves, else the fp32 sums
+// after the D_i vector in the workspace (none: no walk outlasts `flush`).
+void set_bwd_flush(BwdParams* p, const ra_dims& d, void* workspace, int flush) {
+  p->flush_pairs = flush;
+  if (p->grad_fp32) {
+    p->dk_acc = static_cast<float*>(p->dk);
+    p->dv_acc = static_cast<float*>(p->dv);
+  } else if (bwd_may_flush(d, flush)) {
+    char* w = static_cast<char*>(workspace) + lse_bytes(d);
+    p->dk_acc = reinterpret_cast<float*>(w);
+    p->dv_acc = reinterpret_cast<float*>(w + kv_f32_bytes(d));
+  } else {
+    p->flush_pairs = 0;
+  }
+}
 
 }  // namespace
 }  // namespace ra
@@ -660,7 +701,13 @@ extern "C" {
 
 size_t ringattn_bwd_workspace_size(ra_dims dims) {
   if (dims.total_tokens < 0 || dims.hq < 1 || dims.head_dim < 1) return 0;
-  return lse_bytes(dims);  // D_i = dO_i . O_i, fp32 [Hq, T]
+  return bwd_workspace_bytes(dims, g_bwd_flush_pairs.load());
+}
+
+ra_status ringattn_set_bwd_flush_interval(int pairs) {
+  if (pairs < 0) return RA_ERR_INVALID_ARG;
+  g_bwd_flush_pairs.store(pairs);
+  return RA_OK;
 }
 
 ra_status ringattn_bwd(const void* q, const void* k, const void* v, const void* out,
@@ -676,7 +723,8 @@ ra_status ringattn_bwd(const void* q, const void* k, const void* v, const void* 
   for (const void* t : {q, k, v, out, dout, static_cast<const void*>(dq), static_cast<const void*>(dk),
                         static_cast<const void*>(dv)})
     if (!aligned16(t)) return RA_ERR_INVALID_ARG;
-  if (!workspace || workspace_bytes < ringattn_bwd_workspace_size(dims) || !aligned16(workspace))
+  const int flush = g_bwd_flush_pairs.load();  // one reading for the size check and the launch
+  if (!workspace || workspace_bytes < bwd_workspace_bytes(dims, flush) || !aligned16(workspace))
     return RA_ERR_WORKSPACE;
   std::lock_guard<std::mutex> lock(g_mu);
   int dev;
@@ -733,6 +781,7 @@ ra_status ringattn_bwd(const void* q, const void* k, const void* v, const void* 
   p.num_bsegs = static_cast<int>(cp->bwd.segs.size());
   p.q_rows = dims.total_tokens;
   p.k_rows = dims.total_tokens;
+  set_bwd_flush(&p, dims, workspace, flush);
   cudaError_t e = f32 ? launch_bwd_simt_fp32(p, s)
                       : launch_bwd_tc_bf16(p, maps.q, maps.k, maps.v, map_do, s);
   if (e != cudaSuccess) return RA_ERR_CUDA;
@@ -899,6 +948,7 @@ ra_status ringattn_bwd_rank_step(const void* q, const void* k, const void* v, co
   // step 0 starts dq (this rank's rows) and dk, dv (its own keys, which
   // then travel the ring); later steps add to them
   p.accumulate = step == 0 ? 0 : 1;
+  set_bwd_flush(&p, dims, nullptr, g_bwd_flush_pairs.load());  // fp32 outputs take the flushes
   if (launch_bwd_tc_bf16(p, maps.q, maps.k, maps.v, map_do, s) != cudaSuccess) return RA_ERR_CUDA;
   if (cudaEventRecord(cp->last_use, s) != cudaSuccess) return RA_ERR_CUDA;
   return RA_OK;

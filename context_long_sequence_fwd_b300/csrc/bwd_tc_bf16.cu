@@ -23,6 +23,10 @@
 //     TMEM: S^T_a 0-63, dP^T_a 64-127, S^T_b 128-191, dP^T_b 192-255,
 //     dV 256-383, dK 384-511; P^T and dS^T (bf16, two per column) overwrite
 //     the first 32 columns of their S^T / dP^T block.
+//     The tensor cores' fp32 accumulation loses a little toward zero at
+//     every step, so a long walk moves dV and dK to fp32 memory every
+//     flush_pairs (query tile, head) pairs and restarts them; the epilogue
+//     adds the flushed sums.
 //
 //   bwd_dq_kernel  one CTA per 128-row query tile (the forward plan's tiles),
 //     walking its key ranges in ring order, one 128-key tile at a time:
@@ -138,6 +142,27 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t
                       pack_bf16x2(__uint_as_float(u[8 * i + 6]) * mul, __uint_as_float(u[8 * i + 7]) * mul));
 }
 
+// Stores acc + 32 fp32 values (times `mul`) as bf16 at dst; acc holds the
+// earlier partial sums of the same 32 outputs (fp32, 16-byte aligned).
+__device__ __forceinline__ void store_bf16x32_plus(__nv_bfloat16* dst, const float* acc,
+                                                   const uint32_t (&u)[32], float mul) {
+  const float4* a = reinterpret_cast<const float4*>(acc);
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 t = a[i];
+    v[4 * i] = t.x + __uint_as_float(u[4 * i]) * mul;
+    v[4 * i + 1] = t.y + __uint_as_float(u[4 * i + 1]) * mul;
+    v[4 * i + 2] = t.z + __uint_as_float(u[4 * i + 2]) * mul;
+    v[4 * i + 3] = t.w + __uint_as_float(u[4 * i + 3]) * mul;
+  }
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    d[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                      pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+}
+
 // Elementwise core of the backward for 32 score columns of one TMEM row:
 //   P = 2^(S scale log2(e) - lse log2(e)),  dS = P (dP - D),
 // two columns per paired fp32 instruction, with the columns the mask hides
@@ -219,7 +244,8 @@ struct CtlKV {
   uint64_t stage_empty[kMaxKvStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
-  uint64_t acc_full;
+  uint64_t acc_full;   // dV, dK complete: at each flush and at the end
+  uint64_t acc_empty;  // a flush has read dV, dK out of TMEM
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -266,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->p_full[x], 128);
     }
     mbar_init(&ctl->acc_full, 1);
+    mbar_init(&ctl->acc_empty, 256);
     mbar_init(&ctl->mma_done, 1);
     ctl->abort = 0;
     fence_barrier_init();
@@ -415,11 +442,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_s(0, 0);
         issue_s(0, 1);
       }
+      int flushes = 0;  // dV, dK handed to the flush so far
       for (int j = 0; j < n && ok; ++j) {
         const bool more = j + 1 < n;
+        // the first pair after a flush starts dV, dK afresh once the flush
+        // has read them
+        const bool fresh = j > 0 && p.flush_pairs > 0 && j % p.flush_pairs == 0;
         if (!(ok = mbar_wait(&ctl->p_full[0], j & 1, p.status, abort))) break;
+        if (fresh && !(ok = mbar_wait(&ctl->acc_empty, (flushes - 1) & 1, p.status, abort))) break;
         tc_fence_after_sync();
-        issue_acc(j, 0, j > 0);
+        issue_acc(j, 0, j > 0 && !fresh);
         if (more) {
           if (!(ok = q_ready(j + 1))) break;
           tc_fence_after_sync();
@@ -429,6 +461,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         issue_acc(j, 1, true);
         mma_commit(&ctl->stage_empty[j % kKvStages]);
+        if (more && p.flush_pairs > 0 && (j + 1) % p.flush_pairs == 0) {
+          mma_commit(&ctl->acc_full);
+          ++flushes;
+        }
         if (more) issue_s(j + 1, 1);
       }
       if (ok) mma_commit(&ctl->acc_full);
@@ -446,6 +482,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + x * 128;
     const uint32_t tdP = tS + 64;
     const float sl2 = p.scale_log2;
+    // half 0 writes dV, half 1 writes dK (times the softmax scale), at the
+    // flushes and at the end
+    const uint32_t tAcc = tmem + lane_off + (x == 0 ? 256 : 384);
+    const int jl = local_row(p.kmap, j);
+    const bool store = kr < it.klen && index_ok(jl, p.k_rows, p.status, kSiteBwdDkDv) &&
+                       index_ok(g, p.hkv, p.status, kSiteHead);
+    const size_t off = ((size_t)jl * p.hkv + g) * kD;
+    void* dst = x == 0 ? p.dv : p.dk;
+    float* acc = (x == 0 ? p.dv_acc : p.dk_acc) + off;  // fp32 partial sums of the flushes
+    const float mul = x == 0 ? 1.f : p.scale;
+    int flushes = 0;
     bool ok = true;
     for (int jj = 0; jj < n; ++jj) {
       const int slot = jj % kKvStages;
@@ -475,18 +522,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_store_wait();
       tc_fence_before_sync();
       mbar_arrive(&ctl->p_full[x]);
+      // flush: after every flush_pairs pairs (the last pair excepted) dV and
+      // dK leave TMEM for fp32 memory, and the MMAs start them afresh, so
+      // that no accumulation in TMEM runs longer than flush_pairs pairs
+      if (p.flush_pairs > 0 && jj + 1 < n && (jj + 1) % p.flush_pairs == 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->acc_full, flushes & 1, p.status, abort));
+        if (!ok) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < kD / 32; ++c) {
+          uint32_t u[32];
+          tmem_load_32(tAcc + c * 32, u);
+          if (store) {
+            if (flushes == 0 && !p.accumulate)
+              store_f32x32(acc + c * 32, u, mul);
+            else
+              add_f32x32(acc + c * 32, u, mul);
+          }
+        }
+        tc_fence_before_sync();
+        mbar_arrive(&ctl->acc_empty);
+        ++flushes;
+      }
     }
     if (!ok) *abort = 1;
-    if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->acc_full, 0, p.status, abort));
+    if (ok && n > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->acc_full, flushes & 1, p.status, abort));
     tc_fence_after_sync();
-    // epilogue: half 0 writes dV, half 1 writes dK (times the softmax scale)
-    const uint32_t tAcc = tmem + lane_off + (x == 0 ? 256 : 384);
-    const int jl = local_row(p.kmap, j);
-    const bool store = kr < it.klen && index_ok(jl, p.k_rows, p.status, kSiteBwdDkDv) &&
-                       index_ok(g, p.hkv, p.status, kSiteHead);
-    const size_t off = ((size_t)jl * p.hkv + g) * kD;
-    void* dst = x == 0 ? p.dv : p.dk;
-    const float mul = x == 0 ? 1.f : p.scale;
+    // epilogue: TMEM plus the flushed partial sums
 #pragma unroll
     for (int c = 0; c < kD / 32; ++c) {
       uint32_t u[32];
@@ -497,7 +560,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 32; ++i) u[i] = 0u;
       }
       if (ok && store) {
-        if (p.accumulate)
+        if (flushes > 0 && !p.accumulate && !p.grad_fp32)
+          store_bf16x32_plus(static_cast<__nv_bfloat16*>(dst) + off + c * 32, acc + c * 32, u,
+                             mul);
+        else if (p.accumulate || flushes > 0)
           add_f32x32(static_cast<float*>(dst) + off + c * 32, u, mul);
         else if (p.grad_fp32)
           store_f32x32(static_cast<float*>(dst) + off + c * 32, u, mul);

@@ -127,6 +127,12 @@ struct BwdParams {
   RowMap kmap;              // rows of k, v, dk and dv
   int lse_stride;           // rows per head of lse and Dvec
   int accumulate;           // 1: add into fp32 dq, dk, dv instead of writing them
+  // dK/dV: every flush_pairs (query tile, head) pairs of a key tile's walk
+  // (0: never) the TMEM sums are added to fp32 dk_acc, dv_acc [rows, Hkv, D]
+  // (dk, dv themselves when they are fp32) and restarted
+  int flush_pairs;
+  float* dk_acc;
+  float* dv_acc;
   // extents for the debug build's checks
   int num_segs, num_bsegs;  // entries of segs and bsegs
   int q_rows, k_rows;       // rows of the q-side buffers and of the k-side buffers

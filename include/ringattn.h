@@ -167,12 +167,32 @@ ra_status ringattn_fwd_stepwise_noalloc(const void* q, const void* k, const void
  *   dv_j = sum_i P_ij dout_i,  dS_ij = P_ij (dout_i . v_j - D_i),
  *   dq_i = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i.
  * Needs a caller-owned device workspace of ringattn_bwd_workspace_size(dims)
- * bytes (the fp32 D_i vector, [Hq, T]).  dq accumulates in tensor memory
- * over each query tile's whole ring, and dk, dv over each key tile's, so no
- * output is accumulated with atomics and the result does not depend on the
- * schedule.  bf16 runs on the tensor cores, fp32 on CUDA cores.
+ * bytes: the fp32 D_i vector [Hq, T], and for bf16 gradients of long
+ * sequences the fp32 sums of dk and dv (2 x [T, Hkv, D], see below).  dq
+ * accumulates in tensor memory over each query tile's whole ring, and dk,
+ * dv over each key tile's, so no output is accumulated with atomics and the
+ * result does not depend on the schedule.  bf16 runs on the tensor cores,
+ * fp32 on CUDA cores.
+ *
+ * The tensor cores' fp32 accumulation loses a little toward zero at every
+ * step (measured on B300: about 2^-26 of the sum per K = 16 step); a key
+ * tile's walk is up to T G / 16 such steps for G query heads per key/value
+ * head, which shrank dk and dv by about 2e-9 T at G = 4.  So the dk/dv
+ * kernel moves its sums to fp32 memory and restarts them every
+ * ringattn_set_bwd_flush_interval() (query tile, head) pairs (default 1024:
+ * only walks of more than 1024 = (T / 128) G pairs flush, e.g. above 32K
+ * tokens at G = 4): into dk, dv when they are fp32, else into the
+ * workspace's fp32 sums, which the last step adds before rounding to bf16.
  */
 size_t ringattn_bwd_workspace_size(ra_dims dims);
+
+/*
+ * Sets the dk/dv flush interval above, in (query tile, head) pairs; 0 turns
+ * the flushes off.  Process-wide; it changes ringattn_bwd_workspace_size()'s
+ * answer, so set it before sizing a workspace and not while a backward call
+ * is being made on another thread.  RA_ERR_INVALID_ARG for pairs < 0.
+ */
+ra_status ringattn_set_bwd_flush_interval(int pairs);
 ra_status ringattn_bwd(const void* q, const void* k, const void* v, const void* out,
                        const float* lse, const void* dout, const int32_t* cu_seqlens,
                        ra_dims dims, int num_shards, int shard_layout, int causal, void* dq,

@@ -107,6 +107,30 @@ def test_workspace_sizes(lib):
     assert lib.ringattn_bwd_workspace_size(d) >= 4 * 1024 * 4   # the D_i vector
 
 
+def test_bwd_flush_interval_sizes_the_workspace(lib):
+    """bf16 gradients whose key-tile walks (T / 128 query tiles x G heads)
+    outlast the dK/dV flush interval need fp32 sums of dk and dv in the
+    workspace; fp32 gradients take the flushes themselves."""
+    d_vec = lambda T, hq: (hq * T * 4 + 255) // 256 * 256
+    sums = lambda T, hkv: 2 * ((T * hkv * 128 * 4 + 255) // 256 * 256)
+    try:
+        assert lib.ringattn_set_bwd_flush_interval(-1) == -1
+        assert lib.ringattn_set_bwd_flush_interval(1024) == 0
+        # 256 query tiles x 4 heads = 1024 pairs: no flush at 32K tokens
+        assert lib.ringattn_bwd_workspace_size(dims(T=32768, hq=32, hkv=8)) == d_vec(32768, 32)
+        big = dims(T=65536, hq=32, hkv=8)
+        assert lib.ringattn_bwd_workspace_size(big) == d_vec(65536, 32) + sums(65536, 8)
+        big.grad_fp32 = 1
+        assert lib.ringattn_bwd_workspace_size(big) == d_vec(65536, 32)
+        assert lib.ringattn_set_bwd_flush_interval(0) == 0  # off
+        assert lib.ringattn_bwd_workspace_size(dims(T=65536, hq=32, hkv=8)) == d_vec(65536, 32)
+        assert lib.ringattn_set_bwd_flush_interval(4) == 0
+        assert lib.ringattn_bwd_workspace_size(dims(T=1024, hq=4, hkv=2)) == \
+            d_vec(1024, 4) + sums(1024, 2)
+    finally:
+        lib.ringattn_set_bwd_flush_interval(1024)
+
+
 def test_trace_without_launches(lib):
     """Tracing is host bookkeeping: enabling it and collecting an empty record
     needs no GPU."""

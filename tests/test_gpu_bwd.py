@@ -166,3 +166,54 @@ def test_ulysses_backward(case):
     q, k, v, do = make_qkv(T, hq, hkv, 128, "bf16", seed=32, with_dout=True)
     check_full(q, k, v, do, cu, P, ra.CONTIGUOUS, True, TOL_BF16_GRAD, hks=hkv // P,
                grad_fp32=True, exchange=ra.ALLGATHER)
+
+
+@pytest.fixture
+def flush_every():
+    """Sets the dK/dV flush interval for one test and restores the default."""
+    def set_(pairs):
+        ra.set_bwd_flush_interval(pairs)
+    yield set_
+    ra.set_bwd_flush_interval(1024)
+
+
+FLUSH_CASES = [
+    # T, hq, hkv, d, P, layout, causal, cu, flush interval in (query tile, head) pairs
+    (2048, 4, 2, 128, 4, ra.ZIGZAG, True, None, 1),        # a flush after every pair
+    (2048, 4, 1, 128, 2, ra.CONTIGUOUS, True, None, 3),    # group of 4, interval not a multiple
+    (1920, 8, 2, 64, 4, ra.ZIGZAG, True, [0, 700, 701, 1920], 2),   # D = 64, packed documents
+    (1024, 2, 2, 128, 2, ra.CONTIGUOUS, False, None, 5),   # non-causal
+]
+
+
+@pytest.mark.parametrize("grad_fp32", [True, False], ids=["fp32grad", "bf16grad"])
+@pytest.mark.parametrize("case", FLUSH_CASES, ids=[str(i) for i in range(len(FLUSH_CASES))])
+def test_dkdv_flushes_keep_the_result(case, grad_fp32, flush_every):
+    """The dK/dV kernel's flushes (TMEM sums moved to fp32 memory every few
+    pairs and restarted: into fp32 gradients directly, or into the
+    workspace's fp32 sums for bf16 ones) against the oracle, with intervals
+    short enough that every key tile flushes many times."""
+    T, hq, hkv, d, P, layout, causal, cu, every = case
+    flush_every(every)
+    q, k, v, do = make_qkv(T, hq, hkv, d, "bf16", seed=41, with_dout=True)
+    if not grad_fp32:
+        qd, kd = q.to(DEV), k.to(DEV)
+        assert ra.bwd_workspace_size(qd, kd) > ra.bwd_workspace_size(qd, kd, grad_fp32=True)
+    check_full(q, k, v, do, cu, P, layout, causal, TOL_BF16_GRAD, grad_fp32=grad_fp32)
+
+
+def test_dkdv_flushes_in_the_ring_steps(flush_every):
+    """The multi-GPU ring's per-step backward adds each step into fp32
+    gradients; with flushes the partial sums go there too."""
+    from context_long_sequence_fwd_b300.ring import emulate_ring_bwd
+    flush_every(2)
+    T, hq, hkv, P = 2048, 4, 2, 4
+    q, k, v, do = make_qkv(T, hq, hkv, 128, "bf16", seed=43, with_dout=True)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    out, lse = ra.ringattn_fwd(qd, kd, vd, None, P, ra.ZIGZAG, True)
+    dq, dk, dv = emulate_ring_bwd(qd, kd, vd, out, lse, dod, num_shards=P, layout=ra.ZIGZAG,
+                                  causal=True)
+    assert ra.ringattn_get_status() == 0
+    rq, rk, rv, _, _ = oracle.attention_bwd(q, k, v, do, causal=True)
+    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
+        assert max_err(to_np(got), ref) <= TOL_BF16_GRAD

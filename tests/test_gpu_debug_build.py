@@ -6,7 +6,8 @@ of the first failure and skips the access instead of trapping.  It stands in
 for a memory checker: the edge cases below (ragged tiles, zigzag chunks
 shorter than a tile, packed and empty documents, GQA groups, head dimension
 64, the fp32 path, split forward items, the stepwise and multi-GPU ring
-forms, the backward with bf16 and fp32 gradients) must run with a clean
+forms, the backward with bf16 and fp32 gradients, with and without dK/dV
+flushes) must run with a clean
 status word, no recorded failure, and results that still match the oracle.
 The cases run in a child process that sets RINGATTN_DEBUG=1, which makes the
 binding load the debug library.
@@ -57,6 +58,8 @@ CASES = [  # T, hq, hkv, d, P, layout, causal, cu
     (1024, 4, 4, 64, 2, ra.ZIGZAG, True, [0, 100, 100, 700, 1024]),
 ]
 for i, (T, hq, hkv, d, P, lay, causal, cu) in enumerate(CASES):
+    # every other case moves dK, dV out of TMEM every 3 pairs (flushes)
+    ra.set_bwd_flush_interval(3 if i % 2 else 1024)
     q, k, v, do = make_qkv(T, hq, hkv, d, "bf16", seed=50 + i, with_dout=True)
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
     ro, rl = oracle.attention_fwd(q, k, v, causal=causal, cu_seqlens=cu)
