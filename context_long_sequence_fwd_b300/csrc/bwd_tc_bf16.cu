@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        index_ok(g, p.hkv, p.status, kSiteHead);
     const size_t off = ((size_t)jl * p.hkv + g) * kD;
     void* dst = x == 0 ? p.dv : p.dk;
-    float* acc = (x == 0 ? p.dv_acc : p.dk_acc) + off;  // fp32 partial sums of the flushes
+    float* const acc_base = x == 0 ? p.dv_acc : p.dk_acc;  // fp32 sums of the flushes, or null
     const float mul = x == 0 ? 1.f : p.scale;
     int flushes = 0;
     bool ok = true;
@@ -535,9 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_load_32(tAcc + c * 32, u);
           if (store) {
             if (flushes == 0 && !p.accumulate)
-              store_f32x32(acc + c * 32, u, mul);
+              store_f32x32(acc_base + off + c * 32, u, mul);
             else
-              add_f32x32(acc + c * 32, u, mul);
+              add_f32x32(acc_base + off + c * 32, u, mul);
           }
         }
         tc_fence_before_sync();
@@ -561,8 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok && store) {
         if (flushes > 0 && !p.accumulate && !p.grad_fp32)
-          store_bf16x32_plus(static_cast<__nv_bfloat16*>(dst) + off + c * 32, acc + c * 32, u,
-                             mul);
+          store_bf16x32_plus(static_cast<__nv_bfloat16*>(dst) + off + c * 32,
+                             acc_base + off + c * 32, u, mul);
         else if (p.accumulate || flushes > 0)
           add_f32x32(static_cast<float*>(dst) + off + c * 32, u, mul);
         else if (p.grad_fp32)
