@@ -345,3 +345,26 @@ def test_fused_list_of_a_big_problem_keeps_pass_order():
     fi, _ = ra.plan_fwd_fused(32768, 32, 8, 8, ra.ZIGZAG, True, 148)
     assert len(fi) == len(items) and np.all(fi[:, 15] == -1)
     assert np.all(np.diff(fi[:, 14]) >= 0)
+
+
+def test_plans_past_2_31_elements_cover_the_causal_mask():
+    """786432 tokens, 32 / 8 heads, 8 zigzag shards (q holds 3.2e9 values):
+    every forward item's key segments tile [0, end of its rows) exactly once,
+    and every backward key tile's query segments tile [its first key, T)
+    exactly once, so the plans stay exact where the tensors pass 2^31
+    elements."""
+    T, hq, hkv, P = 786432, 32, 8, 8
+    items, segs = ra.plan_fwd(T, hq, hkv, P, ra.ZIGZAG, True)
+    assert len(items) == (T // TILE) * hq // 2
+    for it in items:
+        s = segs[it[6]:it[6] + it[7]]
+        s = s[np.argsort(s[:, 0])]
+        end = max(it[0] + it[2], it[1] + it[3])
+        assert s[0, 0] == 0 and s[-1, 1] == end and np.all(s[1:, 0] == s[:-1, 1])
+    bitems, bsegs = ra.plan_bwd(T, hq, hkv, P, ra.ZIGZAG, True)
+    assert len(bitems) == (T // TILE) * hkv
+    for k0, klen, g, src, sb, sc, cost, _ in bitems:
+        s = bsegs[sb:sb + sc]
+        s = s[np.argsort(s[:, 0])]
+        assert s[0, 0] == k0 and s[-1, 1] == T and np.all(s[1:, 0] == s[:-1, 1])
+        assert cost == (T - k0) // TILE * (hq // hkv)
