@@ -16,7 +16,10 @@ the 126 MB L2, so no flush is needed between steps.  N > 1 GPUs run
 independent replicas (one process per GPU, launched by torchrun); the value
 is the sum over ranks of the work divided by the slowest rank's time.
 
-Prints one JSON line (rank 0).
+Prints one JSON line (rank 0).  With ``--results FILE`` the line is also
+appended to FILE, and a configuration already recorded there is printed from
+it instead of being run again, so a sweep over workloads that was cut short
+resumes where it stopped.
 """
 from __future__ import annotations
 
@@ -612,7 +615,7 @@ def run_ours(args):
         bt = 2.5 * f_fwd / (bm * 1e-3) / 1e12
         line["bwd"] = {"ms": round(bm, 4), "tflops": round(bt, 2), "frac": round(bt / peak, 4),
                        "frac_of_sustained": round(bt / peak_s, 4)}
-    print(json.dumps(line), flush=True)
+    emit(line)
 
 
 # --------------------------------------------- Mamba2 selective scan (CP)
@@ -793,7 +796,7 @@ def run_ssd(args):
         "clocks": clk,
         "status": ra.STATUS.get(status, status),
     }
-    print(json.dumps(line), flush=True)
+    emit(line)
 
 
 # ------------------------------------------------------------- reference
@@ -840,7 +843,51 @@ def run_reference(args):
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+    emit(line)
+
+
+# --results FILE: each finished run appends {"run_key": ..., "line": ...} to FILE,
+# and a run whose key is already there prints the stored line instead of
+# running again, so an interrupted sweep of configurations resumes where it
+# stopped (the op keeps no state of its own to checkpoint).
+_RESULTS = {"path": None, "key": None}
+
+
+def run_key(args) -> dict:
+    return {"impl": args.impl, "workload": args.workload, "pass": args.pass_,
+            "schedule": args.schedule, "gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "seed": args.seed}
+
+
+def stored_line(path, key):
+    if not path or not os.path.exists(path):
+        return None
+    found = None
+    with open(path) as f:
+        for raw in f:
+            try:
+                rec = json.loads(raw)
+            except ValueError:
+                continue  # a line cut short by an interrupted run
+            if isinstance(rec, dict) and rec.get("run_key") == key:
+                found = rec.get("line")
+    return found
+
+
+def emit(line):
+    """Prints the run's JSON line (and records it with --results)."""
     print(json.dumps(line), flush=True)
+    if _RESULTS["path"]:
+        path = _RESULTS["path"]
+        # a line cut short by an interrupted run stays on a line of its own
+        cut = os.path.exists(path) and os.path.getsize(path) > 0
+        if cut:
+            with open(path, "rb") as f:
+                f.seek(-1, os.SEEK_END)
+                cut = f.read(1) != b"\n"
+        with open(path, "a") as f:
+            f.write(("\n" if cut else "") + json.dumps({"run_key": _RESULTS["key"], "line": line})
+                    + "\n")
 
 
 def main():
@@ -860,9 +907,22 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--results", default=None,
+                    help="append each finished run to this file; a run already recorded "
+                         "there prints its stored line and does not run again")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.results:
+        key = run_key(args)
+        done = stored_line(args.results, key)
+        if done is not None:
+            if int(os.environ.get("RANK", "0")) == 0:
+                print(json.dumps(done), flush=True)
+            return
+        # only rank 0 prints, so only rank 0 records
+        if int(os.environ.get("RANK", "0")) == 0:
+            _RESULTS.update(path=args.results, key=key)
     sys.path.insert(0, ROOT)
     from context_long_sequence_fwd_b300.workloads import SSD_WORKLOADS
     if args.workload in SSD_WORKLOADS:

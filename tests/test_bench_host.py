@@ -121,3 +121,31 @@ def test_committed_profiles_parse():
             text = open(os.path.join(root, "profiles", name)).read()
             assert "- kernel_source_sha256_16: `" in text, name
             assert "- dram_bytes_per_launch: `" in text, name
+
+
+def test_results_file_resumes_a_sweep(tmp_path):
+    """--results: a run whose configuration is already recorded prints the
+    stored line and does not run (so no GPU is needed here); a different
+    configuration is not taken for it, and a line cut short by an
+    interrupted run is skipped."""
+    res = tmp_path / "runs.jsonl"
+    args = ["--steps", "2", "--warmup", "3", "--no-cpu-baseline", "--pass", "fwd"]
+    key = {"impl": "ours", "workload": bench.DEFAULT_WORKLOAD, "pass": "fwd",
+           "schedule": "fused", "gpus": 1, "steps": 2, "warmup": 3, "seed": 0}
+    other = dict(key, steps=5)
+    with open(res, "w") as f:
+        f.write(json.dumps({"run_key": other, "line": {"value": 1.0}}) + "\n")
+        f.write(json.dumps({"run_key": key, "line": {"value": 2.0, "metric": "m"}}) + "\n")
+        f.write('{"run_key": {"impl": "ours", "workl')  # interrupted
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--results", str(res),
+                        *args], capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert json.loads(r.stdout.strip().splitlines()[-1]) == {"value": 2.0, "metric": "m"}
+    assert bench.stored_line(str(res), dict(key, seed=1)) is None
+    # a record appended after the cut line stays readable
+    bench._RESULTS.update(path=str(res), key=dict(key, seed=1))
+    try:
+        bench.emit({"value": 3.0})
+    finally:
+        bench._RESULTS.update(path=None, key=None)
+    assert bench.stored_line(str(res), dict(key, seed=1)) == {"value": 3.0}
