@@ -228,9 +228,11 @@ def max_over_ranks(x: float, world: int) -> float:
 
 # ------------------------------------------------------------- CPU oracle
 
-def oracle_sample(w, inputs, budget_s: float, seed: int, backward: bool):
+def oracle_sample(w, inputs, budget_s: float, seed: int, backward: bool, last=None):
     """Times the fp64 oracle on a bounded sample of the workload and returns
-    (flops, seconds, description, threads).
+    (flops, seconds, description, threads).  When `last` is a dict, the rows
+    and results of the final (timed) call of each kind are left in it, for
+    sample_errors.
 
     The sample is random (head, row) outputs: forward rows (O, lse), and for a
     fwd+bwd pass as many backward rows (dQ, with the row's lse and D).  Each
@@ -263,16 +265,22 @@ def oracle_sample(w, inputs, budget_s: float, seed: int, backward: bool):
     def run_fwd(n):
         hs, is_, vis = pick(n)
         t0 = time.perf_counter()
-        oracle.fwd_rows(inputs["q64"], inputs["k64"], inputs["v64"], hs, is_,
-                        causal=w.causal, cu_seqlens=cu)
-        return 4.0 * w.head_dim * vis, time.perf_counter() - t0
+        res = oracle.fwd_rows(inputs["q64"], inputs["k64"], inputs["v64"], hs, is_,
+                              causal=w.causal, cu_seqlens=cu)
+        t = time.perf_counter() - t0
+        if last is not None:
+            last["fwd"] = (hs, is_, res)
+        return 4.0 * w.head_dim * vis, t
 
     def run_bwd(n):
         hs, is_, vis = pick(n)
         t0 = time.perf_counter()
-        oracle.bwd_rows(inputs["q64"], inputs["k64"], inputs["v64"], inputs["dout64"], hs, is_,
-                        causal=w.causal, cu_seqlens=cu)
-        return 6.0 * w.head_dim * vis, time.perf_counter() - t0
+        res = oracle.bwd_rows(inputs["q64"], inputs["k64"], inputs["v64"], inputs["dout64"],
+                              hs, is_, causal=w.causal, cu_seqlens=cu)
+        t = time.perf_counter() - t0
+        if last is not None:
+            last["bwd"] = (hs, is_, res)
+        return 6.0 * w.head_dim * vis, t
 
     parts = [("forward rows", run_fwd)] + ([("dQ rows", run_bwd)] if backward else [])
     flops, secs, desc = 0.0, 0.0, []
@@ -285,6 +293,36 @@ def oracle_sample(w, inputs, budget_s: float, seed: int, backward: bool):
         secs += t1
         desc.append(f"{n} {name}")
     return flops, secs, ", ".join(desc), oracle.num_threads()
+
+
+def sample_errors(last, out, lse, dq=None):
+    """Largest absolute differences between the step's outputs (torch tensors
+    [T, Hq, D] and [Hq, T]) and the oracle's on the rows oracle_sample left in
+    `last`: the bench line's own parity check, with the bounds the tests use
+    (bf16 gradients: 2e-2 plus half a bf16 ulp of the exact value)."""
+    import torch
+    errs = {}
+    if "fwd" in last:
+        hs, is_, (ro, rl) = last["fwd"]
+        h, i = torch.from_numpy(hs).long(), torch.from_numpy(is_).long()
+        o = out.detach()[i.to(out.device), h.to(out.device)].double().cpu().numpy()
+        l = lse.detach()[h.to(lse.device), i.to(lse.device)].double().cpu().numpy()
+        errs["rows"] = int(hs.size)
+        errs["o"] = float(np.max(np.abs(o - ro))) if hs.size else 0.0
+        errs["lse"] = float(np.max(np.abs(l - rl))) if hs.size else 0.0
+        errs["within_bounds"] = errs["o"] <= 2e-2 and errs["lse"] <= 1e-3
+    if "bwd" in last and dq is not None:
+        hs, is_, (rq, _, _) = last["bwd"]
+        h, i = torch.from_numpy(hs).long(), torch.from_numpy(is_).long()
+        g = dq.detach()[i.to(dq.device), h.to(dq.device)].double().cpu().numpy()
+        errs["dq_rows"] = int(hs.size)
+        errs["dq"] = float(np.max(np.abs(g - rq))) if hs.size else 0.0
+        a = np.abs(rq)
+        half_ulp = np.where(a > 0, 2.0 ** (np.floor(np.log2(np.where(a > 0, a, 1.0))) - 8), 0.0)
+        bound = 2e-2 + (half_ulp if dq.dtype != torch.float32 else 0.0)
+        errs["within_bounds"] = bool(errs.get("within_bounds", True) and
+                                     np.all(np.abs(g - rq) <= bound))
+    return errs
 
 
 # ----------------------------------------------------------------- ours
@@ -543,11 +581,16 @@ def run_ours(args):
     status = status or ra.ringattn_get_status()
 
     cpu = None
+    parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        f, t, desc, thr = oracle_sample(w, x, args.cpu_budget, args.seed, backward)
+        last = {}
+        f, t, desc, thr = oracle_sample(w, x, args.cpu_budget, args.seed, backward, last)
         cpu = {"value": round(f / t / 1e12, 6), "unit": "TFLOP/s", "cores": thr,
                "kind": "oracle",
                "sample": f"{desc} of the workload (random head and row), fp64, {t:.1f} s"}
+        # the same rows of this run's outputs (after the timed region)
+        parity = sample_errors(last, main_set["out"], main_set["lse"],
+                               main_set["dq"] if backward else None)
 
     if rank != 0:
         return
@@ -592,6 +635,7 @@ def run_ours(args):
         "roofline": roof,
         "kernels": ktab,
         "cpu_baseline": cpu,
+        "parity_sample": parity,
         "e2e": {"value": round(world * f_step / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_ms, 4),

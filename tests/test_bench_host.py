@@ -149,3 +149,28 @@ def test_results_file_resumes_a_sweep(tmp_path):
     finally:
         bench._RESULTS.update(path=None, key=None)
     assert bench.stored_line(str(res), dict(key, seed=1)) == {"value": 3.0}
+
+
+def test_parity_sample_of_the_bench_line():
+    """The bench line's parity sample: the oracle rows the CPU-baseline leg
+    computed, compared with the step's outputs at the same (head, row)."""
+    import numpy as np
+    import torch
+    from context_long_sequence_fwd_b300.workloads import make_inputs
+    import oracle
+    w = WORKLOADS["tiny_fp32_noncausal_t256"]
+    x = make_inputs(w, seed=0, with_dout=True)
+    last = {}
+    bench.oracle_sample(w, x, 0.05, 0, True, last)
+    assert set(last) == {"fwd", "bwd"}
+    ro, rl = oracle.attention_fwd(x["q"], x["k"], x["v"], causal=w.causal)
+    rq, _, _, _, _ = oracle.attention_bwd(x["q"], x["k"], x["v"], x["dout"], causal=w.causal)
+    out, lse = torch.from_numpy(ro).float(), torch.from_numpy(rl).float()
+    dq = torch.from_numpy(rq).to(torch.bfloat16)
+    e = bench.sample_errors(last, out, lse, dq)
+    assert e["within_bounds"] and e["o"] < 1e-6 and e["lse"] < 1e-5 and e["dq"] < 1e-2
+    hs, is_, _ = last["fwd"]
+    out[int(is_[0]), int(hs[0]), 0] += 0.5   # a planted error in one sampled output
+    e = bench.sample_errors(last, out, lse, dq)
+    assert not e["within_bounds"] and abs(e["o"] - 0.5) < 1e-3
+    assert np.isfinite(e["dq"])
