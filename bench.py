@@ -651,6 +651,7 @@ def run_ours(args):
                         "peak_gbs": float(peaks["hbm_gbs"]),
                         "peak_source": peaks["source"] + " hbm_gbs (copy)"},
         "clocks": clk,
+        "device": torch.cuda.get_device_name(dev),
         "peak_mem_gb": round(peak_mem / 1e9, 3),
         "status": ra.STATUS.get(status, status),
     }
@@ -838,6 +839,7 @@ def run_ssd(args):
         "kernel_timing": "per-kernel CUDA events over a second run of the same K steps after "
                          "the timed region (none inside it)",
         "clocks": clk,
+        "device": torch.cuda.get_device_name(dev),
         "status": ra.STATUS.get(status, status),
     }
     emit(line)
