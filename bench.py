@@ -780,19 +780,29 @@ def run_ssd(args):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
     cpu = None
+    parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         heads = max(1, min(w.heads, int(args.cpu_budget * 2)))  # about 0.5 s per head
         t_c = time.perf_counter()
-        oracle.ssd_scan(inp["x"][:, :heads], inp["dt"][:, :heads], inp["A"][:heads],
-                        inp["B"][:, :1], inp["C"][:, :1], inp["D"][:heads],
-                        inp["position_ids"])
+        ry, _ = oracle.ssd_scan(inp["x"][:, :heads], inp["dt"][:, :heads], inp["A"][:heads],
+                                inp["B"][:, :1], inp["C"][:, :1], inp["D"][:heads],
+                                inp["position_ids"])
         dt_c = time.perf_counter() - t_c
         cpu = {"value": round(ssd_flops(w.total_tokens, heads, w.head_dim, w.state_dim) /
                               dt_c / 1e12, 6),
                "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
                "sample": f"{heads} of {w.heads} heads over all {w.total_tokens} tokens, fp64, "
                          f"{dt_c:.1f} s"}
+        # the sample's heads of group 0 (the timed call reads group 0's B and C
+        # for every head) against this run's y, at the tests' 2e-5 relative bound
+        g0 = min(heads, w.heads // w.groups)
+        ref = np.asarray(ry)[:, :g0]
+        got = y[:, :g0].double().cpu().numpy()
+        scale = max(1.0, float(np.max(np.abs(ref))))
+        rel = float(np.max(np.abs(got - ref))) / scale
+        parity = {"heads": g0, "tokens": w.total_tokens, "y_rel": rel,
+                  "within_bounds": rel <= 2e-5}
     if rank != 0:
         return
     f = ssd_flops(w.total_tokens, w.heads, w.head_dim, w.state_dim)
@@ -827,6 +837,7 @@ def run_ssd(args):
                      "recurrence_flops_per_launch": f},
         "kernels": ktab,
         "cpu_baseline": cpu,
+        "parity_sample": parity,
         "e2e": {"value": round(world * f / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": h_y.numel() * 4 + h_s.numel() * 4,
